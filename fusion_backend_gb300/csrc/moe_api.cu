@@ -1,0 +1,287 @@
+// C ABI of the fused MoE FFN layer: plan, validation, workspace layout and
+// launches.  See include/moe_ffn.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <new>
+
+#include "../../include/moe_ffn.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0x4D6F4546u;  // "MoEF"
+constexpr int kMaxDevices = 64;
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t ctrl, logits, h, hsh, counts, offsets, perm, active, nactive, total;
+};
+
+}  // namespace
+
+struct moe_ffn_plan {
+  uint32_t magic;
+  moe_ffn_shapes s;
+  int act, wfmt;
+  int path;  // 0 decode
+  WsLayout ws;
+};
+
+namespace {
+
+struct DeviceInfo {
+  std::atomic<int> ready{0};
+  int sm_count = 0;
+  int smem_optin = 0;
+  int major = 0, minor = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Device properties are read once per device, lazily on the first execute
+// (prepare never touches the device).
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_FFN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_FFN_ERR_DEVICE;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_FFN_ERR_CUDA;
+      d.ready.store(1, std::memory_order_release);
+    }
+  }
+  if (d.major != 10 || d.minor != 3) return MOE_FFN_ERR_DEVICE;
+  *out = &d;
+  return MOE_FFN_OK;
+}
+
+long long matrix_bytes(int wfmt, long long rows, long long cols) {
+  return wfmt == MOE_FFN_W_BF16 ? rows * cols * 2 : rows * (cols * 9 / 16);
+}
+int row_bytes(int wfmt, int cols) { return wfmt == MOE_FFN_W_BF16 ? cols * 2 : cols * 9 / 16; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_plan(const moe_ffn_plan* p) { return p && p->magic == kPlanMagic; }
+
+void fill_decode_params(const moe_ffn_plan* plan, DecodeParams& P, void* ws) {
+  memset(&P, 0, sizeof(P));
+  const moe_ffn_shapes& s = plan->s;
+  P.T = s.T;
+  P.H = s.H;
+  P.E = s.E;
+  P.K = s.top_k;
+  P.I = s.I;
+  P.Is = s.Is;
+  P.act = plan->act;
+  P.wfmt = plan->wfmt;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  P.ctrl = reinterpret_cast<uint32_t*>(w + plan->ws.ctrl);
+  P.logits = reinterpret_cast<float*>(w + plan->ws.logits);
+  P.h = reinterpret_cast<float*>(w + plan->ws.h);
+  P.hsh = reinterpret_cast<float*>(w + plan->ws.hsh);
+  P.r_counts = reinterpret_cast<int32_t*>(w + plan->ws.counts);
+  P.r_offsets = reinterpret_cast<int32_t*>(w + plan->ws.offsets);
+  P.r_perm = reinterpret_cast<int32_t*>(w + plan->ws.perm);
+  P.r_active = reinterpret_cast<int32_t*>(w + plan->ws.active);
+  P.r_nactive = reinterpret_cast<int32_t*>(w + plan->ws.nactive);
+  P.expert_bytes = 2 * matrix_bytes(plan->wfmt, s.I, s.H) + matrix_bytes(plan->wfmt, s.H, s.I);
+  P.gu_bytes = matrix_bytes(plan->wfmt, s.I, s.H);
+  P.sgu_bytes = matrix_bytes(plan->wfmt, s.Is, s.H);
+  P.rbH = row_bytes(plan->wfmt, s.H);
+  P.rbI = row_bytes(plan->wfmt, s.I);
+  P.rbIs = row_bytes(plan->wfmt, s.Is);
+}
+
+int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes, const void* x,
+        const void* router_w, const void* expert_w, const void* shexp_w, const void* shexp_gate_w, float* out,
+        int32_t* topk_ids, float* topk_w, int block_mode, float eps) {
+  if (!valid_plan(plan)) return MOE_FFN_ERR_INVALID_ARG;
+  if (!workspace || !x || !router_w || !expert_w || !shexp_w || !shexp_gate_w || !out)
+    return MOE_FFN_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws.total) return MOE_FFN_ERR_WORKSPACE;
+  if (!aligned(workspace, 256) || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(expert_w, 16) ||
+      !aligned(shexp_w, 16) || !aligned(shexp_gate_w, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
+      !aligned(topk_w, 4))
+    return MOE_FFN_ERR_MISALIGNED;
+  if (block_mode && (plan->act != MOE_FFN_ACT_BF16 || plan->path != 0)) return MOE_FFN_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != MOE_FFN_OK) return rc;
+
+  DecodeParams P;
+  fill_decode_params(plan, P, workspace);
+  P.x = x;
+  P.router_w = static_cast<const uint16_t*>(router_w);
+  P.gate_w = static_cast<const uint16_t*>(shexp_gate_w);
+  P.expert_w = static_cast<const uint8_t*>(expert_w);
+  P.shexp_w = static_cast<const uint8_t*>(shexp_w);
+  P.out = out;
+  P.topk_ids = topk_ids;
+  P.topk_w = topk_w;
+  P.block_mode = block_mode;
+  P.eps = eps;
+  P.G = dev->sm_count;
+  if (decode_smem_layout(P, dev->smem_optin) < 0) return MOE_FFN_ERR_UNSUPPORTED;
+  cudaError_t err = launch_decode(P, reinterpret_cast<cudaStream_t>(stream), true);
+  return err == cudaSuccess ? MOE_FFN_OK : MOE_FFN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_plan_t* plan,
+                    size_t* workspace_bytes) {
+  if (!shapes || !plan || !workspace_bytes) return MOE_FFN_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const moe_ffn_shapes s = *shapes;
+  if (dtype.act != MOE_FFN_ACT_F32 && dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_INVALID_ARG;
+  if (dtype.wfmt != MOE_FFN_W_BF16 && dtype.wfmt != MOE_FFN_W_Q4B32) return MOE_FFN_ERR_INVALID_ARG;
+  if (s.T < 1 || s.T > 256 || s.E < 1 || s.E > kMaxExperts || s.top_k < 1 || s.top_k > s.E ||
+      s.top_k > kMaxTopK || s.H < 1 || s.I < 1 || s.Is < 1)
+    return MOE_FFN_ERR_UNSUPPORTED;
+  const int mult = dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256;
+  if (s.H % mult || s.I % mult || s.Is % mult) return MOE_FFN_ERR_UNSUPPORTED;
+  if (s.H > (1 << 20) || s.I > (1 << 20) || s.Is > (1 << 20)) return MOE_FFN_ERR_UNSUPPORTED;
+  // Decode path limits: T <= 8, one gate+up row pair and one down row per ring stage.
+  if (s.T > kDecodeMaxT) return MOE_FFN_ERR_UNSUPPORTED;
+  if (2 * row_bytes(dtype.wfmt, s.H) > kStageBytes || row_bytes(dtype.wfmt, s.I) > kStageBytes ||
+      row_bytes(dtype.wfmt, s.Is) > kStageBytes)
+    return MOE_FFN_ERR_UNSUPPORTED;
+
+  moe_ffn_plan* p = new (std::nothrow) moe_ffn_plan();
+  if (!p) return MOE_FFN_ERR_INVALID_ARG;
+  p->magic = kPlanMagic;
+  p->s = s;
+  p->act = dtype.act;
+  p->wfmt = dtype.wfmt;
+  p->path = 0;
+  size_t off = 0;
+  WsLayout& L = p->ws;
+  const size_t T = s.T, E = s.E, K = s.top_k;
+  L.ctrl = off;
+  off = align256(off + kCtrlWords * 4);
+  L.logits = off;
+  off = align256(off + T * (E + 1) * 4);
+  L.h = off;
+  off = align256(off + T * K * (size_t)s.I * 4);
+  L.hsh = off;
+  off = align256(off + T * (size_t)s.Is * 4);
+  L.counts = off;
+  off = align256(off + E * 4);
+  L.offsets = off;
+  off = align256(off + (E + 1) * 4);
+  L.perm = off;
+  off = align256(off + T * K * 4);
+  L.active = off;
+  off = align256(off + E * 4);
+  L.nactive = off;
+  off = align256(off + 4);
+  L.total = off;
+  *plan = p;
+  *workspace_bytes = off;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_execute(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                    const void* x, const void* router_w, const void* expert_w, const void* shexp_w,
+                    const void* shexp_gate_w, float* out) {
+  return run(plan, stream, workspace, workspace_bytes, x, router_w, expert_w, shexp_w, shexp_gate_w, out, nullptr,
+             nullptr, 0, 0.f);
+}
+
+int moe_ffn_execute_ex(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                       const void* x, const void* router_w, const void* expert_w, const void* shexp_w,
+                       const void* shexp_gate_w, float* out, int32_t* topk_ids, float* topk_w) {
+  return run(plan, stream, workspace, workspace_bytes, x, router_w, expert_w, shexp_w, shexp_gate_w, out, topk_ids,
+             topk_w, 0, 0.f);
+}
+
+int moe_ffn_execute_block(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                          float* x_res, const void* router_w, const void* expert_w, const void* shexp_w,
+                          const void* shexp_gate_w, float eps, int32_t* topk_ids, float* topk_w) {
+  if (!(eps >= 0.f)) return MOE_FFN_ERR_INVALID_ARG;
+  return run(plan, stream, workspace, workspace_bytes, x_res, router_w, expert_w, shexp_w, shexp_gate_w, x_res,
+             topk_ids, topk_w, 1, eps);
+}
+
+int moe_ffn_read_status(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stream_t stream,
+                        int32_t* device_status) {
+  if (!valid_plan(plan) || !workspace || !device_status) return MOE_FFN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_FFN_ERR_CUDA;
+  const uint8_t* w = static_cast<const uint8_t*>(workspace);
+  if (cudaMemcpy(device_status, w + plan->ws.ctrl + kCtrlStatus * 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_FFN_ERR_CUDA;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stream_t stream, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* active, int32_t* num_active) {
+  if (!valid_plan(plan) || !workspace || !counts || !offsets || !perm || !active || !num_active)
+    return MOE_FFN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_FFN_ERR_CUDA;
+  const uint8_t* w = static_cast<const uint8_t*>(workspace);
+  const size_t E = plan->s.E, TK = (size_t)plan->s.T * plan->s.top_k;
+  int32_t n = 0;
+  if (cudaMemcpy(&n, w + plan->ws.nactive, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_FFN_ERR_CUDA;
+  if (n < 0 || (size_t)n > E) n = 0;
+  if (cudaMemcpy(counts, w + plan->ws.counts, E * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(offsets, w + plan->ws.offsets, (E + 1) * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(perm, w + plan->ws.perm, TK * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      (n > 0 && cudaMemcpy(active, w + plan->ws.active, (size_t)n * 4, cudaMemcpyDeviceToHost) != cudaSuccess))
+    return MOE_FFN_ERR_CUDA;
+  *num_active = n;
+  return MOE_FFN_OK;
+}
+
+int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value) {
+  if (!valid_plan(plan) || !value) return MOE_FFN_ERR_INVALID_ARG;
+  switch (what) {
+    case MOE_FFN_QUERY_PATH:
+      *value = plan->path;
+      return MOE_FFN_OK;
+    case MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE:
+      *value = decode_kernel_count();
+      return MOE_FFN_OK;
+    default:
+      return MOE_FFN_ERR_INVALID_ARG;
+  }
+}
+
+void moe_ffn_destroy(moe_ffn_plan_t plan) {
+  if (!valid_plan(plan)) return;
+  plan->magic = 0;
+  delete plan;
+}
+
+const char* moe_ffn_strerror(int status) {
+  switch (status) {
+    case MOE_FFN_OK: return "ok";
+    case MOE_FFN_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_FFN_ERR_UNSUPPORTED: return "unsupported shapes or dtype";
+    case MOE_FFN_ERR_WORKSPACE: return "workspace too small";
+    case MOE_FFN_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_FFN_ERR_CUDA: return "CUDA error";
+    case MOE_FFN_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case MOE_FFN_ERR_DEVICE: return "unsupported device (needs sm_103)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+/*
+ * moe_ffn.h -- C ABI of the fused mixture-of-experts FFN layer for GB300
+ * (sm_103a), one GPU.
+ *
+ * The layer is the one named in "ggml-cuda: overlap the MoE shared expert on
+ * a separate stream" (ROCm/llama.cpp PR #36, "What this changes"): a router,
+ * top-k routed SwiGLU experts and a gated shared expert forked from the same
+ * FFN input and joined by add(ffn_moe_out, ffn_shexp), in the small-batch
+ * (decode) mat-vec regime.  Here the two branches are one fused operator;
+ * nothing is overlapped across CUDA streams.
+ *
+ * Per token t (x_t is one row of x):
+ *   logit[e] = sum_h router_w[e,h] x_t[h]                        (fp32)
+ *   ids      = the top_k largest logits, larger first, equal logits ordered
+ *              by the lower expert index
+ *   p_j      = exp(logit[ids_j] - logit[ids_0]) / sum_i exp(logit[ids_i] - logit[ids_0])
+ *              (softmax over all experts followed by renormalisation of the
+ *              kept top_k: the same numbers)
+ *   s        = sigmoid(sum_h shexp_gate_w[h] x_t[h])
+ *   FFN(x)   = down( silu(gate x) * (up x) ),  silu(z) = z / (1 + exp(-z))
+ *   out_t    = sum_{j=0..top_k-1} p_j FFN_{ids_j}(x_t)  +  s FFN_shared(x_t)
+ * The routed sum runs in rank order and the shared term is added last.  GPU
+ * results are bitwise reproducible run to run (no floating-point atomics).
+ *
+ * The lifecycle follows the prepare / execute / destroy contract of the
+ * "ggml operator extensions" page (stable-diffusion.cpp docs/ggml_extensions.md,
+ * sections "Kernel selection" and "CUDA kernels can opt into device replay"):
+ *   - prepare is host-only: it validates shapes, builds an immutable plan and
+ *     reports the workspace size.  It launches nothing and allocates no
+ *     device memory.
+ *   - execute enqueues device work on the caller's stream only.  It makes no
+ *     host decision based on tensor contents and never synchronises, so it
+ *     can be captured in a CUDA graph and replayed.  Every counter and flag
+ *     in the workspace is initialised by the recorded device work of each
+ *     call; workspace contents are not preserved between calls.  An error is
+ *     returned, never retried.
+ *   - destroy frees the host plan only.
+ *
+ * Ownership: the caller owns every tensor and the workspace.  The library
+ * keeps no pointer beyond a call.  One plan may be executed concurrently on
+ * several streams when each call has its own workspace.
+ *
+ * All functions return MOE_FFN_OK (0) or a negative moe_ffn_status.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* moe_ffn_stream_t;
+
+typedef enum {
+  MOE_FFN_OK = 0,
+  MOE_FFN_ERR_INVALID_ARG = -1, /* null required pointer, null plan, bad enum */
+  MOE_FFN_ERR_UNSUPPORTED = -2, /* shapes or dtype outside the supported set (see moe_ffn_prepare) */
+  MOE_FFN_ERR_WORKSPACE = -3,   /* workspace_bytes smaller than prepare reported */
+  MOE_FFN_ERR_MISALIGNED = -4,  /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  MOE_FFN_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  MOE_FFN_ERR_TIMEOUT = -6,     /* device status only: a bounded in-kernel wait gave up */
+  MOE_FFN_ERR_DEVICE = -7       /* the current device is not sm_103 (GB300) or lacks a needed feature */
+} moe_ffn_status;
+
+/* T tokens, hidden size H, E experts, top_k kept per token, expert
+ * intermediate size I, shared-expert intermediate size Is. */
+typedef struct {
+  int32_t T, H, E, top_k, I, Is;
+} moe_ffn_shapes;
+
+typedef enum { MOE_FFN_ACT_F32 = 0, MOE_FFN_ACT_BF16 = 1 } moe_ffn_act_dtype;
+
+/* Weight format of the routed experts and of the shared expert.  The router
+ * and the shared-gate vector are bf16 in both formats. */
+typedef enum {
+  MOE_FFN_W_BF16 = 0,
+  /* 4-bit blocks of 32 along each row (the reduction dimension): one fp16
+   * scale d per block and 4-bit codes n in 0..15 with weight = d * (n - 8).
+   * Row layout: C/2 bytes of codes (element 2j in the low nibble of byte j,
+   * element 2j+1 in the high nibble), then C/32 little-endian fp16 scales;
+   * 9*C/16 bytes per row of C elements. */
+  MOE_FFN_W_Q4B32 = 1
+} moe_ffn_weight_format;
+
+typedef struct {
+  int32_t act;  /* moe_ffn_act_dtype: dtype of x */
+  int32_t wfmt; /* moe_ffn_weight_format */
+} moe_ffn_dtype;
+
+typedef struct moe_ffn_plan* moe_ffn_plan_t;
+
+/*
+ * Validate `shapes` and `dtype`, build a plan and report the workspace size.
+ * Host only: no device call, no launch, no device allocation.
+ * Supported:
+ *   1 <= T <= 256; 1 <= E <= 1024; 1 <= top_k <= min(E, 32); H, I, Is >= 1;
+ *   bf16 weights: H, I, Is multiples of 8 (16-byte rows);
+ *   4-bit weights: H, I, Is multiples of 256 (16-byte rows in the 4-bit
+ *   layout) and T <= 8 (the grouped-GEMM regime is bf16 only);
+ *   x fp32 or bf16.
+ * Tokens T <= 8 take the decode path (router kernel + persistent expert
+ * kernel); larger T take the tensor-core grouped-GEMM path.
+ * Returns MOE_FFN_ERR_UNSUPPORTED otherwise, MOE_FFN_ERR_INVALID_ARG for null
+ * pointers.  On success *plan is owned by the caller (moe_ffn_destroy).
+ */
+int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_plan_t* plan,
+                    size_t* workspace_bytes);
+
+/*
+ * Enqueue the layer on `stream` (the current device must be a GB300).
+ * Device pointers, all caller-owned:
+ *   workspace     >= workspace_bytes from prepare, 256-byte aligned, scratch
+ *   x             [T,H] fp32 or bf16 (plan dtype), row-major
+ *   router_w      bf16 [E,H]
+ *   expert_w      E consecutive blocks, block e = gate[I,H] | up[I,H] | down[H,I]
+ *                 in the plan's weight format (each matrix row-major [out,in])
+ *   shexp_w       gate[Is,H] | up[Is,H] | down[H,Is]
+ *   shexp_gate_w  bf16 [H]
+ *   out           fp32 [T,H]; may alias x exactly (the layer reads all of x
+ *                 before it writes out); any other overlap is undefined.
+ * Every pointer must be 16-byte aligned.  Returns without synchronising.
+ */
+int moe_ffn_execute(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                    const void* x, const void* router_w, const void* expert_w, const void* shexp_w,
+                    const void* shexp_gate_w, float* out);
+
+/*
+ * moe_ffn_execute, and also write the routing: topk_ids int32 [T,top_k] and
+ * topk_w fp32 [T,top_k] in rank order (either may be NULL).
+ */
+int moe_ffn_execute_ex(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                       const void* x, const void* router_w, const void* expert_w, const void* shexp_w,
+                       const void* shexp_gate_w, float* out, int32_t* topk_ids, float* topk_w);
+
+/*
+ * Pre-norm transformer-block form (one layer of a decode stack):
+ *   xn = bf16( x_res / sqrt(mean(x_res^2) + eps) )      (RMSNorm, weight 1)
+ *   x_res <- x_res + layer(xn)
+ * with the layer output and the residual add rounded to fp32 separately.
+ * x_res is fp32 [T,H], read and updated in place.  The plan must have been
+ * prepared with act = MOE_FFN_ACT_BF16 (the layer sees the bf16 xn) and
+ * T <= 8.  topk_ids / topk_w as in moe_ffn_execute_ex (may be NULL).  Other
+ * arguments as moe_ffn_execute; eps >= 0 or MOE_FFN_ERR_INVALID_ARG.
+ */
+int moe_ffn_execute_block(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                          float* x_res, const void* router_w, const void* expert_w, const void* shexp_w,
+                          const void* shexp_gate_w, float eps, int32_t* topk_ids, float* topk_w);
+
+/*
+ * Test/debug: synchronise `stream`, then copy the device status word of the
+ * last execute that used `workspace` (MOE_FFN_OK or MOE_FFN_ERR_TIMEOUT) to
+ * *device_status.  Returns a host-side status.
+ */
+int moe_ffn_read_status(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stream_t stream,
+                        int32_t* device_status);
+
+/*
+ * Test/debug: synchronise `stream`, then copy the token -> expert bucketing
+ * of the last execute that used `workspace` to host arrays:
+ *   counts [E]      tokens routed to each expert
+ *   offsets [E+1]   exclusive prefix sum of counts
+ *   perm [T*top_k]  flat (t*top_k + j) indices grouped by ascending expert,
+ *                   token-major inside a group (a stable counting sort)
+ *   active [E]      experts with counts > 0, ascending; *num_active of them
+ */
+int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stream_t stream, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* active, int32_t* num_active);
+
+/* Queries on a plan. */
+typedef enum {
+  MOE_FFN_QUERY_PATH = 0,                /* 0 = decode, 1 = grouped GEMM */
+  MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE = 1 /* kernels one execute launches */
+} moe_ffn_query_t;
+int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value);
+
+/* Free a plan (host memory only).  NULL is ignored. */
+void moe_ffn_destroy(moe_ffn_plan_t plan);
+
+/* Static text for a status code. */
+const char* moe_ffn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

@@ -1,0 +1,91 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+validates shapes in prepare (no GPU needed) and reports errors."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import datagen
+import fusion_backend_gb300 as fb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fb.build()
+    return fb.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_ffn_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(fb.EXPORTS)
+
+
+def test_prepare_reports_workspace_without_device(lib):
+    plan, ws = fb.moe_ffn_prepare(datagen.Shapes(1, 2048, 128, 8, 768, 512), fb.ACT_BF16, fb.W_BF16)
+    assert ws > 0 and ws % 256 == 0
+    assert fb.moe_ffn_query(plan, fb.QUERY_PATH) == 0
+    assert fb.moe_ffn_query(plan, fb.QUERY_LAUNCHES_PER_EXECUTE) == 2
+    fb.moe_ffn_destroy(plan)
+
+
+@pytest.mark.parametrize(
+    "shapes,wfmt",
+    [
+        (datagen.Shapes(0, 256, 8, 2, 128, 256), fb.W_BF16),      # T = 0
+        (datagen.Shapes(1, 260, 8, 2, 128, 256), fb.W_BF16),      # H not a multiple of 8
+        (datagen.Shapes(1, 256, 8, 9, 128, 256), fb.W_BF16),      # top_k > E
+        (datagen.Shapes(1, 256, 40, 33, 128, 256), fb.W_BF16),    # top_k > 32
+        (datagen.Shapes(1, 256, 2000, 2, 128, 256), fb.W_BF16),   # E > 1024
+        (datagen.Shapes(1, 256, 8, 2, 128, 256), fb.W_Q4B32),     # 4-bit needs multiples of 256
+        (datagen.Shapes(1, 16384, 8, 2, 128, 256), fb.W_BF16),    # a gate+up row pair exceeds a ring stage
+    ],
+)
+def test_prepare_rejects_unsupported(lib, shapes, wfmt):
+    with pytest.raises(fb.MoeFFNError) as e:
+        fb.moe_ffn_prepare(shapes, fb.ACT_BF16, wfmt)
+    assert e.value.status == fb.ERR_UNSUPPORTED
+
+
+def test_prepare_rejects_bad_enums_and_nulls(lib):
+    s = fb.Shapes(1, 256, 8, 2, 128, 256)
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.moe_ffn_prepare(ctypes.byref(s), fb.DType(5, 0), ctypes.byref(plan), ctypes.byref(ws)) == fb.ERR_INVALID_ARG
+    assert lib.moe_ffn_prepare(ctypes.byref(s), fb.DType(0, 7), ctypes.byref(plan), ctypes.byref(ws)) == fb.ERR_INVALID_ARG
+    assert lib.moe_ffn_prepare(None, fb.DType(0, 0), ctypes.byref(plan), ctypes.byref(ws)) == fb.ERR_INVALID_ARG
+
+
+def test_execute_argument_errors_before_any_device_call(lib):
+    plan, ws = fb.moe_ffn_prepare(datagen.Shapes(1, 256, 8, 2, 128, 256), fb.ACT_F32, fb.W_BF16)
+    fake = 1 << 20  # aligned, never dereferenced: validation fails first
+    # null plan / null pointers
+    assert lib.moe_ffn_execute(None, None, fake, ws, fake, fake, fake, fake, fake, fake) == fb.ERR_INVALID_ARG
+    assert lib.moe_ffn_execute(plan, None, fake, ws, None, fake, fake, fake, fake, fake) == fb.ERR_INVALID_ARG
+    # workspace too small
+    assert lib.moe_ffn_execute(plan, None, fake, ws - 1, fake, fake, fake, fake, fake, fake) == fb.ERR_WORKSPACE
+    # misaligned
+    assert lib.moe_ffn_execute(plan, None, fake + 8, ws, fake, fake, fake, fake, fake, fake) == fb.ERR_MISALIGNED
+    assert lib.moe_ffn_execute(plan, None, fake, ws, fake + 4, fake, fake, fake, fake, fake) == fb.ERR_MISALIGNED
+    # block form needs a bf16-activation plan
+    assert lib.moe_ffn_execute_block(plan, None, fake, ws, fake, fake, fake, fake, fake, 1e-6, None, None) == fb.ERR_UNSUPPORTED
+    assert lib.moe_ffn_execute_block(plan, None, fake, ws, fake, fake, fake, fake, fake, -1.0, None, None) == fb.ERR_INVALID_ARG
+    fb.moe_ffn_destroy(plan)
+
+
+def test_strerror_covers_codes(lib):
+    for code in range(0, -8, -1):
+        assert fb.strerror(code) != "unknown status"
+    assert fb.strerror(-99) == "unknown status"
