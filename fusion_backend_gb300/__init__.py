@@ -45,7 +45,10 @@ EXPORTS = (
     "moe_ffn_query",
     "moe_ffn_destroy",
     "moe_ffn_strerror",
+    "moe_ffn_execute_static_scratch",
 )
+
+STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class MoeFFNError(RuntimeError):
@@ -93,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.moe_ffn_query.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
         L.moe_ffn_destroy.restype = None
         L.moe_ffn_destroy.argtypes = [vp]
+        L.moe_ffn_execute_static_scratch.restype = ctypes.c_int
+        L.moe_ffn_execute_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_ffn_strerror.restype = ctypes.c_char_p
         L.moe_ffn_strerror.argtypes = [ctypes.c_int]
         _lib = L
@@ -194,6 +199,15 @@ def moe_ffn_query(plan, what: int) -> int:
 def moe_ffn_destroy(plan) -> None:
     if plan:
         lib().moe_ffn_destroy(plan)
+
+
+def moe_ffn_execute_static_scratch(plan, x, router_w, expert_w, shexp_w, shexp_gate_w, out, stream=None):
+    """moe_ffn_execute without a workspace: the scratch is the library's own
+    device array (STATIC_SCRATCH_BYTES).  Allocates nothing.  Calls that overlap
+    on the GPU share that array and race; serialise them."""
+    _check(lib().moe_ffn_execute_static_scratch(plan, _stream(stream), _ptr(x), _ptr(router_w), _ptr(expert_w),
+                                                _ptr(shexp_w), _ptr(shexp_gate_w), _ptr(out)),
+           "moe_ffn_execute_static_scratch")
 
 
 def moe_ffn_strerror(status: int) -> str:

@@ -285,3 +285,47 @@ const char* moe_ffn_strerror(int status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the scratch lives in a file-scope device array
+// instead of a caller-provided workspace (see moe_ffn.h).
+namespace {
+
+// Scratch of moe_ffn_execute_static_scratch, shared by every call on a device.
+// Every GPU that loads this library holds these bytes until the process exits.
+__device__ __align__(256) uint8_t g_static_scratch[MOE_FFN_STATIC_SCRATCH_BYTES];
+
+void* g_static_scratch_addr[kMaxDevices];
+std::mutex g_static_scratch_mu;
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the host-side symbol is only a stand-in for it).
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_FFN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_FFN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_FFN_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return MOE_FFN_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream, const void* x,
+                                              const void* router_w, const void* expert_w, const void* shexp_w,
+                                              const void* shexp_gate_w, float* out) {
+  if (!valid_plan(plan)) return MOE_FFN_ERR_INVALID_ARG;
+  if (plan->ws.total > (size_t)MOE_FFN_STATIC_SCRATCH_BYTES) return MOE_FFN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = static_scratch_address(&scratch);
+  if (rc != MOE_FFN_OK) return rc;
+  // The kernels initialise every control word they read in each call, so no
+  // part of the (shared, reused) array has to be cleared here.
+  return run(plan, stream, scratch, MOE_FFN_STATIC_SCRATCH_BYTES, x, router_w, expert_w, shexp_w, shexp_gate_w, out,
+             nullptr, nullptr, 0, 0.f);
+}

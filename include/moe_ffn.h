@@ -170,6 +170,33 @@ int moe_ffn_read_status(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stre
 int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stream_t stream, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* active, int32_t* num_active);
 
+/*
+ * Allocation-free variant of moe_ffn_execute, for callers that cannot
+ * allocate device memory: for example a library embedded in a runtime that
+ * has already handed all free device memory to its own pool (an inference
+ * server that reserves the memory for its caches at start-up), or a plugin
+ * given no allocator and no workspace.  This entry point has no counterpart
+ * on the pages the layer is built from; it is an addition of this library.
+ *
+ * The scratch lives in one file-scope __device__ array of
+ * MOE_FFN_STATIC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  The caller still passes
+ * inputs and output exactly as for moe_ffn_execute.  Plans whose workspace is
+ * larger than the array are rejected with MOE_FFN_ERR_WORKSPACE (the decode
+ * shapes of one token batch, e.g. T <= 8, H = 2048, E = 128, top_k = 8,
+ * I = 768, fit).  No cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array and the kernels re-initialise what they read in each call, but
+ * calls whose work overlaps on the GPU (other streams, or graphs replayed
+ * concurrently) race on the array and give undefined results: serialise them.
+ */
+#define MOE_FFN_STATIC_SCRATCH_BYTES (1 << 20)
+int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream, const void* x, const void* router_w,
+                                   const void* expert_w, const void* shexp_w, const void* shexp_gate_w, float* out);
+
 /* Queries on a plan. */
 typedef enum {
   MOE_FFN_QUERY_PATH = 0,                /* 0 = decode, 1 = grouped GEMM */
