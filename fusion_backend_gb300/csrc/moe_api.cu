@@ -8,7 +8,7 @@
 #include <mutex>
 #include <new>
 
-#include "../../include/moe_ffn.h"
+#include "moe_ffn.h"
 #include "moe_internal.h"
 
 using namespace moe;
@@ -91,6 +91,7 @@ void fill_decode_params(const moe_ffn_plan* plan, DecodeParams& P, void* ws) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   P.ctrl = reinterpret_cast<uint32_t*>(w + plan->ws.ctrl);
   P.logits = reinterpret_cast<float*>(w + plan->ws.logits);
+  P.ls = (s.E + 1 + 3) / 4 * 4;
   P.h = reinterpret_cast<float*>(w + plan->ws.h);
   P.hsh = reinterpret_cast<float*>(w + plan->ws.hsh);
   P.r_counts = reinterpret_cast<int32_t*>(w + plan->ws.counts);
@@ -135,8 +136,17 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   P.block_mode = block_mode;
   P.eps = eps;
   P.G = dev->sm_count;
-  if (decode_smem_layout(P, dev->smem_optin) < 0) return MOE_FFN_ERR_UNSUPPORTED;
-  cudaError_t err = launch_decode(P, reinterpret_cast<cudaStream_t>(stream), true);
+  cudaError_t err;
+  // Fast path (per-warp rings) when the shapes fit it; the 4-bit fast path
+  // forms products in fp16, so it takes bf16 activations (or the block form,
+  // whose normalised input is bf16).  Otherwise the general kernel.
+  const bool fast_ok = plan->wfmt == MOE_FFN_W_BF16 || plan->act == MOE_FFN_ACT_BF16;
+  if (fast_ok && decode_v2_layout(P, dev->smem_optin) >= 0) {
+    err = launch_decode_v2(P, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    if (decode_smem_layout(P, dev->smem_optin) < 0) return MOE_FFN_ERR_UNSUPPORTED;
+    err = launch_decode(P, reinterpret_cast<cudaStream_t>(stream), true);
+  }
   return err == cudaSuccess ? MOE_FFN_OK : MOE_FFN_ERR_CUDA;
 }
 
@@ -176,7 +186,7 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   L.ctrl = off;
   off = align256(off + kCtrlWords * 4);
   L.logits = off;
-  off = align256(off + T * (E + 1) * 4);
+  off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
   L.h = off;
   off = align256(off + T * K * (size_t)s.I * 4);
   L.hsh = off;

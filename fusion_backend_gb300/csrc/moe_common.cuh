@@ -60,6 +60,11 @@ MOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Bulk prefetch of [src, src + bytes) into L2 (hint only; src 16-byte aligned,
+// bytes a multiple of 16).
+MOE_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 MOE_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -73,6 +78,8 @@ MOE_DEV uint64_t policy_evict_last() {
 // Order this thread's earlier generic-proxy global accesses (and the ones it
 // acquired) before its later async-proxy (bulk copy) accesses.
 MOE_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// The same for all state spaces (global and shared).
+MOE_DEV void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // -------------------------------------------- programmatic dependent launch
 MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -32,13 +32,11 @@
 
 #include <algorithm>
 
-#include "moe_common.cuh"
-#include "moe_internal.h"
+#include "moe_decode_common.cuh"
 
 namespace moe {
 
 namespace {
-
 constexpr int kBarCons = 1;   // named barrier: the 256 consumer threads
 constexpr int kBarRoute = 2;  // named barrier: all threads of the CTA
 constexpr int kConsThreads = kNumConsumerWarps * 32;
@@ -68,7 +66,6 @@ struct Item {
   bool first, last;  // first / last item of its down group
 };
 
-MOE_DEV int div_floor_ll(long long a, long long b) { return static_cast<int>(a / b); }
 
 MOE_DEV int cap_gu(const DecodeParams& P) { return min(kMaxGuRows, kStageBytes / (2 * P.rbH)); }
 MOE_DEV int cap_dn(int rb) { return min(kMaxDownRows, kStageBytes / rb); }
@@ -93,10 +90,6 @@ MOE_DEV void walk_routed_gu(const DecodeParams& P, int c, int U, F&& f) {
   }
 }
 
-MOE_DEV void down_rows(const DecodeParams& P, int c, int& a, int& b) {
-  a = div_floor_ll((long long)P.H * c, P.G);
-  b = div_floor_ll((long long)P.H * (c + 1), P.G);
-}
 
 template <class F>
 MOE_DEV void walk_down(const DecodeParams& P, int c, int U, F&& f) {
@@ -109,181 +102,10 @@ MOE_DEV void walk_down(const DecodeParams& P, int c, int U, F&& f) {
     for (int r = a; r < b; r += cr) f(Item{3, u, r, min(cr, b - r), 1 + u, r == a, r + cr >= b});
 }
 
-// -------------------------------------------------------------- reductions
-MOE_DEV float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Butterfly reduction of a (sum, compensation) pair; every lane ends with
-// the same bits because TwoSum is symmetric in its operands.
-MOE_DEV void warp_sum2(float& s, float& c) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float so = __shfl_xor_sync(0xffffffffu, s, o);
-    const float co = __shfl_xor_sync(0xffffffffu, c, o);
-    float t, e;
-    two_sum(s, so, t, e);
-    s = t;
-    c = __fadd_rn(__fadd_rn(c, co), e);
-  }
-}
-
-// RMSNorm factor of one fp32 row: inv = 1/sqrt(mean(x^2) + eps), computed
-// from an error-free sum of squares and returned as hi + lo floats.  All
-// lanes of the warp return the same value.
-MOE_DEV void warp_norm_factor(const float* row, int H, float eps, float& hi, float& lo) {
-  const int lane = threadIdx.x & 31;
-  float s = 0.f, c = 0.f;
-  for (int h = lane; h < H; h += 32) {
-    const float v = row[h];
-    float p, e1, t, e2;
-    two_prod(v, v, p, e1);
-    two_sum(s, p, t, e2);
-    s = t;
-    c = __fadd_rn(c, __fadd_rn(e1, e2));
-  }
-  warp_sum2(s, c);
-  const double ss = (double)s + (double)c;
-  const double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
-  hi = (float)inv;
-  lo = (float)(inv - (double)hi);
-}
-
-// bf16(fp32(x * inv)) for the pre-norm block form, inv given as hi + lo.
-MOE_DEV float norm_apply(float x, float hi, float lo) {
-  float p, e;
-  two_prod(x, hi, p, e);
-  const float r = __fadd_rn(p, __fmaf_rn(x, lo, e));
-  return bf16_to_float(float_to_bf16_rne(r));
-}
-
-// Eight activations of token t starting at column c0 (c0 % 8 == 0).
-MOE_DEV void load_x8(const DecodeParams& P, const Tabs& tb, int t, int c0, float* xf) {
-  if (P.block_mode) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(P.x) + (size_t)t * P.H + c0);
-    const float4 a = src[0], b = src[1];
-    const float hi = tb.inv[t][0], lo = tb.inv[t][1];
-    xf[0] = norm_apply(a.x, hi, lo); xf[1] = norm_apply(a.y, hi, lo);
-    xf[2] = norm_apply(a.z, hi, lo); xf[3] = norm_apply(a.w, hi, lo);
-    xf[4] = norm_apply(b.x, hi, lo); xf[5] = norm_apply(b.y, hi, lo);
-    xf[6] = norm_apply(b.z, hi, lo); xf[7] = norm_apply(b.w, hi, lo);
-  } else if (P.act == 0) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(P.x) + (size_t)t * P.H + c0);
-    const float4 a = src[0], b = src[1];
-    xf[0] = a.x; xf[1] = a.y; xf[2] = a.z; xf[3] = a.w;
-    xf[4] = b.x; xf[5] = b.y; xf[6] = b.z; xf[7] = b.w;
-  } else {
-    const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.x) + (size_t)t * P.H + c0);
-    xf[0] = bf16_lo(v.x); xf[1] = bf16_hi(v.x); xf[2] = bf16_lo(v.y); xf[3] = bf16_hi(v.y);
-    xf[4] = bf16_lo(v.z); xf[5] = bf16_hi(v.z); xf[6] = bf16_lo(v.w); xf[7] = bf16_hi(v.w);
-  }
-}
-
-// Eight weights starting at column c0 of a stored row (bf16 or 4-bit).
-MOE_DEV void load_w8(const uint8_t* row, int cols, int wfmt, int c0, float* w) {
-  if (wfmt == 0) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + (size_t)c0 * 2);
-    w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
-    w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
-  } else {
-    const uint32_t q = *reinterpret_cast<const uint32_t*>(row + c0 / 2);
-    const float d = __half2float(*reinterpret_cast<const __half*>(row + cols / 2 + (c0 / 32) * 2));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = d * static_cast<float>(static_cast<int>((q >> (4 * j)) & 0xFu) - 8);
-  }
-}
-
 }  // namespace
-
-// ===================================================================== router
-template <int TMAX>
-__global__ void __launch_bounds__(kRouteThreads) k_route(DecodeParams P) {
-  pdl_launch_dependents();
-  __shared__ float red_s[kRouteThreads / 32][TMAX];
-  __shared__ float red_c[kRouteThreads / 32][TMAX];
-  __shared__ float s_inv[TMAX][2];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
-  if (row == 0 && tid < kCtrlWords) P.ctrl[tid] = 0u;
-  if (P.block_mode) {
-    for (int t = warp; t < P.T; t += kRouteThreads / 32) {
-      float hi, lo;
-      warp_norm_factor(static_cast<const float*>(P.x) + (size_t)t * P.H, P.H, P.eps, hi, lo);
-      if (lane == 0) {
-        s_inv[t][0] = hi;
-        s_inv[t][1] = lo;
-      }
-    }
-    __syncthreads();
-  }
-  const uint16_t* w = row < P.E ? P.router_w + (size_t)row * P.H : P.gate_w;
-  float s[TMAX], c[TMAX];
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) s[t] = c[t] = 0.f;
-  const bool exact_products = P.block_mode || P.act == 1;  // bf16 x bf16 is exact in fp32
-  for (int c0 = tid * 8; c0 < P.H; c0 += kRouteThreads * 8) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(w + c0);
-    const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                         bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (t >= P.T) break;
-      float xf[8];
-      if (P.block_mode) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(P.x) + (size_t)t * P.H + c0);
-        const float4 a = src[0], b = src[1];
-        const float av[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xf[j] = norm_apply(av[j], s_inv[t][0], s_inv[t][1]);
-      } else if (P.act == 0) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(P.x) + (size_t)t * P.H + c0);
-        const float4 a = src[0], b = src[1];
-        xf[0] = a.x; xf[1] = a.y; xf[2] = a.z; xf[3] = a.w;
-        xf[4] = b.x; xf[5] = b.y; xf[6] = b.z; xf[7] = b.w;
-      } else {
-        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.x) + (size_t)t * P.H + c0);
-        xf[0] = bf16_lo(v.x); xf[1] = bf16_hi(v.x); xf[2] = bf16_lo(v.y); xf[3] = bf16_hi(v.y);
-        xf[4] = bf16_lo(v.z); xf[5] = bf16_hi(v.z); xf[6] = bf16_lo(v.w); xf[7] = bf16_hi(v.w);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float p, e1 = 0.f, tt, e2;
-        if (exact_products)
-          p = __fmul_rn(wf[j], xf[j]);
-        else
-          two_prod(wf[j], xf[j], p, e1);
-        two_sum(s[t], p, tt, e2);
-        s[t] = tt;
-        c[t] = __fadd_rn(c[t], __fadd_rn(e1, e2));
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) {
-    warp_sum2(s[t], c[t]);
-    if (lane == 0) {
-      red_s[warp][t] = s[t];
-      red_c[warp][t] = c[t];
-    }
-  }
-  __syncthreads();
-  if (tid < P.T) {
-    float S = red_s[0][tid], C = red_c[0][tid];
-    for (int wi = 1; wi < kRouteThreads / 32; ++wi) {
-      float tt, e;
-      two_sum(S, red_s[wi][tid], tt, e);
-      S = tt;
-      C = __fadd_rn(__fadd_rn(C, red_c[wi][tid]), e);
-    }
-    P.logits[(size_t)tid * (P.E + 1) + row] = __fadd_rn(S, C);
-  }
-}
 
 // ============================================================ expert kernel
 namespace {
-
 struct Smem {
   uint8_t* stage;
   uint8_t* hslot;
@@ -308,60 +130,12 @@ MOE_DEV Smem smem_views(const DecodeParams& P, uint8_t* base) {
   return s;
 }
 
-MOE_DEV unsigned long long topk_key(float v, int e) {
-  return (static_cast<unsigned long long>(float_order_key(v)) << 32) | (0xFFFFFFFFull - (unsigned)e);
-}
-
-// Top-k of one token's logits by one warp: the k-th largest lane maximum is a
-// lower bound of the k-th largest key, so only keys at or above it can be
-// chosen; those candidates are ranked among themselves.  Keys order by value
-// and then by lower expert index, which is the tie rule of the layer.
-MOE_DEV void warp_topk(const float* lg, int E, int K, unsigned long long* cand, int32_t* ids, float* pout) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long mx = 0ull;
-  for (int e = lane; e < E; e += 32) {
-    const unsigned long long k = topk_key(lg[e], e);
-    mx = k > mx ? k : mx;
-  }
-  int r = 0;
-#pragma unroll 8
-  for (int l = 0; l < 32; ++l) {
-    const unsigned long long o = __shfl_sync(0xffffffffu, mx, l);
-    r += (o > mx) ? 1 : 0;
-  }
-  const unsigned b = __ballot_sync(0xffffffffu, r == K - 1);
-  const unsigned long long tau = __shfl_sync(0xffffffffu, mx, __ffs(b) - 1);
-  int nc = 0;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const unsigned long long k = e < E ? topk_key(lg[e], e) : 0ull;
-    const bool pred = e < E && k >= tau;
-    const unsigned bb = __ballot_sync(0xffffffffu, pred);
-    if (pred) cand[nc + __popc(bb & ((1u << lane) - 1u))] = k;
-    nc += __popc(bb);
-  }
-  __syncwarp();
-  for (int i = lane; i < nc; i += 32) {
-    const unsigned long long k = cand[i];
-    int rank = 0;
-    for (int j = 0; j < nc; ++j) rank += (cand[j] > k) ? 1 : 0;
-    if (rank < K) ids[rank] = static_cast<int32_t>(0xFFFFFFFFull - (k & 0xFFFFFFFFull));
-  }
-  __syncwarp();
-  const float l0 = lg[ids[0]];
-  const float z = lane < K ? expf(lg[ids[lane]] - l0) : 0.f;
-  const float sum = warp_sum(z);
-  if (lane < K) pout[lane] = z / sum;
-  __syncwarp();
-}
-
 }  // namespace
 
 template <int TMAX>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_experts(DecodeParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem S = smem_views(P, smem_raw);
-  const int ncand = P.E;  // candidates of one token never exceed E
   Tabs& tb = *S.tb;
   uint64_t* full = S.bar;
   uint64_t* empty = S.bar + P.nst;
@@ -523,7 +297,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_experts(DecodeParams P) {
         xseg = sgi;
 #pragma unroll
         for (int t = 0; t < TMAX; ++t)
-          if (t < T && valid) load_x8(P, tb, t, c0, xs[t]);
+          if (t < T && valid) load_x8_any(P, &tb.inv[0][0], t, c0, xs[t]);
       }
       float ag[TMAX], au[TMAX];
 #pragma unroll
@@ -656,9 +430,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_experts(DecodeParams P) {
   pdl_wait();
   for (int t = warp; t < T; t += kNumConsumerWarps) {
     float* lg = S.logits + (size_t)t * (P.E + 1);
-    for (int e = lane; e <= P.E; e += 32) lg[e] = P.logits[(size_t)t * (P.E + 1) + e];
+    for (int e = lane; e <= P.E; e += 32) lg[e] = P.logits[(size_t)t * P.ls + e];
     __syncwarp();
-    warp_topk(lg, P.E, K, S.cand + (size_t)t * ncand, &tb.ids[t * K], &tb.p[t * K]);
+    warp_topk(lg, P.E, K, &tb.ids[t * K], &tb.p[t * K]);
     if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-lg[P.E]));
   }
   for (int e = ctid; e < P.E; e += kConsThreads) {
@@ -753,9 +527,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_experts(DecodeParams P) {
 
 int decode_kernel_count() { return 2; }
 
-static int tmax_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
-
-static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 int decode_smem_layout(DecodeParams& p, int smem_limit) {
   const int TM = tmax_for(p.T);
@@ -804,16 +575,11 @@ static cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream, bool use
   static_assert(TMAX <= kDecodeMaxT, "TMAX");
   cudaError_t err = cudaFuncSetAttribute(k_experts<TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
   if (err != cudaSuccess) return err;
+  err = launch_route(p, stream, false);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(p.E + 1);
-  cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
-  err = cudaLaunchKernelEx(&cfg, k_route<TMAX>, p);
-  if (err != cudaSuccess) return err;
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = p.smem_bytes;

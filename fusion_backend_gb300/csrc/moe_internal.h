@@ -43,7 +43,8 @@ struct DecodeParams {
 
   // workspace
   uint32_t* ctrl;
-  float* logits;  // [T][E+1], column E = shared-gate logit
+  float* logits;  // [T][ls], columns 0..E-1 router logits, column E the shared-gate logit
+  int ls;         // logits row stride in floats: E + 1 rounded up to a multiple of 4
   float* h;       // [T*K][I]
   float* hsh;     // [T][Is]
   int32_t* r_counts;
@@ -58,11 +59,26 @@ struct DecodeParams {
   long long sgu_bytes;     // shared gate (or up) matrix [Is,H]
   int rbH, rbI, rbIs;      // bytes of one row with H / I / Is columns
 
-  // shared-memory layout (bytes from the dynamic base)
+  // shared-memory layout of the general expert kernel (bytes from the dynamic base)
   int nst, nhs, hslot_bytes;
   int off_stage, off_hslot, off_red, red_floats, off_ys, ys_rows_max, off_logits, off_tab, off_bar;
   int smem_bytes;
+
+  // layout of the per-warp-ring expert kernel (fast path)
+  int v2;           // 1 when the fast path is launched
+  int v2_nw;        // consumer warps
+  int v2_nslots;    // ring slots per warp
+  int v2_slot;      // bytes per slot
+  int v2_xmode;     // 0 x in registers (T=1), 1 x fp32 in smem, 2 x fp16 (4-bit layout) in smem
+  int v2_hmode;     // 0 h fp32 in smem, 1 h bf16, 2 h fp16 (4-bit layout)
+  int v2_rows_w;    // max output rows per CTA (stride of the down outputs)
+  int v2_cap_gu;    // gate/up row pairs per slot
+  int v2_off_bar, v2_off_ring, v2_off_tab, v2_off_union, v2_union_bytes, v2_off_list, v2_smem;
 };
+
+// Router kernel (moe_route.cu); pdl = launch behind the previous kernel with
+// programmatic stream serialisation.
+cudaError_t launch_route(const DecodeParams& p, cudaStream_t stream, bool pdl);
 
 // Launchers (moe_decode.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, bool use_pdl);
@@ -70,5 +86,11 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, bool use_p
 // layout fields of p.  Returns -1 when the shapes do not fit.
 int decode_smem_layout(DecodeParams& p, int smem_optin_limit);
 int decode_kernel_count();
+
+// Per-warp-ring fast path (moe_decode_v2.cu): fills the v2 layout fields and
+// returns the shared-memory bytes, or -1 when these shapes need the general
+// kernel.
+int decode_v2_layout(DecodeParams& p, int smem_optin_limit);
+cudaError_t launch_decode_v2(const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace moe

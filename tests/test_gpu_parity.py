@@ -73,6 +73,8 @@ def test_tiny_layer_bf16_x_and_repeat_bitwise():
         Shapes(T=5, H=128, E=4, top_k=4, I=40, Is=16),    # every expert selected
         Shapes(T=8, H=1024, E=64, top_k=6, I=320, Is=256),
         Shapes(T=7, H=776, E=33, top_k=32, I=24, Is=48),  # top_k = 32, E not a multiple of 32
+        Shapes(T=1, H=2304, E=16, top_k=4, I=256, Is=128),  # H > 2048: the general kernel
+        Shapes(T=3, H=3072, E=8, top_k=2, I=64, Is=64),    # H > 2048, several tokens
     ],
 )
 def test_ragged_and_degenerate_shapes(shapes):
@@ -93,6 +95,12 @@ def test_small_q4_layer(T):
     layer = datagen.make_layer(1005, SMALL_Q4, WFMT_Q4B32)
     x, _ = draw_tokens(1005, layer, T, ACT_BF16)
     check_case(layer, x, ACT_BF16, f"small q4 T={T}")
+
+
+def test_small_q4_layer_fp32_x_general_kernel():
+    layer = datagen.make_layer(1008, SMALL_Q4, WFMT_Q4B32)
+    x, _ = draw_tokens(1008, layer, 3, ACT_F32)
+    check_case(layer, x, ACT_F32, "small q4 fp32 x")
 
 
 @pytest.fixture(scope="module")
