@@ -30,8 +30,11 @@
  *   4-bit: each row = cols/2 bytes of nibbles (element 2j in the low nibble of
  *          byte j, element 2j+1 in the high nibble) followed by cols/32 fp16
  *          scales; element value = d * (nibble - 8) for its 32-block.
- * Layer layout: router [E,H]; expert e = gate [I,H] | up [I,H] | down [H,I];
- * shared = gate [Is,H] | up [Is,H] | down [H,Is]; shared-gate vector [H] bf16.
+ * Layer layout: router [E,H]; expert e = gate [I,H] | up [I,H] | downT [I,H];
+ * shared = gate [Is,H] | up [Is,H] | downT [Is,H]; shared-gate vector [H] bf16.
+ * downT is the down projection stored transposed (row i = column i of the
+ * [H,I] matrix Wd), so every stored row has H elements and, in the 4-bit
+ * format, the blocks of all three matrices run along H.
  *
  * Portable C11 with pthreads; built with -ffp-contract=off.
  */
@@ -104,9 +107,9 @@ static int64_t matrix_bytes(int wfmt, int64_t rows, int64_t cols) {
   return wfmt == 0 ? rows * cols * 2 : rows * (cols * 9 / 16);
 }
 
-/* Bytes of one expert block (gate | up | down) with intermediate size `inter`. */
+/* Bytes of one expert block (gate | up | downT) with intermediate size `inter`. */
 int64_t or_expert_bytes(int wfmt, int64_t H, int64_t inter) {
-  return 2 * matrix_bytes(wfmt, inter, H) + matrix_bytes(wfmt, H, inter);
+  return 3 * matrix_bytes(wfmt, inter, H);
 }
 
 /* y[r] = sum_c W[r,c] * v[c], in double, c ascending. */
@@ -120,17 +123,23 @@ static void matvec(const uint8_t* W, int wfmt, int64_t rows, int64_t cols, const
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
-/* One SwiGLU FFN: y = down( silu(gate x) * (up x) ).  blk points at gate|up|down. */
+/* One SwiGLU FFN: y = Wd ( silu(gate x) * (up x) ).  blk points at
+ * gate|up|downT; y[c] = sum_i Wd[c,i] h[i] with Wd[c,i] = downT[i,c], in
+ * double, i ascending. */
 void or_swiglu_ffn(const uint8_t* blk, int wfmt, int64_t H, int64_t inter, const double* x, double* y) {
   double* g = (double*)malloc(sizeof(double) * (size_t)inter);
   double* u = (double*)malloc(sizeof(double) * (size_t)inter);
   const uint8_t* Wg = blk;
   const uint8_t* Wu = blk + matrix_bytes(wfmt, inter, H);
-  const uint8_t* Wd = blk + 2 * matrix_bytes(wfmt, inter, H);
+  const uint8_t* WdT = blk + 2 * matrix_bytes(wfmt, inter, H);
   matvec(Wg, wfmt, inter, H, x, g);
   matvec(Wu, wfmt, inter, H, x, u);
   for (int64_t i = 0; i < inter; ++i) g[i] = silu(g[i]) * u[i];
-  matvec(Wd, wfmt, H, inter, g, y);
+  for (int64_t c = 0; c < H; ++c) {
+    double acc = 0.0;
+    for (int64_t i = 0; i < inter; ++i) acc += weight_at(WdT, wfmt, H, i, c) * g[i];
+    y[c] = acc;
+  }
   free(g);
   free(u);
 }

@@ -53,11 +53,12 @@ def np_layer(layer: datagen.Layer):
     experts = []
     for e in range(E):
         blk = layer.expert_w[e * eb : (e + 1) * eb]
+        # the third matrix is stored transposed ([I,H]); Wd = its transpose
         experts.append((np_matrix(blk[:gu], f, I, H), np_matrix(blk[gu : 2 * gu], f, I, H),
-                        np_matrix(blk[2 * gu :], f, H, I)))
+                        np_matrix(blk[2 * gu :], f, I, H).T.copy()))
     sgu = datagen.matrix_bytes(f, Is, H)
     sh = (np_matrix(layer.shexp_w[:sgu], f, Is, H), np_matrix(layer.shexp_w[sgu : 2 * sgu], f, Is, H),
-          np_matrix(layer.shexp_w[2 * sgu :], f, H, Is))
+          np_matrix(layer.shexp_w[2 * sgu :], f, Is, H).T.copy())
     router = datagen.bf16_to_f32(layer.router_w.reshape(E, H)).astype(np.float64)
     gvec = datagen.bf16_to_f32(layer.shexp_gate_w).astype(np.float64)
     return router, gvec, experts, sh
