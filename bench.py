@@ -38,7 +38,7 @@ H, E, K_TOP, I, IS = 2048, 128, 8, 768, 512
 N_LAYER_COPIES = 16
 N_TOKENS = 100
 SEED = 20261202
-# dram__bytes_read.sum + dram__bytes_write.sum of one k_experts launch from the
+# dram__bytes_read.sum + dram__bytes_write.sum of one k_rows launch from the
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
 NCU_TRAFFIC_BYTES = {"decode_bf16": None, "decode_q4": None}
@@ -344,7 +344,7 @@ def main():
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "traffic": NCU_TRAFFIC_BYTES.get(args.config),
                          "algorithmic_bytes_per_step": bytes_per_step,
-                         "kernel": "k_experts (+ overlapped k_route); duration = step time"},
+                         "kernel": "k_rows (+ k_route, programmatic dependent launch); duration = step time"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4,
                     "steps": e2e_steps, "how": "eager public-API calls: pinned H2D of x, execute, D2H of out"},

@@ -46,9 +46,10 @@ EXPORTS = (
     "moe_ffn_destroy",
     "moe_ffn_strerror",
     "moe_ffn_execute_static_scratch",
+    "moe_ffn_last_cuda_error",
 )
 
-STATIC_SCRATCH_BYTES = 1 << 20
+STATIC_SCRATCH_BYTES = 1 << 24
 
 
 class MoeFFNError(RuntimeError):
@@ -100,6 +101,8 @@ def lib() -> ctypes.CDLL:
         L.moe_ffn_execute_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_ffn_strerror.restype = ctypes.c_char_p
         L.moe_ffn_strerror.argtypes = [ctypes.c_int]
+        L.moe_ffn_last_cuda_error.restype = ctypes.c_char_p
+        L.moe_ffn_last_cuda_error.argtypes = []
         _lib = L
     return _lib
 
@@ -113,6 +116,8 @@ def strerror(status: int) -> str:
 
 def _check(status: int, what: str) -> None:
     if status != OK:
+        if status == ERR_CUDA:
+            what = f"{what} [{lib().moe_ffn_last_cuda_error().decode()}]"
         raise MoeFFNError(status, what)
 
 

@@ -2,6 +2,7 @@
 // launches.  See include/moe_ffn.h for the contract.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -21,7 +22,7 @@ constexpr int kMaxDevices = 64;
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t ctrl, logits, h, hsh, counts, offsets, perm, active, nactive, total;
+  size_t ctrl, logits, partial, counts, offsets, perm, active, nactive, total;
 };
 
 }  // namespace
@@ -68,16 +69,21 @@ int device_info(DeviceInfo** out) {
   return MOE_FFN_OK;
 }
 
-long long matrix_bytes(int wfmt, long long rows, long long cols) {
-  return wfmt == MOE_FFN_W_BF16 ? rows * cols * 2 : rows * (cols * 9 / 16);
+thread_local char t_last_cuda_error[256];
+
+// MOE_FFN_OK, or MOE_FFN_ERR_CUDA with the runtime's text kept for
+// moe_ffn_last_cuda_error.
+int cuda_status(cudaError_t err) {
+  if (err == cudaSuccess) return MOE_FFN_OK;
+  snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", cudaGetErrorName(err), cudaGetErrorString(err));
+  return MOE_FFN_ERR_CUDA;
 }
-int row_bytes(int wfmt, int cols) { return wfmt == MOE_FFN_W_BF16 ? cols * 2 : cols * 9 / 16; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool valid_plan(const moe_ffn_plan* p) { return p && p->magic == kPlanMagic; }
 
-void fill_decode_params(const moe_ffn_plan* plan, DecodeParams& P, void* ws) {
+void fill_params(const moe_ffn_plan* plan, LayerParams& P, void* ws) {
   memset(&P, 0, sizeof(P));
   const moe_ffn_shapes& s = plan->s;
   P.T = s.T;
@@ -92,19 +98,12 @@ void fill_decode_params(const moe_ffn_plan* plan, DecodeParams& P, void* ws) {
   P.ctrl = reinterpret_cast<uint32_t*>(w + plan->ws.ctrl);
   P.logits = reinterpret_cast<float*>(w + plan->ws.logits);
   P.ls = (s.E + 1 + 3) / 4 * 4;
-  P.h = reinterpret_cast<float*>(w + plan->ws.h);
-  P.hsh = reinterpret_cast<float*>(w + plan->ws.hsh);
+  P.partial = reinterpret_cast<float*>(w + plan->ws.partial);
   P.r_counts = reinterpret_cast<int32_t*>(w + plan->ws.counts);
   P.r_offsets = reinterpret_cast<int32_t*>(w + plan->ws.offsets);
   P.r_perm = reinterpret_cast<int32_t*>(w + plan->ws.perm);
   P.r_active = reinterpret_cast<int32_t*>(w + plan->ws.active);
   P.r_nactive = reinterpret_cast<int32_t*>(w + plan->ws.nactive);
-  P.expert_bytes = 2 * matrix_bytes(plan->wfmt, s.I, s.H) + matrix_bytes(plan->wfmt, s.H, s.I);
-  P.gu_bytes = matrix_bytes(plan->wfmt, s.I, s.H);
-  P.sgu_bytes = matrix_bytes(plan->wfmt, s.Is, s.H);
-  P.rbH = row_bytes(plan->wfmt, s.H);
-  P.rbI = row_bytes(plan->wfmt, s.I);
-  P.rbIs = row_bytes(plan->wfmt, s.Is);
 }
 
 int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes, const void* x,
@@ -123,8 +122,8 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   int rc = device_info(&dev);
   if (rc != MOE_FFN_OK) return rc;
 
-  DecodeParams P;
-  fill_decode_params(plan, P, workspace);
+  LayerParams P;
+  fill_params(plan, P, workspace);
   P.x = x;
   P.router_w = static_cast<const uint16_t*>(router_w);
   P.gate_w = static_cast<const uint16_t*>(shexp_gate_w);
@@ -135,19 +134,10 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   P.topk_w = topk_w;
   P.block_mode = block_mode;
   P.eps = eps;
-  P.G = dev->sm_count;
-  cudaError_t err;
-  // Fast path (per-warp rings) when the shapes fit it; the 4-bit fast path
-  // forms products in fp16, so it takes bf16 activations (or the block form,
-  // whose normalised input is bf16).  Otherwise the general kernel.
-  const bool fast_ok = plan->wfmt == MOE_FFN_W_BF16 || plan->act == MOE_FFN_ACT_BF16;
-  if (fast_ok && decode_v2_layout(P, dev->smem_optin) >= 0) {
-    err = launch_decode_v2(P, reinterpret_cast<cudaStream_t>(stream));
-  } else {
-    if (decode_smem_layout(P, dev->smem_optin) < 0) return MOE_FFN_ERR_UNSUPPORTED;
-    err = launch_decode(P, reinterpret_cast<cudaStream_t>(stream), true);
-  }
-  return err == cudaSuccess ? MOE_FFN_OK : MOE_FFN_ERR_CUDA;
+  P.G = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
+  if (rows_layout(P) < 0 || P.smem > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
+  const cudaError_t err = launch_rows(P, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(err);
 }
 
 }  // namespace
@@ -164,14 +154,11 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   if (s.T < 1 || s.T > 256 || s.E < 1 || s.E > kMaxExperts || s.top_k < 1 || s.top_k > s.E ||
       s.top_k > kMaxTopK || s.H < 1 || s.I < 1 || s.Is < 1)
     return MOE_FFN_ERR_UNSUPPORTED;
-  const int mult = dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256;
-  if (s.H % mult || s.I % mult || s.Is % mult) return MOE_FFN_ERR_UNSUPPORTED;
-  if (s.H > (1 << 20) || s.I > (1 << 20) || s.Is > (1 << 20)) return MOE_FFN_ERR_UNSUPPORTED;
-  // Decode path limits: T <= 8, one gate+up row pair and one down row per ring stage.
-  if (s.T > kDecodeMaxT) return MOE_FFN_ERR_UNSUPPORTED;
-  if (2 * row_bytes(dtype.wfmt, s.H) > kStageBytes || row_bytes(dtype.wfmt, s.I) > kStageBytes ||
-      row_bytes(dtype.wfmt, s.Is) > kStageBytes)
-    return MOE_FFN_ERR_UNSUPPORTED;
+  // Decode path: T <= 8; stored rows of H elements (bf16: H a multiple of 8,
+  // 4-bit: of 256, so that rows are 16-byte multiples); H <= 4096.
+  if (s.T > kDecodeMaxT || s.H > kMaxH) return MOE_FFN_ERR_UNSUPPORTED;
+  if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256)) return MOE_FFN_ERR_UNSUPPORTED;
+  if (s.I > (1 << 20) || s.Is > (1 << 20)) return MOE_FFN_ERR_UNSUPPORTED;
 
   moe_ffn_plan* p = new (std::nothrow) moe_ffn_plan();
   if (!p) return MOE_FFN_ERR_INVALID_ARG;
@@ -187,10 +174,8 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   off = align256(off + kCtrlWords * 4);
   L.logits = off;
   off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
-  L.h = off;
-  off = align256(off + T * K * (size_t)s.I * 4);
-  L.hsh = off;
-  off = align256(off + T * (size_t)s.Is * 4);
+  L.partial = off;
+  off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * 4);
   L.counts = off;
   off = align256(off + E * 4);
   L.offsets = off;
@@ -267,7 +252,7 @@ int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value) {
       *value = plan->path;
       return MOE_FFN_OK;
     case MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE:
-      *value = decode_kernel_count();
+      *value = kLaunchesPerExecute;
       return MOE_FFN_OK;
     default:
       return MOE_FFN_ERR_INVALID_ARG;
@@ -279,6 +264,8 @@ void moe_ffn_destroy(moe_ffn_plan_t plan) {
   plan->magic = 0;
   delete plan;
 }
+
+const char* moe_ffn_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* moe_ffn_strerror(int status) {
   switch (status) {
@@ -334,8 +321,9 @@ extern "C" int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_strea
   void* scratch = nullptr;
   const int rc = static_scratch_address(&scratch);
   if (rc != MOE_FFN_OK) return rc;
-  // The kernels initialise every control word they read in each call, so no
-  // part of the (shared, reused) array has to be cleared here.
+  // The router kernel of each call zeroes the control words before the row
+  // kernel of that call counts on them, so no part of the (shared, reused)
+  // array has to be cleared here.
   return run(plan, stream, scratch, MOE_FFN_STATIC_SCRATCH_BYTES, x, router_w, expert_w, shexp_w, shexp_gate_w, out,
              nullptr, nullptr, 0, 0.f);
 }

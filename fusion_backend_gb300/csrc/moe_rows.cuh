@@ -1,0 +1,859 @@
+#pragma once
+// Row kernel of the fused MoE FFN layer (decode path, T <= 8), sm_103a.
+// Instantiated by the moe_rows_*.cu units.
+//
+// Work unit: one intermediate index i of one expert group (the shared expert,
+// or a routed expert selected by some token).  Its weights are three
+// contiguous stored rows of H elements -- gate row i, up row i and row i of
+// the transposed down matrix -- and it contributes
+//     y_t += w_t * silu(gate_i . x_t) * (up_i . x_t) * downT_i
+// to every token t the group serves (w_t = the routing weight p, or the
+// shared-expert gate s).  A block owns a contiguous run of units, so it needs
+// nothing from other blocks until its partial y is complete: the only
+// grid-wide step is the final fixed-order sum of the G partials.
+//
+// One persistent block of 8 warps per SM.  Weights stream through a ring of
+// `ns` stages of `rs` units, each stage three bulk copies (TMA engine) issued
+// by thread 0 on one mbarrier.  Per stage:
+//   A  warp r (< rows in the stage) forms the two dot products of unit r for
+//      its tokens and writes h_t = w_t silu(g_t) u_t to shared memory;
+//   -- one block barrier (after it, thread 0 refills the slot of the
+//      previous stage) --
+//   C  every thread owns 8 (or 16) columns of y for all tokens and adds
+//      h_t * downT_r over the stage's rows, in row order.
+// The shared expert's stages are issued at kernel start, before the wait for
+// the router (weights do not depend on the previous kernel); the routed
+// stages follow once this block has computed the routing itself from the
+// router's logits.
+//
+// End: each block stores its partial y[T][H] (fp32), counts itself done on a
+// release counter, waits (bounded) for all G blocks, then sums the G partials
+// of its own output columns in block order and writes out (adding x_res in
+// the block form).  All orders are fixed, so results are bitwise repeatable.
+//
+// 4-bit weights, fast instance: codes are decoded with the fp16 exponent
+// trick (a nibble n OR-ed into the mantissa of fp16 1024 reads 1024 + n, so
+// (1024 + n) - 1032 = n - 8 exactly); products with the fp16 activation and
+// their 16-element sums are formed with packed half2 FMAs and scaled by the
+// block's d in fp32.  The general instance decodes to fp32.
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "moe_layer_common.cuh"
+
+namespace moe {
+
+enum : int { kXReg = 0, kXF32 = 1 };
+constexpr int kMaxStagesRing = 8;
+constexpr int kBarStage = 1;  // named barrier of the compute warps, once per stage
+constexpr int kRsMaxB16 = 4;  // rows per stage, bf16 weights
+constexpr int kRsMaxQ4 = 8;   // rows per stage, 4-bit weights
+
+// Routing tables of one block, carved from shared memory with sizes of the
+// plan (T tokens, K per token, E experts).
+struct RowTab {
+  int32_t* ids;      // [T*K] chosen experts, rank order
+  float* p;          // [T*K] their weights
+  float* s;          // [T] shared-expert gate sigmoid(g . x_t)
+  float* inv;        // [2T] block form: RMSNorm factor hi, lo
+  uint32_t* bitmap;  // [ceil(E/32)] selected experts
+  int16_t* inv_u;    // [E] active index of a selected expert
+  int32_t* active;   // [T*K] selected experts, ascending
+  uint32_t* mask;    // [T*K] tokens of active expert u (bit t)
+  float* wt;         // [T*K][T] weight of token t for active expert u (0 if not routed)
+  int32_t* misc;     // spare
+};
+
+__host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTab* v) {
+  const int TK = T * K;
+  const int sz[10] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4};
+  int off = 0, o[10];
+  for (int i = 0; i < 10; ++i) {
+    o[i] = off;
+    off += (sz[i] + 15) & ~15;
+  }
+  if (v && base) {
+    v->ids = reinterpret_cast<int32_t*>(base + o[0]);
+    v->p = reinterpret_cast<float*>(base + o[1]);
+    v->s = reinterpret_cast<float*>(base + o[2]);
+    v->inv = reinterpret_cast<float*>(base + o[3]);
+    v->bitmap = reinterpret_cast<uint32_t*>(base + o[4]);
+    v->inv_u = reinterpret_cast<int16_t*>(base + o[5]);
+    v->active = reinterpret_cast<int32_t*>(base + o[6]);
+    v->mask = reinterpret_cast<uint32_t*>(base + o[7]);
+    v->wt = reinterpret_cast<float*>(base + o[8]);
+    v->misc = reinterpret_cast<int32_t*>(base + o[9]);
+  }
+  return off;
+}
+
+// ------------------------------------------------------------ 4-bit helpers
+MOE_DEV uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(m), "r"(c));
+  return r;
+}
+MOE_DEV uint32_t h2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+MOE_DEV uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+MOE_DEV float h2_sum(uint32_t a) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&a);
+  const float2 f = __half22float2(h);
+  return f.x + f.y;
+}
+MOE_DEV uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The 8 codes of one 32-bit word (elements 2j in the low nibble of byte j)
+// -> 4 half2 of (n - 8): (e0,e4) (e1,e5) (e2,e6) (e3,e7), the order of
+// pack_quarter.
+MOE_DEV void dequant_quarter(uint32_t w, uint32_t* o) {
+  constexpr uint32_t kMagic = 0x64006400u, kSub = 0x64086408u, kSixteenth = 0x2C002C00u, kMinus72 = 0xD480D480u;
+  const uint32_t w8 = w >> 8;
+  o[0] = h2_sub(lop3_and_or(w, 0x000F000Fu, kMagic), kSub);
+  o[1] = h2_fma(lop3_and_or(w, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
+  o[2] = h2_sub(lop3_and_or(w8, 0x000F000Fu, kMagic), kSub);
+  o[3] = h2_fma(lop3_and_or(w8, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
+}
+
+// Code n of nibble j of a 32-bit word, as the float n - 8 (exact: the
+// nibble OR-ed into the mantissa of 2^23 reads 2^23 + n).
+MOE_DEV float nib_f32(uint32_t w, int j) {
+  return __fsub_rn(__uint_as_float(0x4B000000u | ((w >> (4 * j)) & 0xFu)), 8388616.0f);
+}
+
+// Eight consecutive values c = 8q .. 8q+7 of a row -> the uint4 of quarter q%4.
+MOE_DEV uint4 pack_quarter(const float* v) {
+  return make_uint4(pack_h2(v[0], v[4]), pack_h2(v[1], v[5]), pack_h2(v[2], v[6]), pack_h2(v[3], v[7]));
+}
+
+// v[0..7] per lane -> the warp sum of v[(lane >> 2) & 7], in every lane of the
+// group of four lanes 4i .. 4i+3 (9 shuffles, 5 levels).
+MOE_DEV float warp_reduce8(const float* v) {
+  const int l = threadIdx.x & 31;
+  const bool b4 = l & 16, b3 = l & 8, b2 = l & 4;
+  float n4[4], n2[2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) n4[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 4], 16);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) n2[j] = (b3 ? n4[j + 2] : n4[j]) + __shfl_xor_sync(0xffffffffu, b3 ? n4[j] : n4[j + 2], 8);
+  float r = (b2 ? n2[1] : n2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? n2[0] : n2[1], 4);
+  r += __shfl_xor_sync(0xffffffffu, r, 2);
+  r += __shfl_xor_sync(0xffffffffu, r, 1);
+  return r;
+}
+
+// Top-k of one token's E logits by one warp.  Each lane holds the order keys
+// of experts lane + 32 i (i < EPL); K rounds take the warp maximum (hardware
+// reduction) and, among lanes holding it, the lowest expert index, so equal
+// logits go to the lower index.  NaN ranks as -inf.  ids[0..K) in rank
+// order; pout = softmax over the K chosen logits.  E <= 32 * EPL, K <= 32.
+template <int EPL>
+MOE_DEV void warp_topk(const float* lg, int E, int K, int32_t* ids, float* pout) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    float v = e < E ? __ldcg(lg + e) : 0.f;
+    v = v != v ? -INFINITY : v;
+    key[i] = e < E ? float_order_key(v) : 0u;  // every real key is >= key(-inf) > 0
+  }
+  int myid = 0;
+  uint32_t mykey = 0u;
+  for (int j = 0; j < K; ++j) {
+    uint32_t best = 0u;
+    uint32_t bi = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (key[i] > best) {
+        best = key[i];
+        bi = (uint32_t)(lane + 32 * i);
+      }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, best == m ? bi : 0xFFFFFFFFu);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if ((uint32_t)(lane + 32 * i) == win) key[i] = 0u;
+    if (lane == j) {
+      myid = (int)win;
+      mykey = m;
+    }
+  }
+  // the chosen logit back from its order key (the key map is a bijection)
+  const float lj = lane < K ? __uint_as_float((mykey & 0x80000000u) ? (mykey & 0x7FFFFFFFu) : ~mykey) : 0.f;
+  const float l0 = __shfl_sync(0xffffffffu, lj, 0);
+  const float z = lane < K ? expf(lj - l0) : 0.f;
+  const float sum = warp_sum(z);
+  if (lane < K) {
+    ids[lane] = myid;
+    pout[lane] = z / sum;
+  }
+}
+
+// Eight activations of one row, columns c0 .. c0+7 (c0 % 8 == 0), from the
+// shared-memory copy of x: fp32 rows (src4; in the block form the
+// normalised bf16 value of x_res, factor hi + lo) or bf16 rows.
+MOE_DEV void x8_from_smem(const uint8_t* row, int src4, int block_mode, float hi, float lo, int c0, float* xf) {
+  if (src4) {
+    const float4* p = reinterpret_cast<const float4*>(row + (size_t)c0 * 4);
+    const float4 a = p[0], b = p[1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xf[e] = block_mode ? norm_apply(v[e], hi, lo) : v[e];
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + (size_t)c0 * 2);
+    xf[0] = bf16_lo(v.x); xf[1] = bf16_hi(v.x); xf[2] = bf16_lo(v.y); xf[3] = bf16_hi(v.y);
+    xf[4] = bf16_lo(v.z); xf[5] = bf16_hi(v.z); xf[6] = bf16_lo(v.w); xf[7] = bf16_hi(v.w);
+  }
+}
+
+MOE_DEV float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// floor(a * b / d) for the block partitions; 32-bit division when a * b fits.
+MOE_DEV uint32_t muldiv(uint32_t a, uint32_t b, uint32_t d) {
+  if (__umulhi(a, b) == 0u) return (a * b) / d;
+  return (uint32_t)(((unsigned long long)a * b) / d);
+}
+
+// ------------------------------------------------------------------- kernel
+// TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048 and
+// E <= 256 (and, for 4-bit weights, an activation exact in fp16).
+template <int TMAX, bool Q4, bool FAST, int NCH>
+__global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
+  constexpr bool H16 = Q4 && FAST;           // fp16 activation + half2 products
+  static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
+  constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
+  extern __shared__ __align__(128) uint8_t sm[];
+  // The parameter block is read once into shared memory, before the wait on
+  // the router: later reads then never miss in the constant cache on the
+  // critical path.
+  __shared__ LayerParams sP;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cta = blockIdx.x;
+  if (tid == 0) sP = Pk;
+  __syncthreads();
+  const LayerParams& P = sP;
+  const int T = P.T, K = P.K, TK = T * K;
+  const int H = FAST ? 2048 : P.H;
+  const int RS = P.rs, NS = P.ns;
+  const long long rb = P.rb;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + P.off_bar);
+  uint64_t* xbar = full + kMaxStagesRing;  // the activation copy
+  int* scnt = reinterpret_cast<int*>(sm + P.off_bar + 96);  // [NS] warps that have read a stage's slot
+  RowTab tb;
+  row_tab(sm + P.off_tab, T, K, P.E, &tb);
+  uint8_t* xs = sm + P.off_x;
+  uint8_t* ring = sm + P.off_ring;
+  const uint64_t pol = policy_evict_first();
+
+  // The next call's router blocks may become resident beside this block.
+  pdl_launch_dependents();
+
+  // Units of this block.  Shared expert: rows [sa, sb), known now.  Routed:
+  // the run [q0, q1) of the flattened (active expert u, row i) order
+  // f = u * I + i, known after the routing, sized so that shared + routed
+  // rows are balanced over the blocks.  Stage s < n_sh holds shared rows
+  // sa + s*RS ..; stage s >= n_sh holds routed f = q0 + (s - n_sh)*RS ..
+  // (up to RS rows, which may span two experts).
+  const int sa = (int)muldiv(P.Is, cta, P.G), sb = (int)muldiv(P.Is, cta + 1, P.G);
+  const int n_sh = (sb - sa + RS - 1) / RS;
+  uint32_t q0 = 0, q1 = 0;
+  int n_stages = n_sh;
+
+  // Stage k -> ring slot k % NS: gate rows at +0, up rows at +RS*rb, downT
+  // rows at +2*RS*rb, one mbarrier; a routed stage that spans two experts
+  // takes two runs of three copies.  Everything it needs is held in
+  // registers: the issuing thread is on the stage loop's critical path.
+  const uint8_t* const r_expert_w = P.expert_w;
+  const uint8_t* const r_shexp_w = P.shexp_w;
+  const long long r_expert_bytes = P.expert_bytes;
+  const long long r_mat = (long long)P.I * rb, r_smat = (long long)P.Is * rb;
+  const int r_I = P.I, r_stage_bytes = P.stage_bytes;
+  auto issue = [&](int k) {
+    const int slot = k % NS;
+    uint8_t* dst = ring + (size_t)slot * r_stage_bytes;
+    uint64_t* bar = &full[slot];
+    if (k < n_sh) {
+      const int i0 = sa + k * RS, n = min(RS, sb - i0);
+      const uint32_t bytes = (uint32_t)(n * rb);
+      const uint8_t* src = r_shexp_w + (long long)i0 * rb;
+      mbar_arrive_expect_tx(bar, 3 * bytes);
+      bulk_g2s(dst, src, bytes, bar, pol);
+      bulk_g2s(dst + (size_t)RS * rb, src + r_smat, bytes, bar, pol);
+      bulk_g2s(dst + (size_t)2 * RS * rb, src + 2 * r_smat, bytes, bar, pol);
+    } else {
+      const uint32_t f0 = q0 + (uint32_t)(k - n_sh) * RS;
+      const int n = (int)min((uint32_t)RS, q1 - f0);
+      mbar_arrive_expect_tx(bar, (uint32_t)(3 * n * rb));
+      uint32_t u = f0 / (uint32_t)r_I, i = f0 - u * (uint32_t)r_I;
+      int r = 0;
+      while (r < n) {
+        const int m = min(n - r, r_I - (int)i);
+        const uint32_t bytes = (uint32_t)(m * rb);
+        const uint8_t* src = r_expert_w + (long long)tb.active[u] * r_expert_bytes + (long long)i * rb;
+        bulk_g2s(dst + (size_t)r * rb, src, bytes, bar, pol);
+        bulk_g2s(dst + (size_t)(RS + r) * rb, src + r_mat, bytes, bar, pol);
+        bulk_g2s(dst + (size_t)(2 * RS + r) * rb, src + 2 * r_mat, bytes, bar, pol);
+        r += m;
+        i = 0;
+        ++u;
+      }
+    }
+  };
+
+  // ---- shared-expert stages: issued before the wait (weights do not depend
+  // on the previous kernel); lane j < NS of warp 0 issues stage j
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      scnt[i] = 0;
+    }
+    mbar_init(xbar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (warp == 0 && lane < min(n_sh, NS)) issue(lane);
+
+  // ---- the router's logits, the activation and (block form) x_res are ready
+  pdl_wait();
+  // The activation (or x_res) of all tokens: one bulk copy per block into
+  // shared memory -- every block needs all of it, and one read per block
+  // keeps the L2 lines of x from being hammered by every warp of the grid.
+  const int src4 = P.act == 0 || P.block_mode;  // fp32 source rows
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)(T * H * (src4 ? 4 : 2));
+    mbar_arrive_expect_tx(xbar, bytes);
+    bulk_g2s(xs, P.x, bytes, xbar, policy_evict_last());
+  }
+  // routing, every block from the router's logits: top-k of token t on warp
+  // 7 - t (the chosen experts and their softmax weights) and the shared gate
+  // sigmoid(logit_E)
+  {
+    const int t = kRowWarps - 1 - warp;
+    if (t < T) {
+      float sl = 0.f;
+      if (lane == 0) sl = __ldcg(P.logits + (size_t)t * P.ls + P.E);
+      warp_topk<EPL>(P.logits + (size_t)t * P.ls, P.E, K, tb.ids + t * K, tb.p + t * K);
+      if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-sl));
+    }
+  }
+  for (int i = tid; i < (P.E + 31) / 32; i += kRowThreads) tb.bitmap[i] = 0u;
+  for (int i = tid; i < TK; i += kRowThreads) tb.mask[i] = 0u;
+  for (int i = tid; i < TK * T; i += kRowThreads) tb.wt[i] = 0.f;
+  if (!mbar_wait(xbar, 0)) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  // block form: RMSNorm factors of the fp32 rows (warp t)
+  if (P.block_mode) {
+    for (int t = warp; t < T; t += kRowWarps) {
+      float hi, lo;
+      warp_norm_factor(reinterpret_cast<const float*>(xs) + (size_t)t * H, H, P.eps, hi, lo);
+      if (lane == 0) {
+        tb.inv[2 * t] = hi;
+        tb.inv[2 * t + 1] = lo;
+      }
+    }
+  }
+  __syncthreads();
+  for (int ts = tid; ts < TK; ts += kRowThreads) {
+    const int e = tb.ids[ts];
+    atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
+  }
+  // activation in its compute form.  Fast shapes: this thread's 8 columns
+  // c0 = 8 * tid of every token, in registers (bf16 pairs, or for 4-bit
+  // weights the packed fp16 pairs of the dequantised order).  Other shapes: fp32
+  // rows rewritten in place in shared memory (all reads of the source
+  // precede the barrier, all writes follow it).
+  uint32_t xb[FAST && !Q4 ? TMAX : 1][4];  // bf16 pairs (the activation is bf16-exact)
+  uint32_t xh[FAST && Q4 ? TMAX : 1][4];
+  if (FAST) {
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (t < T)
+        x8_from_smem(xs + (size_t)t * H * (src4 ? 4 : 2), src4, P.block_mode, P.block_mode ? tb.inv[2 * t] : 0.f,
+                     P.block_mode ? tb.inv[2 * t + 1] : 0.f, 8 * tid, v);
+      if (!Q4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          xb[FAST && !Q4 ? t : 0][e] = (__float_as_uint(v[2 * e]) >> 16) | (__float_as_uint(v[2 * e + 1]) & 0xFFFF0000u);
+      } else {
+        const uint4 q = pack_quarter(v);
+        xh[FAST && Q4 ? t : 0][0] = q.x;
+        xh[FAST && Q4 ? t : 0][1] = q.y;
+        xh[FAST && Q4 ? t : 0][2] = q.z;
+        xh[FAST && Q4 ? t : 0][3] = q.w;
+      }
+    }
+  } else {
+    constexpr int kMaxGroups = kDecodeMaxT * kMaxH / 8 / kRowThreads;  // 8-value groups per compute thread
+    const int groups = T * (H / 8);
+    float v[kMaxGroups][8];
+#pragma unroll
+    for (int k = 0; k < kMaxGroups; ++k) {
+      const int gi = tid + kRowThreads * k;
+      if (gi < groups) {
+        const int t = gi / (H / 8), q = gi % (H / 8);
+        x8_from_smem(xs + (size_t)t * H * (src4 ? 4 : 2), src4, P.block_mode, P.block_mode ? tb.inv[2 * t] : 0.f,
+                     P.block_mode ? tb.inv[2 * t + 1] : 0.f, 8 * q, v[k]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kMaxGroups; ++k) {
+      const int gi = tid + kRowThreads * k;
+      if (gi < groups) {
+        const int t = gi / (H / 8), q = gi % (H / 8);
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(xs) + (size_t)t * H + 8 * q);
+        dst[0] = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
+        dst[1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
+      }
+    }
+  }
+  __syncthreads();
+  // active index of an expert = selected experts below it
+  int U = 0;
+  for (int w = 0; w < (P.E + 31) / 32; ++w) U += __popc(tb.bitmap[w]);
+  for (int ts = tid; ts < TK; ts += kRowThreads) {
+    const int e = tb.ids[ts], t = ts / K;
+    int u = __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+    for (int w = 0; w < (e >> 5); ++w) u += __popc(tb.bitmap[w]);
+    tb.active[u] = e;
+    tb.inv_u[e] = static_cast<int16_t>(u);
+    atomicOr(&tb.mask[u], 1u << t);
+    tb.wt[u * T + t] = tb.p[ts];
+  }
+  {
+    const uint32_t R = (uint32_t)U * (uint32_t)P.I, Is = P.Is, G = P.G, c = cta;
+    if (R >= 2 * G) {
+      q0 = muldiv(R + Is, c, G) - muldiv(Is, c, G);
+      q1 = muldiv(R + Is, c + 1, G) - muldiv(Is, c + 1, G);
+    } else {
+      q0 = muldiv(R, c, G);
+      q1 = muldiv(R, c + 1, G);
+    }
+    n_stages = n_sh + (int)((q1 - q0 + RS - 1) / RS);
+  }
+  __syncthreads();
+  // the first routed stages: lane j of warp 0 issues stage j of the ring
+  if (warp == 0 && lane >= n_sh && lane < min(n_stages, NS)) issue(lane);
+  if (cta == 0 && warp == kRowWarps - 1) {
+    // routing outputs for the caller and the test readers: counts, offsets
+    // (a scan over the experts) and the stable token-major permutation
+    int base = 0;
+    for (int e0 = 0; e0 < P.E; e0 += 32) {
+      const int e = e0 + lane;
+      int cnt = 0;
+      if (e < P.E && (tb.bitmap[e >> 5] >> (e & 31) & 1u)) cnt = __popc(tb.mask[tb.inv_u[e]]);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < P.E) {
+        P.r_counts[e] = cnt;
+        P.r_offsets[e] = base + incl - cnt;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      P.r_offsets[P.E] = base;
+      *P.r_nactive = U;
+    }
+    __syncwarp();
+    for (int ts = lane; ts < TK; ts += 32) {
+      if (P.topk_ids) P.topk_ids[ts] = tb.ids[ts];
+      if (P.topk_w) P.topk_w[ts] = tb.p[ts];
+      const int t = ts / K, e = tb.ids[ts];
+      P.r_perm[P.r_offsets[e] + __popc(tb.mask[tb.inv_u[e]] & ((1u << t) - 1u))] = ts;
+    }
+    for (int u = lane; u < U; u += 32) P.r_active[u] = tb.active[u];
+  }
+  const uint32_t all_tokens = (1u << T) - 1u;
+
+  // ---- stages
+  // Thread j owns the 8-column chunks ch = j + 256 k
+  // (k < NCH) of H: it forms the partial gate/up dot products of every row
+  // of a stage over its chunks (A), and accumulates y over the same chunks
+  // (C).  Each thread first copies its chunks of the stage into registers;
+  // the last warp to do so refills the slot at once, so the copies in flight
+  // never wait on arithmetic.  The 8 warps' partials meet in shared memory:
+  // after the stage barrier a few threads (spread over the warps) form
+  // h = w silu(g) u (A2), which C uses one stage later -- one block barrier
+  // per stage, and C of stage s overlaps A2 of stage s + 1.
+  constexpr int RSM = Q4 ? kRsMaxQ4 : kRsMaxB16;
+  constexpr int NV = 2 * RSM * TMAX;  // dot values per warp per stage: (row, gate|up, token)
+  float* part = reinterpret_cast<float*>(sm + P.off_part);  // [2][kRowWarps][NV]
+  float* hb = reinterpret_cast<float*>(sm + P.off_h);       // [2][RSM][TMAX]
+  bool timed_out = false;
+  float y[TMAX][NCH][8];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+    for (int k = 0; k < NCH; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[t][k][e] = 0.f;
+
+  {
+    // rows of stage s: shared rows sa + s*RS .. or routed f0 = q0 + (s - n_sh)*RS ..
+    auto stage_rows = [&](int s, uint32_t& f0, int& n) {
+      const bool shared = s < n_sh;
+      f0 = shared ? (uint32_t)(sa + s * RS) : q0 + (uint32_t)(s - n_sh) * RS;
+      n = shared ? min(RS, sb - (int)f0) : (int)min((uint32_t)RS, q1 - f0);
+    };
+    // downT chunks of this thread, by stage parity
+    uint4 dwb[2][Q4 ? 1 : RSM][NCH];
+    uint32_t dwq[2][Q4 ? RSM : 1][NCH];
+    uint16_t dsc[2][Q4 ? RSM : 1][NCH];
+    int n_prev = 0;
+    uint32_t m_prev = 0u;
+
+    auto step = [&](auto parc, int s) {
+      constexpr int par = decltype(parc)::value;
+      uint32_t f0 = 0u, m = 0u;
+      int n = 0;
+      if (s < n_stages) {
+        const int slot = s % NS;
+        if (!mbar_wait(&full[slot], (uint32_t)(s / NS) & 1u)) timed_out = true;
+        const bool shared = s < n_sh;
+        stage_rows(s, f0, n);
+        const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
+        // this thread's chunks of every row of the stage, into registers
+        uint4 wgb[Q4 ? 1 : RSM][NCH], wub[Q4 ? 1 : RSM][NCH];
+        uint32_t wgq[Q4 ? RSM : 1][NCH], wuq[Q4 ? RSM : 1][NCH];
+        uint16_t sgq[Q4 ? RSM : 1][NCH], suq[Q4 ? RSM : 1][NCH];
+#pragma unroll
+        for (int r = 0; r < RSM; ++r) {
+          if (r < n) {
+            const uint8_t* rg = sl + (size_t)r * rb;
+            const uint8_t* ru = sl + (size_t)(RS + r) * rb;
+            const uint8_t* rd = sl + (size_t)(2 * RS + r) * rb;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+              const int ch = tid + kRowThreads * k;
+              if (FAST || ch < H / 8) {
+                if (!Q4) {
+                  wgb[Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(rg + (size_t)ch * 16);
+                  wub[Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(ru + (size_t)ch * 16);
+                  dwb[par][Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(rd + (size_t)ch * 16);
+                } else {
+                  const int so = H / 2 + 2 * (ch >> 2);
+                  wgq[Q4 ? r : 0][k] = *reinterpret_cast<const uint32_t*>(rg + (size_t)ch * 4);
+                  wuq[Q4 ? r : 0][k] = *reinterpret_cast<const uint32_t*>(ru + (size_t)ch * 4);
+                  dwq[par][Q4 ? r : 0][k] = *reinterpret_cast<const uint32_t*>(rd + (size_t)ch * 4);
+                  sgq[Q4 ? r : 0][k] = *reinterpret_cast<const uint16_t*>(rg + so);
+                  suq[Q4 ? r : 0][k] = *reinterpret_cast<const uint16_t*>(ru + so);
+                  dsc[par][Q4 ? r : 0][k] = *reinterpret_cast<const uint16_t*>(rd + so);
+                }
+              }
+            }
+          }
+        }
+        // release the slot: the warp's loads are ordered before its arrival
+        // (warp barrier, then a CTA-scope fence), and the last warp to
+        // arrive refills the slot at once
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          if (atomicAdd(&scnt[slot], 1) == kRowWarps - 1) {
+            scnt[slot] = 0;
+            if (s + NS < n_stages) issue(s + NS);
+          }
+        }
+        // tokens of each row's group
+        uint32_t mrow[RSM];
+        {
+          uint32_t u = shared ? 0u : f0 / (uint32_t)P.I, i = shared ? 0u : f0 - u * (uint32_t)P.I;
+#pragma unroll
+          for (int r = 0; r < RSM; ++r) {
+            mrow[r] = r >= n ? 0u : shared ? all_tokens : tb.mask[u];
+            if (!shared && ++i == (uint32_t)P.I) {
+              i = 0;
+              ++u;
+            }
+            m |= mrow[r];
+          }
+        }
+        // -- A: partial dots of every row over this thread's chunks; packed
+        // in eights, reduced across the warp, one partial per warp
+        float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
+        float pend[8];
+#pragma unroll
+        for (int r = 0; r < RSM; ++r) {
+          float ga[TMAX], ua[TMAX];
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) ga[t] = ua[t] = 0.f;
+          if (r < n) {
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+              const int ch = tid + kRowThreads * k;
+              if (!FAST && ch >= H / 8) break;
+              if (!Q4) {
+                const uint4 vg = wgb[Q4 ? 0 : r][k], vu = wub[Q4 ? 0 : r][k];
+                const float gf[8] = {bf16_lo(vg.x), bf16_hi(vg.x), bf16_lo(vg.y), bf16_hi(vg.y),
+                                     bf16_lo(vg.z), bf16_hi(vg.z), bf16_lo(vg.w), bf16_hi(vg.w)};
+                const float uf[8] = {bf16_lo(vu.x), bf16_hi(vu.x), bf16_lo(vu.y), bf16_hi(vu.y),
+                                     bf16_lo(vu.z), bf16_hi(vu.z), bf16_lo(vu.w), bf16_hi(vu.w)};
+#pragma unroll
+                for (int t = 0; t < TMAX; ++t) {
+                  if (!(mrow[r] >> t & 1u)) continue;
+                  float xv[8];
+                  if (FAST) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      xv[2 * e] = bf16_lo(xb[FAST && !Q4 ? t : 0][e]);
+                      xv[2 * e + 1] = bf16_hi(xb[FAST && !Q4 ? t : 0][e]);
+                    }
+                  } else {
+                    const float4* xp =
+                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
+                    const float4 a = xp[0], b = xp[1];
+                    xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+                    xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+                  }
+                  float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    g0 = fmaf(gf[e], xv[e], g0);
+                    g1 = fmaf(gf[e + 4], xv[e + 4], g1);
+                    u0 = fmaf(uf[e], xv[e], u0);
+                    u1 = fmaf(uf[e + 4], xv[e + 4], u1);
+                  }
+                  ga[t] += g0 + g1;
+                  ua[t] += u0 + u1;
+                }
+              } else {
+                const uint32_t qg = wgq[Q4 ? r : 0][k], qu = wuq[Q4 ? r : 0][k];
+                const float dg = __half2float(__ushort_as_half(sgq[Q4 ? r : 0][k]));
+                const float du = __half2float(__ushort_as_half(suq[Q4 ? r : 0][k]));
+                if (H16) {
+                  uint32_t hg[4], hu[4];
+                  dequant_quarter(qg, hg);
+                  dequant_quarter(qu, hu);
+#pragma unroll
+                  for (int t = 0; t < TMAX; ++t) {
+                    if (!(mrow[r] >> t & 1u)) continue;
+                    const uint32_t* xv = xh[FAST && Q4 ? t : 0];
+                    const uint32_t sg = h2_fma(hg[1], xv[1], h2_fma(hg[0], xv[0], 0u));
+                    const uint32_t tg = h2_fma(hg[3], xv[3], h2_fma(hg[2], xv[2], 0u));
+                    const uint32_t su = h2_fma(hu[1], xv[1], h2_fma(hu[0], xv[0], 0u));
+                    const uint32_t tu = h2_fma(hu[3], xv[3], h2_fma(hu[2], xv[2], 0u));
+                    ga[t] = fmaf(dg, h2_sum(sg) + h2_sum(tg), ga[t]);
+                    ua[t] = fmaf(du, h2_sum(su) + h2_sum(tu), ua[t]);
+                  }
+                } else {
+#pragma unroll
+                  for (int t = 0; t < TMAX; ++t) {
+                    if (!(mrow[r] >> t & 1u)) continue;
+                    const float4* xp =
+                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
+                    const float4 a = xp[0], b = xp[1];
+                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    float sg = 0.f, su = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                      sg = fmaf(nib_f32(qg, e), xv[e], sg);
+                      su = fmaf(nib_f32(qu, e), xv[e], su);
+                    }
+                    ga[t] = fmaf(dg, sg, ga[t]);
+                    ua[t] = fmaf(du, su, ua[t]);
+                  }
+                }
+              }
+            }
+          }
+          // values (r, gate|up, t) at v = (2r + gu) * TMAX + t, reduced in eights
+#pragma unroll
+          for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              const int v = (2 * r + gu) * TMAX + t;
+              pend[v & 7] = gu ? ua[t] : ga[t];
+              if ((v & 7) == 7 && 8 * (v >> 3) < 2 * n * TMAX) {
+                const float red = warp_reduce8(pend);
+                if ((lane & 3) == 0) pw[(v & ~7) + (lane >> 2)] = red;
+              }
+            }
+        }
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      if (s < n_stages) {
+        // -- A2: h of (row, token) from the warp partials in order; value j
+        // goes to thread (j % 8) * 32 + j / 8, spreading the work over warps
+        const int j = (tid & 31) * kRowWarps + (tid >> 5);
+        if (j < n * TMAX) {
+          const int r = j / TMAX, t = j % TMAX;
+          const float* pp = part + (size_t)par * kRowWarps * NV;
+          float g = 0.f, u = 0.f;
+#pragma unroll
+          for (int w = 0; w < kRowWarps; ++w) {
+            g += pp[w * NV + (2 * r) * TMAX + t];
+            u += pp[w * NV + (2 * r + 1) * TMAX + t];
+          }
+          float h = 0.f;
+          if (s < n_sh) {
+            h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
+          } else {
+            uint32_t uu = f0 / (uint32_t)P.I, ii = f0 - uu * (uint32_t)P.I + r;
+            while (ii >= (uint32_t)P.I) {
+              ii -= P.I;
+              ++uu;
+            }
+            h = (tb.mask[uu] >> t & 1u) ? tb.wt[uu * T + t] * silu_mul(g, u) : 0.f;
+          }
+          hb[par * RSM * TMAX + j] = h;
+        }
+      }
+      // -- C of the previous stage: y += h_r * downT_r, this thread's chunks
+      if (s >= 1) {
+        constexpr int pp = 1 - par;
+        const float* hp = hb + pp * RSM * TMAX;
+#pragma unroll
+        for (int r = 0; r < RSM; ++r) {
+          if (r < n_prev) {
+            float hv[TMAX];
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) hv[t] = hp[r * TMAX + t];
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+              const int ch = tid + kRowThreads * k;
+              if (!FAST && ch >= H / 8) break;
+              float w[8];
+              float sc = 1.f;  // 4-bit: the block scale d, applied to h
+              if (!Q4) {
+                const uint4 v = dwb[pp][Q4 ? 0 : r][k];
+                w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+                w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+              } else {
+                const uint32_t qw = dwq[pp][Q4 ? r : 0][k];
+                sc = __half2float(__ushort_as_half(dsc[pp][Q4 ? r : 0][k]));
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = nib_f32(qw, e);
+              }
+#pragma unroll
+              for (int t = 0; t < TMAX; ++t) {
+                if (!(m_prev >> t & 1u)) continue;
+                const float c = Q4 ? hv[t] * sc : hv[t];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[t][k][e] = fmaf(c, w[e], y[t][k][e]);
+              }
+            }
+          }
+        }
+      }
+      n_prev = n;
+      m_prev = m;
+    };
+    for (int s = 0; s <= n_stages; s += 2) {
+      step(std::integral_constant<int, 0>(), s);
+      if (s + 1 <= n_stages) step(std::integral_constant<int, 1>(), s + 1);
+    }
+  }
+  if (__syncthreads_or(timed_out) && tid == 0) {
+    // leave no copy in flight into this block's shared memory: wait (bounded)
+    // once more for the last stages issued
+    atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+    for (int s = max(0, n_stages - NS); s < n_stages; ++s) mbar_wait(&full[s % NS], (uint32_t)(s / NS) & 1u);
+  }
+
+  // ---- partial y of this block
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    if (t >= T) break;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      const int ch = tid + kRowThreads * k;
+      if (!FAST && ch >= H / 8) break;
+      float4* dst = reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t) * H + 8 * ch);
+      dst[0] = make_float4(y[t][k][0], y[t][k][1], y[t][k][2], y[t][k][3]);
+      dst[1] = make_float4(y[t][k][4], y[t][k][5], y[t][k][6], y[t][k][7]);
+    }
+  }
+  // every block's partial, then the sum of this block's columns: the block
+  // barrier orders all threads' stores before thread 0's release (a
+  // cumulative release at GPU scope), and its acquire orders every other
+  // block's stores before this block's reads
+  __syncthreads();
+  if (tid == 0) {
+    red_release_gpu_add(&P.ctrl[kCtrlDone], 1u);
+    bool ok = false;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+      if (ld_acquire_gpu(&P.ctrl[kCtrlDone]) >= (uint32_t)P.G) {
+        ok = true;
+        break;
+      }
+      if (i > 256) __nanosleep(32);
+    }
+    if (!ok) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  }
+  __syncthreads();
+  // This block's output columns [da, db) for all tokens: O sums of G
+  // partials.  Thread (sp, o) adds partials sp, sp + S, ... in order, all
+  // loads in flight together; the S part sums are then added in order.
+  const int da = (int)muldiv(H, cta, P.G), db = (int)muldiv(H, cta + 1, P.G);
+  const int nD = db - da, O = T * nD;
+  if (O > 0) {
+    const int S = O >= kRowThreads ? 1 : kRowThreads / O;
+    // The ring is idle now (every issued stage was waited on); reuse it.
+    float* red = reinterpret_cast<float*>(ring);  // [S][O]
+    for (int idx = tid; idx < S * O; idx += kRowThreads) {
+      const int o = idx % O, sp = idx / O;
+      const int t = o / nD, col = da + o % nD;
+      const float* src = P.partial + (size_t)t * H + col;
+      const size_t stride = (size_t)T * H;
+      float acc = 0.f;
+      int c = sp;
+      for (; c + 7 * S < P.G; c += 8 * S) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __ldcg(src + (size_t)(c + q * S) * stride);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc += v[q];
+      }
+      for (; c < P.G; c += S) acc += __ldcg(src + (size_t)c * stride);
+      red[sp * O + o] = acc;
+    }
+    __syncthreads();
+    for (int oo = tid; oo < O; oo += kRowThreads) {
+      float acc = red[oo];
+      for (int q = 1; q < S; ++q) acc += red[q * O + oo];
+      const int t = oo / nD, col = da + oo % nD;
+      float* dst = P.out + (size_t)t * H + col;
+      *dst = P.block_mode ? __fadd_rn(*dst, acc) : acc;
+    }
+  }
+}
+
+template <int TMAX, bool Q4, bool FAST, int NCH = 1>
+inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(k_rows<TMAX, Q4, FAST, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+  if (err != cudaSuccess) return err;
+  err = launch_route(p, stream);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  return cudaLaunchKernelEx(&cfg, k_rows<TMAX, Q4, FAST, NCH>, p);
+}
+
+}  // namespace moe

@@ -193,7 +193,7 @@ int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_str
  * calls whose work overlaps on the GPU (other streams, or graphs replayed
  * concurrently) race on the array and give undefined results: serialise them.
  */
-#define MOE_FFN_STATIC_SCRATCH_BYTES (1 << 20)
+#define MOE_FFN_STATIC_SCRATCH_BYTES (1 << 24)
 int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream, const void* x, const void* router_w,
                                    const void* expert_w, const void* shexp_w, const void* shexp_gate_w, float* out);
 
@@ -209,6 +209,11 @@ void moe_ffn_destroy(moe_ffn_plan_t plan);
 
 /* Static text for a status code. */
 const char* moe_ffn_strerror(int status);
+
+/* Text of the CUDA runtime error behind the last MOE_FFN_ERR_CUDA returned to
+ * the calling host thread ("" if none).  The pointer stays valid until that
+ * thread's next call into the library. */
+const char* moe_ffn_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

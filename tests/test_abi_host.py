@@ -49,8 +49,9 @@ def test_prepare_reports_workspace_without_device(lib):
         (datagen.Shapes(1, 256, 8, 9, 128, 256), fb.W_BF16),      # top_k > E
         (datagen.Shapes(1, 256, 40, 33, 128, 256), fb.W_BF16),    # top_k > 32
         (datagen.Shapes(1, 256, 2000, 2, 128, 256), fb.W_BF16),   # E > 1024
-        (datagen.Shapes(1, 256, 8, 2, 128, 256), fb.W_Q4B32),     # 4-bit needs multiples of 256
-        (datagen.Shapes(1, 16384, 8, 2, 128, 256), fb.W_BF16),    # a gate+up row pair exceeds a ring stage
+        (datagen.Shapes(1, 264, 8, 2, 128, 256), fb.W_Q4B32),     # 4-bit rows need H a multiple of 256
+        (datagen.Shapes(1, 8192, 8, 2, 128, 256), fb.W_BF16),     # H > 4096 (decode path bound)
+        (datagen.Shapes(9, 256, 8, 2, 128, 256), fb.W_BF16),      # T > 8 (grouped-GEMM regime, not built)
     ],
 )
 def test_prepare_rejects_unsupported(lib, shapes, wfmt):

@@ -108,7 +108,7 @@ def decode_bf16_layer():
     return datagen.make_layer(2024, DECODE, WFMT_BF16)
 
 
-@pytest.mark.parametrize("T", [1, 2, 8])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_decode_bf16_full_size(decode_bf16_layer, T):
     x, _ = draw_tokens(2024, decode_bf16_layer, T, ACT_BF16, first_token=10 * T)
     check_case(decode_bf16_layer, x, ACT_BF16, f"decode bf16 T={T}")

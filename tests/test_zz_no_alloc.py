@@ -62,7 +62,7 @@ def test_static_scratch_matches_workspace_entry_point(base, T, act, wfmt):
 def test_static_scratch_rejects_plans_larger_than_the_array():
     import fusion_backend_gb300 as fb
 
-    big = Shapes(T=8, H=2048, E=128, top_k=32, I=1024, Is=512)  # routed h alone is 1 MiB
+    big = Shapes(T=8, H=4096, E=128, top_k=8, I=768, Is=512)  # per-block partial outputs alone exceed 16 MiB
     plan, ws_bytes = fb.moe_ffn_prepare(big, ACT_BF16, WFMT_BF16)
     assert ws_bytes > fb.STATIC_SCRATCH_BYTES
     fake = torch.empty(16, dtype=torch.float32, device="cuda")
