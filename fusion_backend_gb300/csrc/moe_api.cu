@@ -136,7 +136,9 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   P.eps = eps;
   P.G = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
   if (rows_layout(P) < 0 || P.smem > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
-  const cudaError_t err = launch_rows(P, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t err = rows_tensor_maps(P);
+  if (err != cudaSuccess) return cuda_status(err);
+  err = launch_rows(P, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(err);
 }
 

@@ -60,6 +60,18 @@ MOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Tiled tensor copy (TMA engine) of one box of the 5-D tensor map `tmap`
+// (a __grid_constant__ kernel parameter) at coordinates c0..c4 into this
+// CTA's shared memory, completion counted on `bar` in bytes.
+MOE_DEV void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4, uint64_t* bar,
+                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
 // Bulk prefetch of [src, src + bytes) into L2 (hint only; src 16-byte aligned,
 // bytes a multiple of 16).
 MOE_DEV void prefetch_l2(const void* src, uint32_t bytes) {

@@ -2,6 +2,7 @@
 // kernels.  Not installed; the public interface is include/moe_ffn.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -59,10 +60,20 @@ struct LayerParams {
 
   // shared-memory layout of the row kernel (bytes from the dynamic base)
   int rs;           // rows per stage
-  int ns;           // stages in the ring
+  int ns;           // stages in the ring (tensor-core path: gate + up boxes)
+  int nsd;          // tensor-core path: downT boxes in their own ring
+  int rp;           // row pitch in a ring slot (rb)
   int stage_bytes;  // 3 * rs * rb
   int xmode;        // 0 x in registers (each thread its 8 columns), 1 fp32 rows in shared memory
-  int off_bar, off_x, off_tab, off_h, off_part, off_ring, smem;
+  int off_bar, off_x, off_tab, off_h, off_part, off_ring, off_dring, smem;
+
+  // Tensor maps of the tensor-core path (bf16 weights, H = 2048): boxes of
+  // one stage's gate + up rows (gu) and downT rows (d) of the routed experts
+  // (e) and of the shared expert (s), 128-byte swizzled in shared memory.
+  alignas(64) CUtensorMap tm_gu_e;
+  alignas(64) CUtensorMap tm_d_e;
+  alignas(64) CUtensorMap tm_gu_s;
+  alignas(64) CUtensorMap tm_d_s;
 };
 
 // Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
@@ -73,6 +84,9 @@ cudaError_t launch_route(const LayerParams& p, cudaStream_t stream);
 // Row kernel (moe_rows_*.cu).  rows_layout fills the layout fields and
 // returns the dynamic shared-memory bytes, or -1 when the shapes do not fit.
 int rows_layout(LayerParams& p);
+// Encodes the tensor maps when the launch takes the tensor-core path;
+// cudaSuccess or an error.
+cudaError_t rows_tensor_maps(LayerParams& p);
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream);
 constexpr int kLaunchesPerExecute = 2;
 

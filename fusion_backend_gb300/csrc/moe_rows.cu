@@ -1,4 +1,6 @@
 // Row kernel: choice of instance and shared-memory layout (host side).
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 
 #include "moe_rows.cuh"
@@ -23,20 +25,36 @@ int align128(int v) { return (v + 127) & ~127; }
 // Layout with `rs` rows per stage; false when fewer than 3 stages fit.
 static bool rows_layout_rs(LayerParams& p, int rs, int xbytes, int tab, int tmax) {
   p.rs = rs;
-  p.stage_bytes = (int)(3 * rs * p.rb);
+  p.rp = (int)p.rb;
+  p.stage_bytes = 3 * rs * p.rp;
   p.off_bar = 0;
-  p.off_tab = 128;
+  p.off_tab = 256;
   const int rsm = p.wfmt == 1 ? kRsMaxQ4 : kRsMaxB16;
   p.off_h = align128(p.off_tab + tab);
   p.off_part = align128(p.off_h + 2 * rsm * tmax * 4);
   p.off_x = align128(p.off_part + 2 * kRowWarps * 2 * rsm * tmax * 4);
-  p.off_ring = align128(p.off_x + xbytes);
+  p.off_ring = (p.off_x + xbytes + 1023) & ~1023;  // 128-byte-swizzled tensor copies want 1024-byte alignment
   if (p.off_ring >= kSmemBudget) return false;
-  p.ns = std::min(kMaxStagesRing, (kSmemBudget - p.off_ring) / p.stage_bytes);
   // the end-of-kernel column sums reuse the ring: max(threads, T x columns) floats
   const int red_bytes = std::max(kRowThreads, p.T * ((p.H + p.G - 1) / p.G)) * 4;
+  const int avail = kSmemBudget - 1024 - p.off_ring;  // 1024: slack to align the ring in the shared window
+  if (rows_fast(p) && p.wfmt == 0) {
+    // tensor-core path: a ring of gate + up boxes (2 rs rows) and a ring of
+    // downT boxes (rs rows) with one slot more
+    p.stage_bytes = 2 * rs * p.rp;
+    const int dbytes = rs * p.rp;
+    p.ns = std::min(kMaxStagesRing - 1, (avail - dbytes) / (p.stage_bytes + dbytes));
+    p.nsd = p.ns + 1;
+    if (p.ns < 2 || red_bytes > p.ns * p.stage_bytes) return false;
+    p.off_dring = p.off_ring + p.ns * p.stage_bytes;
+    p.smem = p.off_dring + p.nsd * dbytes + 1024;
+    return true;
+  }
+  p.nsd = 0;
+  p.ns = std::min(kMaxStagesRing, avail / p.stage_bytes);
   if (p.ns < 3 || red_bytes > p.ns * p.stage_bytes) return false;
-  p.smem = p.off_ring + p.ns * p.stage_bytes;
+  p.off_dring = p.off_ring;
+  p.smem = p.off_ring + p.ns * p.stage_bytes + 1024;
   return true;
 }
 
@@ -61,9 +79,10 @@ int rows_layout(LayerParams& p) {
   long long best_flight = -1;
   for (int r = 0; r < 4; ++r) {
     if (rs_list[r] > (q4 ? kRsMaxQ4 : kRsMaxB16)) continue;
+    if (fast && !q4 && rs_list[r] != kRsMaxB16) continue;  // tensor-core stages: 4 rows
     LayerParams t = p;
     if (!rows_layout_rs(t, rs_list[r], xbytes, tab, tmax)) continue;
-    const long long flight = (long long)t.ns * t.stage_bytes;
+    const long long flight = (long long)t.ns * t.stage_bytes + (long long)t.nsd * t.rs * t.rp;
     if (flight > best_flight) {
       best_flight = flight;
       best_rs = rs_list[r];
@@ -72,6 +91,51 @@ int rows_layout(LayerParams& p) {
   if (best_rs == 0) return -1;
   rows_layout_rs(p, best_rs, xbytes, tab, tmax);
   return p.smem;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+// 5-D view of an expert block sequence [E][3 matrices][I rows][H] of bf16:
+// (64 elements, row, matrix, 64-element chunk, expert), and a box of
+// `rows` rows x `mats` matrices x all H/64 chunks of one expert, stored in
+// shared memory as [chunk][matrix][row][64] with the 128-byte swizzle.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int H, int I, int E,
+                 int rows, int mats) {
+  const cuuint64_t dims[5] = {64, (cuuint64_t)I, 3, (cuuint64_t)(H / 64), (cuuint64_t)E};
+  const cuuint64_t strides[4] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, 128, (cuuint64_t)3 * I * H * 2};
+  const cuuint32_t box[5] = {64, (cuuint32_t)rows, (cuuint32_t)mats, (cuuint32_t)(H / 64), 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t rows_tensor_maps(LayerParams& p) {
+  if (!(rows_fast(p) && p.wfmt == 0)) return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, p.H, p.I, p.E, kRsMaxB16, 2) ||
+      !encode_rows(fn, &p.tm_d_e, p.expert_w, p.H, p.I, p.E, kRsMaxB16, 1) ||
+      !encode_rows(fn, &p.tm_gu_s, p.shexp_w, p.H, p.Is, 1, kRsMaxB16, 2) ||
+      !encode_rows(fn, &p.tm_d_s, p.shexp_w, p.H, p.Is, 1, kRsMaxB16, 1))
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream) {

@@ -221,6 +221,33 @@ MOE_DEV void x8_from_smem(const uint8_t* row, int src4, int block_mode, float hi
   }
 }
 
+// ------------------------------------------------------------ tensor cores
+// D += A B, m16n8k16, bf16 operands, fp32 accumulators (A row-major 16x16,
+// B column-major 16x8), fragments as in the PTX ISA for mma.m16n8k16.
+MOE_DEV void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four 8x8 b16 matrices, transposed, from the shared-memory row address this
+// lane supplies (lanes 8q .. 8q+7 give the 8 rows of matrix q).
+MOE_DEV void ldmatrix_x4_trans(uint32_t* r, const void* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row)));
+}
+// Byte offset of bf16 element k (even) of a row in a box stored as
+// [H/64 chunks][rows][64 elements] with the 128-byte swizzle of the tensor
+// copies: line L = chunk * rows + row, 16-byte unit (k / 8) % 8 at unit
+// ((k / 8) % 8) ^ (L % 8).
+MOE_DEV int swz_off(int line, int k) { return line * 128 + ((((k >> 3) & 7) ^ (line & 7)) << 4) + ((k & 7) << 1); }
+
+// Two floats -> bf16 pair (round to nearest even), low element first.
+MOE_DEV uint32_t pack_bf16(float lo, float hi) {
+  return (uint32_t)float_to_bf16_rne(lo) | ((uint32_t)float_to_bf16_rne(hi) << 16);
+}
+
 MOE_DEV float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // floor(a * b / d) for the block partitions; 32-bit division when a * b fits.
@@ -233,8 +260,9 @@ MOE_DEV uint32_t muldiv(uint32_t a, uint32_t b, uint32_t d) {
 // TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048 and
 // E <= 256 (and, for 4-bit weights, an activation exact in fp16).
 template <int TMAX, bool Q4, bool FAST, int NCH>
-__global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
+__global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
   constexpr bool H16 = Q4 && FAST;           // fp16 activation + half2 products
+  constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // tensor-core down projection
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
   extern __shared__ __align__(128) uint8_t sm[];
@@ -252,12 +280,18 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
   const int RS = P.rs, NS = P.ns;
   const long long rb = P.rb;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + P.off_bar);
-  uint64_t* xbar = full + kMaxStagesRing;  // the activation copy
-  int* scnt = reinterpret_cast<int*>(sm + P.off_bar + 96);  // [NS] warps that have read a stage's slot
+  uint64_t* xbar = full + kMaxStagesRing;       // the activation copy
+  uint64_t* fulld = full + kMaxStagesRing + 1;  // [nsd] tensor-core path: downT boxes
+  int* scnt = reinterpret_cast<int*>(sm + P.off_bar + 160);  // [NS] warps that have read a stage's slot
   RowTab tb;
   row_tab(sm + P.off_tab, T, K, P.E, &tb);
   uint8_t* xs = sm + P.off_x;
-  uint8_t* ring = sm + P.off_ring;
+  // The ring starts on a 1024-byte boundary of the shared window (the
+  // 128-byte swizzle of the tensor copies follows absolute address bits);
+  // the layout reserves the slack.
+  const uint32_t ring_pad = (1024u - (smem_u32(sm + P.off_ring) & 1023u)) & 1023u;
+  uint8_t* ring = sm + P.off_ring + ring_pad;
+  uint8_t* dring = sm + P.off_dring + ring_pad;  // tensor-core path: downT boxes
   const uint64_t pol = policy_evict_first();
 
   // The next call's router blocks may become resident beside this block.
@@ -274,59 +308,110 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
   uint32_t q0 = 0, q1 = 0;
   int n_stages = n_sh;
 
-  // Stage k -> ring slot k % NS: gate rows at +0, up rows at +RS*rb, downT
-  // rows at +2*RS*rb, one mbarrier; a routed stage that spans two experts
-  // takes two runs of three copies.  Everything it needs is held in
-  // registers: the issuing thread is on the stage loop's critical path.
+  // Stage k -> ring slot k % NS.  A stage holds up to RS consecutive rows of
+  // one expert group: shared stages s < n_sh take rows sa + s*RS ..; the
+  // routed run [q0, q1) of the flattened (active expert u, row i) order is cut
+  // at every expert boundary into stages of RS rows.
   const uint8_t* const r_expert_w = P.expert_w;
   const uint8_t* const r_shexp_w = P.shexp_w;
   const long long r_expert_bytes = P.expert_bytes;
   const long long r_mat = (long long)P.I * rb, r_smat = (long long)P.Is * rb;
   const int r_I = P.I, r_stage_bytes = P.stage_bytes;
+  const long long rp = P.rp;
+  // stage k -> (active index u, or -1 for the shared expert; first row; rows)
+  auto stage_info = [&](int k, int& u, int& i0, int& n) {
+    if (k < n_sh) {
+      u = -1;
+      i0 = sa + k * RS;
+      n = min(RS, sb - i0);
+      return;
+    }
+    int j = k - n_sh;
+    uint32_t left = q1 - q0, uu = q0 / (uint32_t)r_I, ii = q0 - uu * (uint32_t)r_I;
+    for (;;) {
+      const uint32_t seg = min((uint32_t)r_I - ii, left);
+      const int ns = (int)((seg + RS - 1) / RS);
+      if (j < ns) {
+        u = (int)uu;
+        i0 = (int)ii + j * RS;
+        n = min(RS, (int)seg - j * RS);
+        return;
+      }
+      j -= ns;
+      left -= seg;
+      ++uu;
+      ii = 0;
+    }
+  };
+  // Tensor-core path: the downT box of stage k into its own ring.
+  auto issue_d = [&](int k) {
+    const int slot = k % P.nsd;
+    int u, i0, n;
+    stage_info(k, u, i0, n);
+    const int e = u < 0 ? 0 : tb.active[u];
+    const void* dm = u < 0 ? (const void*)&Pk.tm_d_s : (const void*)&Pk.tm_d_e;
+    mbar_arrive_expect_tx(&fulld[slot], (uint32_t)(kRsMaxB16 * rb));
+    tma_load_5d(dring + (size_t)slot * kRsMaxB16 * rb, dm, 0, i0, 2, 0, e, &fulld[slot], pol);
+  };
+  auto routed_stage_count = [&]() {
+    int cnt = 0;
+    uint32_t left = q1 - q0, ii = q0 % (uint32_t)r_I;
+    while (left > 0) {
+      const uint32_t seg = min((uint32_t)r_I - ii, left);
+      cnt += (int)((seg + RS - 1) / RS);
+      left -= seg;
+      ii = 0;
+    }
+    return cnt;
+  };
+  // One thread issues stage k.  Tensor-core path: two tiled tensor copies,
+  // the stage's 4 gate + 4 up rows and its 4 downT rows (whole boxes; rows
+  // past the stage are loaded, or zero-filled past the matrix, and unused).
+  // Otherwise three bulk copies of the n rows of each matrix.
   auto issue = [&](int k) {
     const int slot = k % NS;
     uint8_t* dst = ring + (size_t)slot * r_stage_bytes;
     uint64_t* bar = &full[slot];
-    if (k < n_sh) {
-      const int i0 = sa + k * RS, n = min(RS, sb - i0);
+    int u, i0, n;
+    stage_info(k, u, i0, n);
+    if constexpr (FAST && !Q4) {
+      const int e = u < 0 ? 0 : tb.active[u];
+      const void* gu = u < 0 ? (const void*)&Pk.tm_gu_s : (const void*)&Pk.tm_gu_e;
+      mbar_arrive_expect_tx(bar, (uint32_t)r_stage_bytes);
+      tma_load_5d(dst, gu, 0, i0, 0, 0, e, bar, pol);
+    } else {
+      const uint8_t* src;
+      long long mat;
+      if (u < 0) {
+        src = r_shexp_w + (long long)i0 * rb;
+        mat = r_smat;
+      } else {
+        src = r_expert_w + (long long)tb.active[u] * r_expert_bytes + (long long)i0 * rb;
+        mat = r_mat;
+      }
       const uint32_t bytes = (uint32_t)(n * rb);
-      const uint8_t* src = r_shexp_w + (long long)i0 * rb;
       mbar_arrive_expect_tx(bar, 3 * bytes);
       bulk_g2s(dst, src, bytes, bar, pol);
-      bulk_g2s(dst + (size_t)RS * rb, src + r_smat, bytes, bar, pol);
-      bulk_g2s(dst + (size_t)2 * RS * rb, src + 2 * r_smat, bytes, bar, pol);
-    } else {
-      const uint32_t f0 = q0 + (uint32_t)(k - n_sh) * RS;
-      const int n = (int)min((uint32_t)RS, q1 - f0);
-      mbar_arrive_expect_tx(bar, (uint32_t)(3 * n * rb));
-      uint32_t u = f0 / (uint32_t)r_I, i = f0 - u * (uint32_t)r_I;
-      int r = 0;
-      while (r < n) {
-        const int m = min(n - r, r_I - (int)i);
-        const uint32_t bytes = (uint32_t)(m * rb);
-        const uint8_t* src = r_expert_w + (long long)tb.active[u] * r_expert_bytes + (long long)i * rb;
-        bulk_g2s(dst + (size_t)r * rb, src, bytes, bar, pol);
-        bulk_g2s(dst + (size_t)(RS + r) * rb, src + r_mat, bytes, bar, pol);
-        bulk_g2s(dst + (size_t)(2 * RS + r) * rb, src + 2 * r_mat, bytes, bar, pol);
-        r += m;
-        i = 0;
-        ++u;
-      }
+      bulk_g2s(dst + (size_t)RS * rp, src + mat, bytes, bar, pol);
+      bulk_g2s(dst + (size_t)2 * RS * rp, src + 2 * mat, bytes, bar, pol);
     }
   };
 
   // ---- shared-expert stages: issued before the wait (weights do not depend
-  // on the previous kernel); lane j < NS of warp 0 issues stage j
+  // on the previous kernel), by warp 0
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
       scnt[i] = 0;
     }
+    for (int i = 0; i < P.nsd; ++i) mbar_init(&fulld[i], 1);
     mbar_init(xbar, 1);
     mbar_fence_init();
+    for (int k = 0; k < min(n_sh, NS); ++k) issue(k);
+    if constexpr (FAST && !Q4)
+      for (int k = 0; k < min(n_sh, P.nsd); ++k) issue_d(k);
   }
   __syncthreads();
-  if (warp == 0 && lane < min(n_sh, NS)) issue(lane);
 
   // ---- the router's logits, the activation and (block form) x_res are ready
   pdl_wait();
@@ -444,11 +529,15 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
       q0 = muldiv(R, c, G);
       q1 = muldiv(R, c + 1, G);
     }
-    n_stages = n_sh + (int)((q1 - q0 + RS - 1) / RS);
+    n_stages = n_sh + routed_stage_count();
   }
   __syncthreads();
-  // the first routed stages: lane j of warp 0 issues stage j of the ring
-  if (warp == 0 && lane >= n_sh && lane < min(n_stages, NS)) issue(lane);
+  // the first routed stages of the ring
+  if (tid == 0) {
+    for (int k = n_sh; k < min(n_stages, NS); ++k) issue(k);
+    if constexpr (FAST && !Q4)
+      for (int k = n_sh; k < min(n_stages, P.nsd); ++k) issue_d(k);
+  }
   if (cta == 0 && warp == kRowWarps - 1) {
     // routing outputs for the caller and the test readers: counts, offsets
     // (a scan over the experts) and the stable token-major permutation
@@ -506,14 +595,166 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
     for (int k = 0; k < NCH; ++k)
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[t][k][e] = 0.f;
+  float yc[MMA_C ? 16 : 1][4];  // tensor-core down projection: y of this warp's slice, D fragments
+#pragma unroll
+  for (int j = 0; j < (MMA_C ? 16 : 1); ++j) yc[j][0] = yc[j][1] = yc[j][2] = yc[j][3] = 0.f;
 
-  {
-    // rows of stage s: shared rows sa + s*RS .. or routed f0 = q0 + (s - n_sh)*RS ..
-    auto stage_rows = [&](int s, uint32_t& f0, int& n) {
-      const bool shared = s < n_sh;
-      f0 = shared ? (uint32_t)(sa + s * RS) : q0 + (uint32_t)(s - n_sh) * RS;
-      n = shared ? min(RS, sb - (int)f0) : (int)min((uint32_t)RS, q1 - f0);
-    };
+  if constexpr (FAST && !Q4) {
+    // ---- tensor-core stage loop (bf16 weights, H = 2048, 4 rows a stage).
+    // Warp w owns the 256-column slice [256w, 256w + 256) of H.
+    //   A: D[token][stage row] = x . W over the slice, m16n8k16 with the
+    //      tokens as the 16 A rows (8 real) and the stage's 8 gate/up rows
+    //      as the 8 B columns; 16 k-steps, B read straight from the slot.
+    //   A2: h = w silu(g) u from the 8 warps' partials (after a barrier).
+    //   C: y[16 cols][8 tokens] += downT^T h, one k-step of 16 rows per
+    //      16-column tile (the stage's 4 downT rows; the other 12 are other
+    //      rows of the slot, times h = 0); h enters as two bf16 terms
+    //      (hi + lo), so y keeps fp32 accuracy.
+    // x of this warp's slice as A fragments: row lane/4 = token (rows 8..15
+    // zero), k pairs 2(lane & 3) and +8.
+    uint32_t xa[16][2];
+    {
+      const int t = lane >> 2;
+      const float nhi = (P.block_mode && t < T) ? tb.inv[2 * t] : 0.f;
+      const float nlo = (P.block_mode && t < T) ? tb.inv[2 * t + 1] : 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks) {
+        const int k0 = 256 * warp + 16 * ks + 2 * (lane & 3);
+        uint32_t w0 = 0u, w1 = 0u;
+        if (t < T) {
+          if (src4) {
+            const float* xr = reinterpret_cast<const float*>(xs) + (size_t)t * H;
+            float a = xr[k0], b = xr[k0 + 1], c = xr[k0 + 8], d = xr[k0 + 9];
+            if (P.block_mode) {
+              a = norm_apply(a, nhi, nlo);
+              b = norm_apply(b, nhi, nlo);
+              c = norm_apply(c, nhi, nlo);
+              d = norm_apply(d, nhi, nlo);
+            }
+            // the values are bf16-exact: their upper halves
+            w0 = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+            w1 = (__float_as_uint(c) >> 16) | (__float_as_uint(d) & 0xFFFF0000u);
+          } else {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + (size_t)t * H * 2);
+            w0 = xr[k0 >> 1];
+            w1 = xr[(k0 + 8) >> 1];
+          }
+        }
+        xa[ks][0] = w0;
+        xa[ks][1] = w1;
+      }
+    }
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % NS;
+      if (!mbar_wait(&full[slot], (uint32_t)(s / NS) & 1u)) timed_out = true;
+      int su, si0, n;
+      stage_info(s, su, si0, n);
+      const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
+      // -- A (four accumulators, so the tensor-core steps do not chain).  B
+      // column n = lane / 4 is row n of the gate + up box (lines chunk * 8 + n).
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int nrow = lane >> 2;
+        float dq[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const int k0 = 256 * warp + 16 * ks + 2 * (lane & 3);
+          const int line = (k0 >> 6) * (2 * kRsMaxB16) + nrow;
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0));
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0 + 8));
+          mma_bf16(dq[ks & 3], xa[ks][0], 0u, xa[ks][1], 0u, b0, b1);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) d[e] = (dq[0][e] + dq[1][e]) + (dq[2][e] + dq[3][e]);
+      }
+      {
+        // this lane: token lane/4, stage rows 2(lane & 3) and +1 (0..3 gate, 4..7 up)
+        const int t = lane >> 2;
+        if (t < TMAX) {
+          float* pw = part + (size_t)warp * NV;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int nr = 2 * (lane & 3) + q, gu = nr >> 2, r = nr & 3;
+            pw[(2 * r + gu) * TMAX + t] = d[q];
+          }
+        }
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // every warp is done with this stage's gate + up box and with the
+      // previous stage's downT box: both slots take their next stages
+      if (tid == kRowThreads - 1) {
+        if (s + NS < n_stages) issue(s + NS);
+        if (s >= 1 && s - 1 + P.nsd < n_stages) issue_d(s - 1 + P.nsd);
+      }
+      // -- A2: value j = (row, token) on thread (j % 8) * 32 + j / 8
+      {
+        const int j = (tid & 31) * kRowWarps + (tid >> 5);
+        if (j < n * TMAX) {
+          const int r = j / TMAX, t = j % TMAX;
+          float g = 0.f, u = 0.f;
+#pragma unroll
+          for (int w = 0; w < kRowWarps; ++w) {
+            g += part[w * NV + (2 * r) * TMAX + t];
+            u += part[w * NV + (2 * r + 1) * TMAX + t];
+          }
+          float h = 0.f;
+          if (su < 0)
+            h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
+          else
+            h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
+          hb[j] = h;
+        }
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // -- C
+      if (!mbar_wait(&fulld[s % P.nsd], (uint32_t)(s / P.nsd) & 1u)) timed_out = true;
+      const uint8_t* dbox = dring + (size_t)(s % P.nsd) * kRsMaxB16 * rb;
+      if constexpr (!MMA_C) {
+        // CUDA cores (one or two tokens): chunk tid of every downT row
+        const int k = 8 * tid;
+#pragma unroll
+        for (int r = 0; r < kRsMaxB16; ++r) {
+          if (r < n) {
+            const uint4 v = *reinterpret_cast<const uint4*>(dbox + swz_off((k >> 6) * kRsMaxB16 + r, k));
+            const float w[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              const float hv = hb[r * TMAX + t];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(hv, w[e], y[t][0][e]);
+            }
+          }
+        }
+      } else {
+        const int t = lane >> 2, k0 = 2 * (lane & 3);
+        const float h0 = (k0 < n && t < TMAX) ? hb[k0 * TMAX + t] : 0.f;
+        const float h1 = (k0 + 1 < n && t < TMAX) ? hb[(k0 + 1) * TMAX + t] : 0.f;
+        const uint32_t bh = pack_bf16(h0, h1);
+        const uint32_t bl = pack_bf16(h0 - bf16_lo(bh), h1 - bf16_hi(bh));
+        // matrix q = lane / 8 of the 16x16 A tile: stored rows k = (q / 2) * 8
+        // + lane % 8 at columns (q % 2) * 8 ..; row k is downT row k % 4 of
+        // the stage (k >= 4 repeat them, times h = 0)
+        const int q = lane >> 3, r = lane & 3;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t at[8][4];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int m0 = 256 * warp + 16 * (8 * half + j) + (q & 1) * 8;
+            ldmatrix_x4_trans(at[j], dbox + swz_off((m0 >> 6) * kRsMaxB16 + r, m0));
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bh, 0u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bl, 0u);
+        }
+      }
+    }
+  } else {
+
     // downT chunks of this thread, by stage parity
     uint4 dwb[2][Q4 ? 1 : RSM][NCH];
     uint32_t dwq[2][Q4 ? RSM : 1][NCH];
@@ -523,13 +764,12 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
 
     auto step = [&](auto parc, int s) {
       constexpr int par = decltype(parc)::value;
-      uint32_t f0 = 0u, m = 0u;
-      int n = 0;
+      uint32_t m = 0u;
+      int n = 0, su = -1, si0 = 0;
       if (s < n_stages) {
         const int slot = s % NS;
         if (!mbar_wait(&full[slot], (uint32_t)(s / NS) & 1u)) timed_out = true;
-        const bool shared = s < n_sh;
-        stage_rows(s, f0, n);
+        stage_info(s, su, si0, n);
         const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
         // this thread's chunks of every row of the stage, into registers
         uint4 wgb[Q4 ? 1 : RSM][NCH], wub[Q4 ? 1 : RSM][NCH];
@@ -538,9 +778,9 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
 #pragma unroll
         for (int r = 0; r < RSM; ++r) {
           if (r < n) {
-            const uint8_t* rg = sl + (size_t)r * rb;
-            const uint8_t* ru = sl + (size_t)(RS + r) * rb;
-            const uint8_t* rd = sl + (size_t)(2 * RS + r) * rb;
+            const uint8_t* rg = sl + (size_t)r * rp;
+            const uint8_t* ru = sl + (size_t)(RS + r) * rp;
+            const uint8_t* rd = sl + (size_t)(2 * RS + r) * rp;
 #pragma unroll
             for (int k = 0; k < NCH; ++k) {
               const int ch = tid + kRowThreads * k;
@@ -573,20 +813,11 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
             if (s + NS < n_stages) issue(s + NS);
           }
         }
-        // tokens of each row's group
+        // tokens of the stage's group (every row of a stage has the same one)
+        m = su < 0 ? all_tokens : tb.mask[su];
         uint32_t mrow[RSM];
-        {
-          uint32_t u = shared ? 0u : f0 / (uint32_t)P.I, i = shared ? 0u : f0 - u * (uint32_t)P.I;
 #pragma unroll
-          for (int r = 0; r < RSM; ++r) {
-            mrow[r] = r >= n ? 0u : shared ? all_tokens : tb.mask[u];
-            if (!shared && ++i == (uint32_t)P.I) {
-              i = 0;
-              ++u;
-            }
-            m |= mrow[r];
-          }
-        }
+        for (int r = 0; r < RSM; ++r) mrow[r] = r < n ? m : 0u;
         // -- A: partial dots of every row over this thread's chunks; packed
         // in eights, reduced across the warp, one partial per warp
         float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
@@ -704,16 +935,10 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
             u += pp[w * NV + (2 * r + 1) * TMAX + t];
           }
           float h = 0.f;
-          if (s < n_sh) {
+          if (su < 0)
             h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
-          } else {
-            uint32_t uu = f0 / (uint32_t)P.I, ii = f0 - uu * (uint32_t)P.I + r;
-            while (ii >= (uint32_t)P.I) {
-              ii -= P.I;
-              ++uu;
-            }
-            h = (tb.mask[uu] >> t & 1u) ? tb.wt[uu * T + t] * silu_mul(g, u) : 0.f;
-          }
+          else
+            h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
           hb[par * RSM * TMAX + j] = h;
         }
       }
@@ -767,19 +992,37 @@ __global__ void __maxnreg__(224) k_rows(const LayerParams Pk) {
     // once more for the last stages issued
     atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
     for (int s = max(0, n_stages - NS); s < n_stages; ++s) mbar_wait(&full[s % NS], (uint32_t)(s / NS) & 1u);
+    for (int s = max(0, n_stages - P.nsd); s < n_stages; ++s) mbar_wait(&fulld[s % P.nsd], (uint32_t)(s / P.nsd) & 1u);
   }
 
   // ---- partial y of this block
+  if constexpr (MMA_C) {
+    // D fragment j: columns 256w + 16j + lane/4 (and + 8), tokens 2(lane & 3) (and + 1)
+    const int t0 = 2 * (lane & 3);
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t) {
-    if (t >= T) break;
+    for (int j = 0; j < 16; ++j) {
+      const int c = 256 * warp + 16 * j + (lane >> 2);
+      if (t0 < T) {
+        P.partial[((size_t)cta * T + t0) * H + c] = yc[j][0];
+        P.partial[((size_t)cta * T + t0) * H + c + 8] = yc[j][2];
+      }
+      if (t0 + 1 < T) {
+        P.partial[((size_t)cta * T + t0 + 1) * H + c] = yc[j][1];
+        P.partial[((size_t)cta * T + t0 + 1) * H + c + 8] = yc[j][3];
+      }
+    }
+  } else {
 #pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-      const int ch = tid + kRowThreads * k;
-      if (!FAST && ch >= H / 8) break;
-      float4* dst = reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t) * H + 8 * ch);
-      dst[0] = make_float4(y[t][k][0], y[t][k][1], y[t][k][2], y[t][k][3]);
-      dst[1] = make_float4(y[t][k][4], y[t][k][5], y[t][k][6], y[t][k][7]);
+    for (int t = 0; t < TMAX; ++t) {
+      if (t >= T) break;
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        const int ch = tid + kRowThreads * k;
+        if (!FAST && ch >= H / 8) break;
+        float4* dst = reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t) * H + 8 * ch);
+        dst[0] = make_float4(y[t][k][0], y[t][k][1], y[t][k][2], y[t][k][3]);
+        dst[1] = make_float4(y[t][k][4], y[t][k][5], y[t][k][6], y[t][k][7]);
+      }
     }
   }
   // every block's partial, then the sum of this block's columns: the block
