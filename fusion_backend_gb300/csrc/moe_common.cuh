@@ -72,6 +72,11 @@ MOE_DEV void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2, in
       "l"(policy)
       : "memory");
 }
+// Pulls a tensor map (a kernel parameter) into the descriptor cache ahead of
+// its first tensor copy.
+MOE_DEV void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
 // Bulk prefetch of [src, src + bytes) into L2 (hint only; src 16-byte aligned,
 // bytes a multiple of 16).
 MOE_DEV void prefetch_l2(const void* src, uint32_t bytes) {

@@ -256,6 +256,40 @@ MOE_DEV uint32_t muldiv(uint32_t a, uint32_t b, uint32_t d) {
   return (uint32_t)(((unsigned long long)a * b) / d);
 }
 
+// Walks the stages of a block in order without divisions.  Stage k < n_sh
+// is shared group k (counted from the block's first); stage n_sh is routed
+// group g0 of active expert u0, and later stages follow group by group
+// (gI groups per expert).  slot / ph: the ring slot of the stage and the
+// parity of its use of that slot.
+struct StageCursor {
+  int k, u, g, slot;
+  uint32_t ph;
+};
+MOE_DEV void cursor_init(StageCursor& c, int ns) {
+  c.k = -1;
+  c.u = -1;
+  c.g = 0;
+  c.slot = ns - 1;
+  c.ph = 1u;
+}
+MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int ns) {
+  ++c.k;
+  if (c.k < n_sh) {
+    c.u = -1;
+    c.g = c.k;
+  } else if (c.k == n_sh) {
+    c.u = u0;
+    c.g = g0;
+  } else if (++c.g == gI) {
+    ++c.u;
+    c.g = 0;
+  }
+  if (++c.slot == ns) {
+    c.slot = 0;
+    c.ph ^= 1u;
+  }
+}
+
 // ------------------------------------------------------------------- kernel
 // TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048 and
 // E <= 256 (and, for 4-bit weights, an activation exact in fp16).
@@ -273,6 +307,14 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x;
   if (tid == 0) sP = Pk;
+  if constexpr (FAST && !Q4) {
+    // descriptors of the routed maps are first used after the routing, under
+    // load: fetch all four now
+    if (tid == 32) prefetch_tensormap(&Pk.tm_gu_e);
+    if (tid == 64) prefetch_tensormap(&Pk.tm_d_e);
+    if (tid == 96) prefetch_tensormap(&Pk.tm_gu_s);
+    if (tid == 128) prefetch_tensormap(&Pk.tm_d_s);
+  }
   __syncthreads();
   const LayerParams& P = sP;
   const int T = P.T, K = P.K, TK = T * K;
@@ -297,96 +339,65 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // The next call's router blocks may become resident beside this block.
   pdl_launch_dependents();
 
-  // Units of this block.  Shared expert: rows [sa, sb), known now.  Routed:
-  // the run [q0, q1) of the flattened (active expert u, row i) order
-  // f = u * I + i, known after the routing, sized so that shared + routed
-  // rows are balanced over the blocks.  Stage s < n_sh holds shared rows
-  // sa + s*RS ..; stage s >= n_sh holds routed f = q0 + (s - n_sh)*RS ..
-  // (up to RS rows, which may span two experts).
-  const int sa = (int)muldiv(P.Is, cta, P.G), sb = (int)muldiv(P.Is, cta + 1, P.G);
-  const int n_sh = (sb - sa + RS - 1) / RS;
-  uint32_t q0 = 0, q1 = 0;
+  // Units of this block: groups of RS consecutive rows of one expert (the
+  // last group of an expert may be shorter).  Shared groups [gs0, gs1) are
+  // known now; the routed groups are the run [q0, q1) of the flattened
+  // (active expert u, group) order, known after the routing and sized so
+  // that shared + routed groups (stages) are balanced over the blocks.
+  const int gS = (P.Is + RS - 1) / RS, gI = (P.I + RS - 1) / RS;
+  const int gs0 = (int)muldiv(gS, cta, P.G), gs1 = (int)muldiv(gS, cta + 1, P.G);
+  const int n_sh = gs1 - gs0;
   int n_stages = n_sh;
+  int ur0 = 0, gr0 = 0;  // first routed stage: active expert, group in it
 
-  // Stage k -> ring slot k % NS.  A stage holds up to RS consecutive rows of
-  // one expert group: shared stages s < n_sh take rows sa + s*RS ..; the
-  // routed run [q0, q1) of the flattened (active expert u, row i) order is cut
-  // at every expert boundary into stages of RS rows.
   const uint8_t* const r_expert_w = P.expert_w;
   const uint8_t* const r_shexp_w = P.shexp_w;
   const long long r_expert_bytes = P.expert_bytes;
   const long long r_mat = (long long)P.I * rb, r_smat = (long long)P.Is * rb;
-  const int r_I = P.I, r_stage_bytes = P.stage_bytes;
+  const int r_I = P.I, r_Is = P.Is, r_stage_bytes = P.stage_bytes;
   const long long rp = P.rp;
-  // stage k -> (active index u, or -1 for the shared expert; first row; rows)
-  auto stage_info = [&](int k, int& u, int& i0, int& n) {
-    if (k < n_sh) {
-      u = -1;
-      i0 = sa + k * RS;
-      n = min(RS, sb - i0);
-      return;
-    }
-    int j = k - n_sh;
-    uint32_t left = q1 - q0, uu = q0 / (uint32_t)r_I, ii = q0 - uu * (uint32_t)r_I;
-    for (;;) {
-      const uint32_t seg = min((uint32_t)r_I - ii, left);
-      const int ns = (int)((seg + RS - 1) / RS);
-      if (j < ns) {
-        u = (int)uu;
-        i0 = (int)ii + j * RS;
-        n = min(RS, (int)seg - j * RS);
-        return;
-      }
-      j -= ns;
-      left -= seg;
-      ++uu;
-      ii = 0;
+  // first row and row count of the stage a cursor stands on
+  auto rows_of = [&](const StageCursor& c, int& i0, int& n) {
+    if (c.u < 0) {
+      i0 = (gs0 + c.g) * RS;
+      n = min(RS, r_Is - i0);
+    } else {
+      i0 = c.g * RS;
+      n = min(RS, r_I - i0);
     }
   };
-  // Tensor-core path: the downT box of stage k into its own ring.
-  auto issue_d = [&](int k) {
-    const int slot = k % P.nsd;
-    int u, i0, n;
-    stage_info(k, u, i0, n);
-    const int e = u < 0 ? 0 : tb.active[u];
-    const void* dm = u < 0 ? (const void*)&Pk.tm_d_s : (const void*)&Pk.tm_d_e;
-    mbar_arrive_expect_tx(&fulld[slot], (uint32_t)(kRsMaxB16 * rb));
-    tma_load_5d(dring + (size_t)slot * kRsMaxB16 * rb, dm, 0, i0, 2, 0, e, &fulld[slot], pol);
+  auto advance = [&](StageCursor& c, int ns) { cursor_next(c, n_sh, ur0, gr0, gI, ns); };
+  // Tensor-core path: the downT box of a stage into its own ring.
+  auto issue_d = [&](const StageCursor& c) {
+    int i0, n;
+    rows_of(c, i0, n);
+    const int e = c.u < 0 ? 0 : tb.active[c.u];
+    const void* dm = c.u < 0 ? (const void*)&Pk.tm_d_s : (const void*)&Pk.tm_d_e;
+    mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(kRsMaxB16 * rb));
+    tma_load_5d(dring + (size_t)c.slot * kRsMaxB16 * rb, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
   };
-  auto routed_stage_count = [&]() {
-    int cnt = 0;
-    uint32_t left = q1 - q0, ii = q0 % (uint32_t)r_I;
-    while (left > 0) {
-      const uint32_t seg = min((uint32_t)r_I - ii, left);
-      cnt += (int)((seg + RS - 1) / RS);
-      left -= seg;
-      ii = 0;
-    }
-    return cnt;
-  };
-  // One thread issues stage k.  Tensor-core path: two tiled tensor copies,
-  // the stage's 4 gate + 4 up rows and its 4 downT rows (whole boxes; rows
-  // past the stage are loaded, or zero-filled past the matrix, and unused).
-  // Otherwise three bulk copies of the n rows of each matrix.
-  auto issue = [&](int k) {
-    const int slot = k % NS;
-    uint8_t* dst = ring + (size_t)slot * r_stage_bytes;
-    uint64_t* bar = &full[slot];
-    int u, i0, n;
-    stage_info(k, u, i0, n);
+  // One thread issues a stage.  Tensor-core path: one tiled tensor copy of
+  // the stage's gate + up rows (a whole box; rows past the matrix are
+  // zero-filled and unused).  Otherwise three bulk copies of the n rows of
+  // each matrix.
+  auto issue = [&](const StageCursor& c) {
+    uint8_t* dst = ring + (size_t)c.slot * r_stage_bytes;
+    uint64_t* bar = &full[c.slot];
+    int i0, n;
+    rows_of(c, i0, n);
     if constexpr (FAST && !Q4) {
-      const int e = u < 0 ? 0 : tb.active[u];
-      const void* gu = u < 0 ? (const void*)&Pk.tm_gu_s : (const void*)&Pk.tm_gu_e;
+      const int e = c.u < 0 ? 0 : tb.active[c.u];
+      const void* gu = c.u < 0 ? (const void*)&Pk.tm_gu_s : (const void*)&Pk.tm_gu_e;
       mbar_arrive_expect_tx(bar, (uint32_t)r_stage_bytes);
       tma_load_5d(dst, gu, 0, i0, 0, 0, e, bar, pol);
     } else {
       const uint8_t* src;
       long long mat;
-      if (u < 0) {
+      if (c.u < 0) {
         src = r_shexp_w + (long long)i0 * rb;
         mat = r_smat;
       } else {
-        src = r_expert_w + (long long)tb.active[u] * r_expert_bytes + (long long)i0 * rb;
+        src = r_expert_w + (long long)tb.active[c.u] * r_expert_bytes + (long long)i0 * rb;
         mat = r_mat;
       }
       const uint32_t bytes = (uint32_t)(n * rb);
@@ -396,9 +407,18 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       bulk_g2s(dst + (size_t)2 * RS * rp, src + 2 * mat, bytes, bar, pol);
     }
   };
+  // Issue cursors (main ring, downT ring): every thread advances them in
+  // step so that any thread can issue.
+  StageCursor ci, cd;
+  cursor_init(ci, NS);
+  cursor_init(cd, P.nsd > 0 ? P.nsd : 1);
 
-  // ---- shared-expert stages: issued before the wait (weights do not depend
-  // on the previous kernel), by warp 0
+  // ---- barriers, a cleared routing table, and the shared-expert stages
+  // issued before the wait (their weights do not depend on the previous
+  // kernel)
+  for (int i = tid; i < (P.E + 31) / 32; i += kRowThreads) tb.bitmap[i] = 0u;
+  for (int i = tid; i < TK; i += kRowThreads) tb.mask[i] = 0u;
+  for (int i = tid; i < TK * T; i += kRowThreads) tb.wt[i] = 0.f;
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
@@ -407,11 +427,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     for (int i = 0; i < P.nsd; ++i) mbar_init(&fulld[i], 1);
     mbar_init(xbar, 1);
     mbar_fence_init();
-    for (int k = 0; k < min(n_sh, NS); ++k) issue(k);
-    if constexpr (FAST && !Q4)
-      for (int k = 0; k < min(n_sh, P.nsd); ++k) issue_d(k);
   }
   __syncthreads();
+  for (int k = 0; k < min(n_sh, NS); ++k) {
+    advance(ci, NS);
+    if (tid == 0) issue(ci);
+  }
+  if constexpr (FAST && !Q4)
+    for (int k = 0; k < min(n_sh, P.nsd); ++k) {
+      advance(cd, P.nsd);
+      if (tid == 0) issue_d(cd);
+    }
 
   // ---- the router's logits, the activation and (block form) x_res are ready
   pdl_wait();
@@ -425,20 +451,21 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     bulk_g2s(xs, P.x, bytes, xbar, policy_evict_last());
   }
   // routing, every block from the router's logits: top-k of token t on warp
-  // 7 - t (the chosen experts and their softmax weights) and the shared gate
-  // sigmoid(logit_E)
+  // 7 - t (the chosen experts, their softmax weights and their bits in the
+  // selection bitmap) and the shared gate sigmoid(logit_E)
   {
     const int t = kRowWarps - 1 - warp;
     if (t < T) {
       float sl = 0.f;
       if (lane == 0) sl = __ldcg(P.logits + (size_t)t * P.ls + P.E);
       warp_topk<EPL>(P.logits + (size_t)t * P.ls, P.E, K, tb.ids + t * K, tb.p + t * K);
+      if (lane < K) {
+        const int e = tb.ids[t * K + lane];
+        atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
+      }
       if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-sl));
     }
   }
-  for (int i = tid; i < (P.E + 31) / 32; i += kRowThreads) tb.bitmap[i] = 0u;
-  for (int i = tid; i < TK; i += kRowThreads) tb.mask[i] = 0u;
-  for (int i = tid; i < TK * T; i += kRowThreads) tb.wt[i] = 0.f;
   if (!mbar_wait(xbar, 0)) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
   // block form: RMSNorm factors of the fp32 rows (warp t)
   if (P.block_mode) {
@@ -452,9 +479,51 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   }
   __syncthreads();
-  for (int ts = tid; ts < TK; ts += kRowThreads) {
-    const int e = tb.ids[ts];
-    atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
+  if (warp == 0) {
+    // active experts in ascending order (active index u): bitmap word l on
+    // lane l, an exclusive scan of the word counts
+    const int nw = (P.E + 31) / 32;
+    const uint32_t w = lane < nw ? tb.bitmap[lane] : 0u;
+    const int c = __popc(w);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int U = __shfl_sync(0xffffffffu, incl, 31);
+    int u = incl - c;
+    for (uint32_t m = w; m; m &= m - 1u, ++u) {
+      const int e = 32 * lane + __ffs((int)m) - 1;
+      tb.active[u] = e;
+      tb.inv_u[e] = static_cast<int16_t>(u);
+    }
+    __syncwarp();
+    // tokens of every active expert and their weights
+    for (int t = 0; t < T; ++t)
+      for (int k = lane; k < K; k += 32) {
+        const int ts = t * K + k;
+        const int ua = tb.inv_u[tb.ids[ts]];
+        atomicOr(&tb.mask[ua], 1u << t);
+        tb.wt[ua * T + t] = tb.p[ts];
+      }
+    if (lane == 0) {
+      // routed groups [q0, q1) of this block
+      const uint32_t R = (uint32_t)U * (uint32_t)gI, G = P.G, cc = cta;
+      uint32_t q0, q1;
+      if (R >= G) {
+        q0 = muldiv(R + gS, cc, G) - gs0;
+        q1 = muldiv(R + gS, cc + 1, G) - gs1;
+      } else {
+        q0 = muldiv(R, cc, G);
+        q1 = muldiv(R, cc + 1, G);
+      }
+      const uint32_t u0 = q0 / (uint32_t)gI;
+      tb.misc[0] = U;
+      tb.misc[1] = (int)(q1 - q0);
+      tb.misc[2] = (int)u0;
+      tb.misc[3] = (int)(q0 - u0 * (uint32_t)gI);
+    }
   }
   // activation in its compute form.  Fast shapes: this thread's 8 columns
   // c0 = 8 * tid of every token, in registers (bf16 pairs, or for 4-bit
@@ -508,36 +577,20 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   }
   __syncthreads();
-  // active index of an expert = selected experts below it
-  int U = 0;
-  for (int w = 0; w < (P.E + 31) / 32; ++w) U += __popc(tb.bitmap[w]);
-  for (int ts = tid; ts < TK; ts += kRowThreads) {
-    const int e = tb.ids[ts], t = ts / K;
-    int u = __popc(tb.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-    for (int w = 0; w < (e >> 5); ++w) u += __popc(tb.bitmap[w]);
-    tb.active[u] = e;
-    tb.inv_u[e] = static_cast<int16_t>(u);
-    atomicOr(&tb.mask[u], 1u << t);
-    tb.wt[u * T + t] = tb.p[ts];
+  const int U = tb.misc[0];
+  n_stages = n_sh + tb.misc[1];
+  ur0 = tb.misc[2];
+  gr0 = tb.misc[3];
+  // the first routed stages of the rings
+  while (ci.k + 1 < min(n_stages, NS)) {
+    advance(ci, NS);
+    if (tid == 0) issue(ci);
   }
-  {
-    const uint32_t R = (uint32_t)U * (uint32_t)P.I, Is = P.Is, G = P.G, c = cta;
-    if (R >= 2 * G) {
-      q0 = muldiv(R + Is, c, G) - muldiv(Is, c, G);
-      q1 = muldiv(R + Is, c + 1, G) - muldiv(Is, c + 1, G);
-    } else {
-      q0 = muldiv(R, c, G);
-      q1 = muldiv(R, c + 1, G);
+  if constexpr (FAST && !Q4)
+    while (cd.k + 1 < min(n_stages, P.nsd)) {
+      advance(cd, P.nsd);
+      if (tid == 0) issue_d(cd);
     }
-    n_stages = n_sh + routed_stage_count();
-  }
-  __syncthreads();
-  // the first routed stages of the ring
-  if (tid == 0) {
-    for (int k = n_sh; k < min(n_stages, NS); ++k) issue(k);
-    if constexpr (FAST && !Q4)
-      for (int k = n_sh; k < min(n_stages, P.nsd); ++k) issue_d(k);
-  }
   if (cta == 0 && warp == kRowWarps - 1) {
     // routing outputs for the caller and the test readers: counts, offsets
     // (a scan over the experts) and the stable token-major permutation
@@ -644,12 +697,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         xa[ks][1] = w1;
       }
     }
+    StageCursor cs;
+    cursor_init(cs, NS);
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    uint32_t dph = 1u;
     for (int s = 0; s < n_stages; ++s) {
-      const int slot = s % NS;
-      if (!mbar_wait(&full[slot], (uint32_t)(s / NS) & 1u)) timed_out = true;
-      int su, si0, n;
-      stage_info(s, su, si0, n);
-      const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
+      advance(cs, NS);
+      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+      const int su = cs.u;
+      int si0, n;
+      rows_of(cs, si0, n);
+      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
       // -- A (four accumulators, so the tensor-core steps do not chain).  B
       // column n = lane / 4 is row n of the gate + up box (lines chunk * 8 + n).
       float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -684,9 +742,13 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       named_bar_sync(kBarStage, kRowThreads);
       // every warp is done with this stage's gate + up box and with the
       // previous stage's downT box: both slots take their next stages
-      if (tid == kRowThreads - 1) {
-        if (s + NS < n_stages) issue(s + NS);
-        if (s >= 1 && s - 1 + P.nsd < n_stages) issue_d(s - 1 + P.nsd);
+      if (s + NS < n_stages) {
+        advance(ci, NS);
+        if (tid == kRowThreads - 1) issue(ci);
+      }
+      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+        advance(cd, P.nsd);
+        if (tid == kRowThreads - 1) issue_d(cd);
       }
       // -- A2: value j = (row, token) on thread (j % 8) * 32 + j / 8
       {
@@ -709,8 +771,12 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
       named_bar_sync(kBarStage, kRowThreads);
       // -- C
-      if (!mbar_wait(&fulld[s % P.nsd], (uint32_t)(s / P.nsd) & 1u)) timed_out = true;
-      const uint8_t* dbox = dring + (size_t)(s % P.nsd) * kRsMaxB16 * rb;
+      if (++dslot == P.nsd) {
+        dslot = 0;
+        dph ^= 1u;
+      }
+      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
+      const uint8_t* dbox = dring + (size_t)dslot * kRsMaxB16 * rb;
       if constexpr (!MMA_C) {
         // CUDA cores (one or two tokens): chunk tid of every downT row
         const int k = 8 * tid;
@@ -761,15 +827,19 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     uint16_t dsc[2][Q4 ? RSM : 1][NCH];
     int n_prev = 0;
     uint32_t m_prev = 0u;
+    StageCursor cs;
+    cursor_init(cs, NS);
 
     auto step = [&](auto parc, int s) {
       constexpr int par = decltype(parc)::value;
       uint32_t m = 0u;
       int n = 0, su = -1, si0 = 0;
       if (s < n_stages) {
-        const int slot = s % NS;
-        if (!mbar_wait(&full[slot], (uint32_t)(s / NS) & 1u)) timed_out = true;
-        stage_info(s, su, si0, n);
+        advance(cs, NS);
+        const int slot = cs.slot;
+        if (!mbar_wait(&full[slot], cs.ph)) timed_out = true;
+        su = cs.u;
+        rows_of(cs, si0, n);
         const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
         // this thread's chunks of every row of the stage, into registers
         uint4 wgb[Q4 ? 1 : RSM][NCH], wub[Q4 ? 1 : RSM][NCH];
@@ -805,12 +875,14 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         // release the slot: the warp's loads are ordered before its arrival
         // (warp barrier, then a CTA-scope fence), and the last warp to
         // arrive refills the slot at once
+        const bool refill = s + NS < n_stages;
+        if (refill) advance(ci, NS);
         __syncwarp();
         if (lane == 0) {
           __threadfence_block();
           if (atomicAdd(&scnt[slot], 1) == kRowWarps - 1) {
             scnt[slot] = 0;
-            if (s + NS < n_stages) issue(s + NS);
+            if (refill) issue(ci);
           }
         }
         // tokens of the stage's group (every row of a stage has the same one)
