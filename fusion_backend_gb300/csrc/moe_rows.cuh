@@ -65,14 +65,16 @@ struct RowTab {
   int32_t* active;   // [T*K] selected experts, ascending
   uint32_t* mask;    // [T*K] tokens of active expert u (bit t)
   float* wt;         // [T*K][T] weight of token t for active expert u (0 if not routed)
-  int32_t* misc;     // spare
+  int32_t* misc;     // [4] the number of active experts U
+  int32_t* qtab;     // [T*K - K + 1][4] per possible U: routed stages, first active expert, first group
 };
 
 __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTab* v) {
   const int TK = T * K;
-  const int sz[10] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4};
-  int off = 0, o[10];
-  for (int i = 0; i < 10; ++i) {
+  const int sz[11] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
+                      (TK - K + 1) * 16};
+  int off = 0, o[11];
+  for (int i = 0; i < 11; ++i) {
     o[i] = off;
     off += (sz[i] + 15) & ~15;
   }
@@ -87,6 +89,7 @@ __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTa
     v->mask = reinterpret_cast<uint32_t*>(base + o[7]);
     v->wt = reinterpret_cast<float*>(base + o[8]);
     v->misc = reinterpret_cast<int32_t*>(base + o[9]);
+    v->qtab = reinterpret_cast<int32_t*>(base + o[10]);
   }
   return off;
 }
@@ -419,6 +422,25 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   for (int i = tid; i < (P.E + 31) / 32; i += kRowThreads) tb.bitmap[i] = 0u;
   for (int i = tid; i < TK; i += kRowThreads) tb.mask[i] = 0u;
   for (int i = tid; i < TK * T; i += kRowThreads) tb.wt[i] = 0.f;
+  // the routed run of this block for every possible count U of active
+  // experts (K <= U <= min(E, T K)): groups [q0, q1) of the flattened
+  // (active expert, group) order, so that shared + routed groups are
+  // balanced over the blocks
+  for (int j = tid; j <= min(P.E, TK) - K; j += kRowThreads) {
+    const uint32_t R = (uint32_t)(K + j) * (uint32_t)gI, G = P.G, cc = cta;
+    uint32_t q0, q1;
+    if (R >= G) {
+      q0 = muldiv(R + gS, cc, G) - gs0;
+      q1 = muldiv(R + gS, cc + 1, G) - gs1;
+    } else {
+      q0 = muldiv(R, cc, G);
+      q1 = muldiv(R, cc + 1, G);
+    }
+    const uint32_t u0 = q0 / (uint32_t)gI;
+    tb.qtab[4 * j] = (int)(q1 - q0);
+    tb.qtab[4 * j + 1] = (int)u0;
+    tb.qtab[4 * j + 2] = (int)(q0 - u0 * (uint32_t)gI);
+  }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
@@ -507,23 +529,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         atomicOr(&tb.mask[ua], 1u << t);
         tb.wt[ua * T + t] = tb.p[ts];
       }
-    if (lane == 0) {
-      // routed groups [q0, q1) of this block
-      const uint32_t R = (uint32_t)U * (uint32_t)gI, G = P.G, cc = cta;
-      uint32_t q0, q1;
-      if (R >= G) {
-        q0 = muldiv(R + gS, cc, G) - gs0;
-        q1 = muldiv(R + gS, cc + 1, G) - gs1;
-      } else {
-        q0 = muldiv(R, cc, G);
-        q1 = muldiv(R, cc + 1, G);
-      }
-      const uint32_t u0 = q0 / (uint32_t)gI;
-      tb.misc[0] = U;
-      tb.misc[1] = (int)(q1 - q0);
-      tb.misc[2] = (int)u0;
-      tb.misc[3] = (int)(q0 - u0 * (uint32_t)gI);
-    }
+    if (lane == 0) tb.misc[0] = U;
   }
   // activation in its compute form.  Fast shapes: this thread's 8 columns
   // c0 = 8 * tid of every token, in registers (bf16 pairs, or for 4-bit
@@ -578,19 +584,25 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   }
   __syncthreads();
   const int U = tb.misc[0];
-  n_stages = n_sh + tb.misc[1];
-  ur0 = tb.misc[2];
-  gr0 = tb.misc[3];
-  // the first routed stages of the rings
-  while (ci.k + 1 < min(n_stages, NS)) {
-    advance(ci, NS);
-    if (tid == 0) issue(ci);
+  {
+    const int32_t* q = tb.qtab + 4 * (U - K);
+    n_stages = n_sh + q[0];
+    ur0 = q[1];
+    gr0 = q[2];
   }
-  if constexpr (FAST && !Q4)
-    while (cd.k + 1 < min(n_stages, P.nsd)) {
-      advance(cd, P.nsd);
-      if (tid == 0) issue_d(cd);
+  // the first routed stages of the rings, issued by the warps in turn
+  {
+    int j = 0;
+    while (ci.k + 1 < min(n_stages, NS)) {
+      advance(ci, NS);
+      if (tid == 32 * (j++ & (kRowWarps - 1))) issue(ci);
     }
+    if constexpr (FAST && !Q4)
+      while (cd.k + 1 < min(n_stages, P.nsd)) {
+        advance(cd, P.nsd);
+        if (tid == 32 * (j++ & (kRowWarps - 1))) issue_d(cd);
+      }
+  }
   if (cta == 0 && warp == kRowWarps - 1) {
     // routing outputs for the caller and the test readers: counts, offsets
     // (a scan over the experts) and the stable token-major permutation
