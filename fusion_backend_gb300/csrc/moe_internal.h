@@ -19,6 +19,7 @@ constexpr int kMaxH = 4096;       // H of the decode path (bf16: multiple of 8, 
 constexpr int kSmemBudget = 220 * 1024;  // row kernel: leaves room for a router block on the SM
 constexpr int kMaxGrid = 192;            // row kernel blocks (one per SM, at most this many)
 constexpr int kStatusTimeout = -6;       // device status word: a bounded wait gave up
+constexpr int kXPitch = 4160;            // tensor-core loops: bytes per token row of x fragments (4 KB + 64)
 
 // Control words at the start of the workspace.  The router kernel of each
 // call zeroes them before the row kernel of that call reads them.

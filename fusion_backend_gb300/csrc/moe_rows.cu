@@ -13,9 +13,9 @@ cudaError_t launch_rows_generic(const LayerParams& p, cudaStream_t stream);
 
 namespace {
 
-// The fast instances: H = 2048, E <= 256, and an activation that bf16 (and
-// so fp16) holds exactly -- bf16 x, or the block form whose normalised input
-// is bf16 -- kept packed in registers; 4-bit weights form fp16 products.
+// The fast (tensor-core) instances: H = 2048, E <= 256, and an activation
+// that bf16 holds exactly -- bf16 x, or the block form whose normalised
+// input is bf16 -- so that it enters the bf16 products unchanged.
 bool rows_fast(const LayerParams& p) { return p.H == 2048 && p.E <= 256 && (p.act == 1 || p.block_mode); }
 
 int align128(int v) { return (v + 127) & ~127; }
@@ -38,7 +38,7 @@ static bool rows_layout_rs(LayerParams& p, int rs, int xbytes, int tab, int tmax
   // the end-of-kernel column sums reuse the ring: max(threads, T x columns) floats
   const int red_bytes = std::max(kRowThreads, p.T * ((p.H + p.G - 1) / p.G)) * 4;
   const int avail = kSmemBudget - 1024 - p.off_ring;  // 1024: slack to align the ring in the shared window
-  if (rows_fast(p) && p.wfmt == 0) {
+  if (rows_fast(p)) {
     // tensor-core path: a ring of gate + up boxes (2 rs rows) and a ring of
     // downT boxes (rs rows) with one slot more
     p.stage_bytes = 2 * rs * p.rp;
@@ -70,7 +70,8 @@ int rows_layout(LayerParams& p) {
   // x region: the bulk copy of the source rows (fp32 for fp32 x and the block
   // form, else bf16), rewritten in place into the compute form
   const bool src4 = p.act == 0 || p.block_mode;
-  const int xbytes = p.T * p.H * (p.xmode == kXF32 || src4 ? 4 : 2);
+  int xbytes = p.T * p.H * (p.xmode == kXF32 || src4 ? 4 : 2);
+  if (fast) xbytes = std::max(xbytes, p.T * kXPitch);  // rewritten in place as A fragments
   const int tab = row_tab(nullptr, p.T, p.K, p.E, nullptr);
   // Rows per stage: the choice that keeps the most bytes in flight (all ns
   // stages), with at least 3 stages in the ring; ties go to larger stages.
@@ -79,7 +80,7 @@ int rows_layout(LayerParams& p) {
   long long best_flight = -1;
   for (int r = 0; r < 4; ++r) {
     if (rs_list[r] > (q4 ? kRsMaxQ4 : kRsMaxB16)) continue;
-    if (fast && !q4 && rs_list[r] != kRsMaxB16) continue;  // tensor-core stages: 4 rows
+    if (fast && rs_list[r] != (q4 ? kRsMaxQ4 : kRsMaxB16)) continue;  // tensor-core stages: fixed rows
     LayerParams t = p;
     if (!rows_layout_rs(t, rs_list[r], xbytes, tab, tmax)) continue;
     const long long flight = (long long)t.ns * t.stage_bytes + (long long)t.nsd * t.rs * t.rp;
@@ -109,17 +110,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 5-D view of an expert block sequence [E][3 matrices][I rows][H] of bf16:
-// (64 elements, row, matrix, 64-element chunk, expert), and a box of
-// `rows` rows x `mats` matrices x all H/64 chunks of one expert, stored in
-// shared memory as [chunk][matrix][row][64] with the 128-byte swizzle.
-bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int H, int I, int E,
+// 5-D byte view of an expert block sequence [E][3 matrices][I rows][rb bytes]
+// (a bf16 row, or a 4-bit row of nibbles + scales): (128 bytes, row, matrix,
+// 128-byte chunk, expert), and a box of `rows` rows x `mats` matrices x all
+// rb/128 chunks of one expert, stored in shared memory as
+// [chunk][matrix][row][128 bytes] with the 128-byte swizzle.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int rb, int I, int E,
                  int rows, int mats) {
-  const cuuint64_t dims[5] = {64, (cuuint64_t)I, 3, (cuuint64_t)(H / 64), (cuuint64_t)E};
-  const cuuint64_t strides[4] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, 128, (cuuint64_t)3 * I * H * 2};
-  const cuuint32_t box[5] = {64, (cuuint32_t)rows, (cuuint32_t)mats, (cuuint32_t)(H / 64), 1};
+  if (rb % 128) return false;
+  const cuuint64_t dims[5] = {128, (cuuint64_t)I, 3, (cuuint64_t)(rb / 128), (cuuint64_t)E};
+  const cuuint64_t strides[4] = {(cuuint64_t)rb, (cuuint64_t)I * rb, 128, (cuuint64_t)3 * I * rb};
+  const cuuint32_t box[5] = {128, (cuuint32_t)rows, (cuuint32_t)mats, (cuuint32_t)(rb / 128), 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -127,13 +130,15 @@ bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const voi
 }  // namespace
 
 cudaError_t rows_tensor_maps(LayerParams& p) {
-  if (!(rows_fast(p) && p.wfmt == 0)) return cudaSuccess;
+  if (!rows_fast(p)) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, p.H, p.I, p.E, kRsMaxB16, 2) ||
-      !encode_rows(fn, &p.tm_d_e, p.expert_w, p.H, p.I, p.E, kRsMaxB16, 1) ||
-      !encode_rows(fn, &p.tm_gu_s, p.shexp_w, p.H, p.Is, 1, kRsMaxB16, 2) ||
-      !encode_rows(fn, &p.tm_d_s, p.shexp_w, p.H, p.Is, 1, kRsMaxB16, 1))
+  const int rs = p.wfmt == 1 ? kRsMaxQ4 : kRsMaxB16;
+  const int rb = (int)p.rb;
+  if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, rb, p.I, p.E, rs, 2) ||
+      !encode_rows(fn, &p.tm_d_e, p.expert_w, rb, p.I, p.E, rs, 1) ||
+      !encode_rows(fn, &p.tm_gu_s, p.shexp_w, rb, p.Is, 1, rs, 2) ||
+      !encode_rows(fn, &p.tm_d_s, p.shexp_w, rb, p.Is, 1, rs, 1))
     return cudaErrorInvalidValue;
   return cudaSuccess;
 }

@@ -224,6 +224,21 @@ MOE_DEV void x8_from_smem(const uint8_t* row, int src4, int block_mode, float hi
   }
 }
 
+// Two activations of one row, columns c0, c0+1 (c0 even), as x8_from_smem.
+MOE_DEV void x2_from_smem(const uint8_t* row, int src4, int block_mode, float hi, float lo, int c0, float* xf) {
+  if (src4) {
+    const float2 a = *reinterpret_cast<const float2*>(row + (size_t)c0 * 4);
+    xf[0] = block_mode ? norm_apply(a.x, hi, lo) : a.x;
+    xf[1] = block_mode ? norm_apply(a.y, hi, lo) : a.y;
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(row + (size_t)c0 * 2);
+    xf[0] = bf16_lo(v);
+    xf[1] = bf16_hi(v);
+  }
+}
+// bf16 pair of two bf16-exact floats (their upper halves), a low.
+MOE_DEV uint32_t bf16_pair_exact(float a, float b) { return (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u); }
+
 // ------------------------------------------------------------ tensor cores
 // D += A B, m16n8k16, bf16 operands, fp32 accumulators (A row-major 16x16,
 // B column-major 16x8), fragments as in the PTX ISA for mma.m16n8k16.
@@ -232,6 +247,26 @@ MOE_DEV void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t 
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D += A B, m16n8k8, bf16 operands, fp32 accumulators (A row-major 16x8:
+// a0 rows lane/4, a1 rows lane/4 + 8, k pair 2(lane & 3); B k pair
+// 2(lane & 3) of column lane/4).
+MOE_DEV void mma_bf16_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+// Two 4-bit codes (bits 0-3 and 16-19 of v) -> the bf16 pair (code - 8):
+// 0x4300 | n is the bf16 of 128 + n, and 128 + n - 136 is exact.
+MOE_DEV uint32_t q4_pair_bf16(uint32_t v) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(lop3_and_or(v, 0x000F000Fu, 0x43004300u)), "r"(0x43084308u));
+  return r;
+}
+// Scale k (0..7) of the 8 fp16 values in a 16-byte unit, as a float.
+MOE_DEV float half_at(const uint4& v, int k) {
+  const uint32_t w = k < 2 ? v.x : k < 4 ? v.y : k < 6 ? v.z : v.w;
+  return __half2float(__ushort_as_half(static_cast<unsigned short>((k & 1) ? (w >> 16) : (w & 0xFFFFu))));
 }
 // Four 8x8 b16 matrices, transposed, from the shared-memory row address this
 // lane supplies (lanes 8q .. 8q+7 give the 8 rows of matrix q).
@@ -294,12 +329,14 @@ MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int n
 }
 
 // ------------------------------------------------------------------- kernel
-// TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048 and
-// E <= 256 (and, for 4-bit weights, an activation exact in fp16).
+// TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048,
+// E <= 256 and a bf16-exact activation (the tensor-core loops).
 template <int TMAX, bool Q4, bool FAST, int NCH>
 __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
-  constexpr bool H16 = Q4 && FAST;           // fp16 activation + half2 products
-  constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // tensor-core down projection
+  constexpr bool H16 = false;                // (generic instances only)
+  constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // bf16: tensor-core down projection
+  constexpr bool Q4C = FAST && Q4;                  // 4-bit tensor-core loop
+  constexpr bool Q4MC = Q4C && TMAX >= 4;           // 4-bit: tensor-core down projection
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
   extern __shared__ __align__(128) uint8_t sm[];
@@ -310,7 +347,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x;
   if (tid == 0) sP = Pk;
-  if constexpr (FAST && !Q4) {
+  if constexpr (FAST) {
     // descriptors of the routed maps are first used after the routing, under
     // load: fetch all four now
     if (tid == 32) prefetch_tensormap(&Pk.tm_gu_e);
@@ -376,8 +413,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     rows_of(c, i0, n);
     const int e = c.u < 0 ? 0 : tb.active[c.u];
     const void* dm = c.u < 0 ? (const void*)&Pk.tm_d_s : (const void*)&Pk.tm_d_e;
-    mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(kRsMaxB16 * rb));
-    tma_load_5d(dring + (size_t)c.slot * kRsMaxB16 * rb, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
+    mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(RS * rb));
+    tma_load_5d(dring + (size_t)c.slot * RS * rb, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
   };
   // One thread issues a stage.  Tensor-core path: one tiled tensor copy of
   // the stage's gate + up rows (a whole box; rows past the matrix are
@@ -388,7 +425,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     uint64_t* bar = &full[c.slot];
     int i0, n;
     rows_of(c, i0, n);
-    if constexpr (FAST && !Q4) {
+    if constexpr (FAST) {
       const int e = c.u < 0 ? 0 : tb.active[c.u];
       const void* gu = c.u < 0 ? (const void*)&Pk.tm_gu_s : (const void*)&Pk.tm_gu_e;
       mbar_arrive_expect_tx(bar, (uint32_t)r_stage_bytes);
@@ -455,7 +492,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     advance(ci, NS);
     if (tid == 0) issue(ci);
   }
-  if constexpr (FAST && !Q4)
+  if constexpr (FAST)
     for (int k = 0; k < min(n_sh, P.nsd); ++k) {
       advance(cd, P.nsd);
       if (tid == 0) issue_d(cd);
@@ -531,32 +568,44 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     if (lane == 0) tb.misc[0] = U;
   }
-  // activation in its compute form.  Fast shapes: this thread's 8 columns
-  // c0 = 8 * tid of every token, in registers (bf16 pairs, or for 4-bit
-  // weights the packed fp16 pairs of the dequantised order).  Other shapes: fp32
-  // rows rewritten in place in shared memory (all reads of the source
-  // precede the barrier, all writes follow it).
-  uint32_t xb[FAST && !Q4 ? TMAX : 1][4];  // bf16 pairs (the activation is bf16-exact)
-  uint32_t xh[FAST && Q4 ? TMAX : 1][4];
-  if (FAST) {
+  // activation in its compute form, in place.  Fast shapes: the bf16 A
+  // fragments of the tensor-core loops, token t's row at t * kXPitch, 16
+  // bytes per (warp slice w, 32-column block kp, lane quad q) -- unit
+  // tid = (8w + kp) * 4 + q, the fragments of steps 2kp and 2kp + 1.
+  // Other shapes: fp32 rows.  All reads of the source precede the barrier,
+  // all writes follow it.
+  uint32_t xb[1][4];  // (generic instances only)
+  uint32_t xh[1][4];
+  if constexpr (FAST) {
+    uint32_t fr[TMAX][4];
+    const int w = tid >> 5, kp = (tid >> 2) & 7, q = tid & 3;
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
-      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (t < T)
-        x8_from_smem(xs + (size_t)t * H * (src4 ? 4 : 2), src4, P.block_mode, P.block_mode ? tb.inv[2 * t] : 0.f,
-                     P.block_mode ? tb.inv[2 * t + 1] : 0.f, 8 * tid, v);
-      if (!Q4) {
+      fr[t][0] = fr[t][1] = fr[t][2] = fr[t][3] = 0u;
+      if (t < T) {
+        const uint8_t* row = xs + (size_t)t * H * (src4 ? 4 : 2);
+        const float hi = P.block_mode ? tb.inv[2 * t] : 0.f, lo = P.block_mode ? tb.inv[2 * t + 1] : 0.f;
+        if constexpr (Q4) {
+          // 4-bit loop: step 2kp + h, pair e = (x[c + 2h + e], x[c + 2h + e + 4]), c = 256w + 32kp + 8q
+          float v[8];
+          x8_from_smem(row, src4, P.block_mode, hi, lo, 256 * w + 32 * kp + 8 * q, v);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          xb[FAST && !Q4 ? t : 0][e] = (__float_as_uint(v[2 * e]) >> 16) | (__float_as_uint(v[2 * e + 1]) & 0xFFFF0000u);
-      } else {
-        const uint4 q = pack_quarter(v);
-        xh[FAST && Q4 ? t : 0][0] = q.x;
-        xh[FAST && Q4 ? t : 0][1] = q.y;
-        xh[FAST && Q4 ? t : 0][2] = q.z;
-        xh[FAST && Q4 ? t : 0][3] = q.w;
+          for (int j = 0; j < 4; ++j) fr[t][j] = bf16_pair_exact(v[j], v[j + 4]);
+        } else {
+          // bf16 loop: step 2kp + h, pair e = x[k0 + 8e], x[k0 + 8e + 1], k0 = 256w + 32kp + 16h + 2q
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float v[2];
+            x2_from_smem(row, src4, P.block_mode, hi, lo, 256 * w + 32 * kp + 16 * (j >> 1) + 8 * (j & 1) + 2 * q, v);
+            fr[t][j] = bf16_pair_exact(v[0], v[1]);
+          }
+        }
       }
     }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+      if (t < T) *reinterpret_cast<uint4*>(xs + (size_t)t * kXPitch + 16 * tid) = make_uint4(fr[t][0], fr[t][1], fr[t][2], fr[t][3]);
   } else {
     constexpr int kMaxGroups = kDecodeMaxT * kMaxH / 8 / kRowThreads;  // 8-value groups per compute thread
     const int groups = T * (H / 8);
@@ -597,7 +646,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       advance(ci, NS);
       if (tid == 32 * (j++ & (kRowWarps - 1))) issue(ci);
     }
-    if constexpr (FAST && !Q4)
+    if constexpr (FAST)
       while (cd.k + 1 < min(n_stages, P.nsd)) {
         advance(cd, P.nsd);
         if (tid == 32 * (j++ & (kRowWarps - 1))) issue_d(cd);
@@ -663,6 +712,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   float yc[MMA_C ? 16 : 1][4];  // tensor-core down projection: y of this warp's slice, D fragments
 #pragma unroll
   for (int j = 0; j < (MMA_C ? 16 : 1); ++j) yc[j][0] = yc[j][1] = yc[j][2] = yc[j][3] = 0.f;
+  float yc4[Q4MC ? 16 : 1][4];  // 4-bit tensor-core down projection: y of this warp's slice, D fragments
+#pragma unroll
+  for (int j = 0; j < (Q4MC ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
 
   if constexpr (FAST && !Q4) {
     // ---- tensor-core stage loop (bf16 weights, H = 2048, 4 rows a stage).
@@ -675,40 +727,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      16-column tile (the stage's 4 downT rows; the other 12 are other
     //      rows of the slot, times h = 0); h enters as two bf16 terms
     //      (hi + lo), so y keeps fp32 accuracy.
-    // x of this warp's slice as A fragments: row lane/4 = token (rows 8..15
-    // zero), k pairs 2(lane & 3) and +8.
-    uint32_t xa[16][2];
-    {
-      const int t = lane >> 2;
-      const float nhi = (P.block_mode && t < T) ? tb.inv[2 * t] : 0.f;
-      const float nlo = (P.block_mode && t < T) ? tb.inv[2 * t + 1] : 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 16; ++ks) {
-        const int k0 = 256 * warp + 16 * ks + 2 * (lane & 3);
-        uint32_t w0 = 0u, w1 = 0u;
-        if (t < T) {
-          if (src4) {
-            const float* xr = reinterpret_cast<const float*>(xs) + (size_t)t * H;
-            float a = xr[k0], b = xr[k0 + 1], c = xr[k0 + 8], d = xr[k0 + 9];
-            if (P.block_mode) {
-              a = norm_apply(a, nhi, nlo);
-              b = norm_apply(b, nhi, nlo);
-              c = norm_apply(c, nhi, nlo);
-              d = norm_apply(d, nhi, nlo);
-            }
-            // the values are bf16-exact: their upper halves
-            w0 = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
-            w1 = (__float_as_uint(c) >> 16) | (__float_as_uint(d) & 0xFFFF0000u);
-          } else {
-            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + (size_t)t * H * 2);
-            w0 = xr[k0 >> 1];
-            w1 = xr[(k0 + 8) >> 1];
-          }
-        }
-        xa[ks][0] = w0;
-        xa[ks][1] = w1;
-      }
-    }
+    // x: the A fragments of token lane/4 (rows 8..15 zero) from the
+    // fragment rows in shared memory, 16 bytes per 32-column block.
+    const uint8_t* xrow = xs + (size_t)(lane >> 2) * kXPitch + (size_t)(32 * warp + (lane & 3)) * 16;
+    const bool xon = (lane >> 2) < T;
     StageCursor cs;
     cursor_init(cs, NS);
     int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
@@ -728,13 +750,21 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         float dq[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.f;
+#pragma unroll 1
+        for (int kp2 = 0; kp2 < 8; kp2 += 2) {
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const int k0 = 256 * warp + 16 * ks + 2 * (lane & 3);
-          const int line = (k0 >> 6) * (2 * kRsMaxB16) + nrow;
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0));
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0 + 8));
-          mma_bf16(dq[ks & 3], xa[ks][0], 0u, xa[ks][1], 0u, b0, b1);
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int kp = kp2 + e2;
+            const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int k0 = 256 * warp + 32 * kp + 16 * h + 2 * (lane & 3);
+              const int line = (k0 >> 6) * (2 * kRsMaxB16) + nrow;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0));
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0 + 8));
+              mma_bf16(dq[2 * e2 + h], h ? xv.z : xv.x, 0u, h ? xv.w : xv.y, 0u, b0, b1);
+            }
+          }
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) d[e] = (dq[0][e] + dq[1][e]) + (dq[2][e] + dq[3][e]);
@@ -747,7 +777,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int nr = 2 * (lane & 3) + q, gu = nr >> 2, r = nr & 3;
-            pw[(2 * r + gu) * TMAX + t] = d[q];
+            pw[(gu * RSM + r) * TMAX + t] = d[q];
           }
         }
       }
@@ -762,16 +792,16 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         advance(cd, P.nsd);
         if (tid == kRowThreads - 1) issue_d(cd);
       }
-      // -- A2: value j = (row, token) on thread (j % 8) * 32 + j / 8
+      // -- A2: value j = (row, token) = r * TMAX + t on thread j
       {
-        const int j = (tid & 31) * kRowWarps + (tid >> 5);
+        const int j = tid;
         if (j < n * TMAX) {
-          const int r = j / TMAX, t = j % TMAX;
+          const int t = j % TMAX;
           float g = 0.f, u = 0.f;
 #pragma unroll
           for (int w = 0; w < kRowWarps; ++w) {
-            g += part[w * NV + (2 * r) * TMAX + t];
-            u += part[w * NV + (2 * r + 1) * TMAX + t];
+            g += part[w * NV + j];
+            u += part[w * NV + RSM * TMAX + j];
           }
           float h = 0.f;
           if (su < 0)
@@ -828,6 +858,165 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bh, 0u);
 #pragma unroll
           for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bl, 0u);
+        }
+      }
+    }
+  } else if constexpr (Q4C) {
+    // ---- tensor-core stage loop (4-bit weights, H = 2048, 8 rows a stage).
+    // A stored row is 9 chunks of 128 bytes: chunks 0..7 the nibbles, chunk
+    // 8 the 64 fp16 block scales.  Warp w owns the 256-column slice
+    // [256w, 256w + 256) of H: nibble chunk w of every row, and the 8 block
+    // scales in 16-byte unit w of chunk 8.
+    //   A: per 32-column block kp, D[token][row] = x . Q over the block
+    //      (two m16n8k16 steps; Q = code - 8 is exact in bf16), then times
+    //      the row's block scale into fp32 accumulators; the gate rows and
+    //      the up rows are two 8-row tiles.  The k order inside a block
+    //      follows the nibble order of a 32-bit word, and the x fragments
+    //      follow it.
+    //   A2: h = w silu(g) u from the 8 warps' partials.
+    //   C: per block b of the slice, y[col][token] += Q^T (h d_b), one
+    //      m16n8k8 step per 16-column tile with the stage's 8 rows as k;
+    //      h d_b enters as bf16 hi + lo, so y keeps fp32 accuracy.  Tile i
+    //      of block b holds columns 32b + 4g + 2i (rows g) and + 1 (rows
+    //      g + 8) of the slice, g = 0..7.
+    const int gq = lane >> 2, qq = lane & 3;
+    // x: the A fragments of token lane/4 (rows 8..15 zero) from the
+    // fragment rows in shared memory (nibble order), 16 bytes per block.
+    const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(32 * warp + qq) * 16;
+    const bool xon = gq < T;
+    StageCursor cs;
+    cursor_init(cs, NS);
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    uint32_t dph = 1u;
+    for (int s = 0; s < n_stages; ++s) {
+      advance(cs, NS);
+      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+      const int su = cs.u;
+      int si0, n;
+      rows_of(cs, si0, n);
+      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
+      // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
+      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [gate|up][row 2q + e], token lane/4
+      {
+        uint4 sc[2][2];  // block scales of rows 2q, 2q + 1 of the gate and up tiles
+        int lw[2];       // nibble chunk w, row lane/4 (the B column) of each tile
+#pragma unroll
+        for (int gu = 0; gu < 2; ++gu) {
+          const int l0 = (16 + gu) * kRsMaxQ4 + 2 * qq;  // scale chunk
+          sc[gu][0] = *reinterpret_cast<const uint4*>(sl + l0 * 128 + ((warp ^ (l0 & 7)) << 4));
+          sc[gu][1] = *reinterpret_cast<const uint4*>(sl + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
+          lw[gu] = (2 * warp + gu) * kRsMaxQ4 + gq;
+        }
+#pragma unroll 2
+        for (int kp = 0; kp < 8; ++kp) {
+          const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int gu = 0; gu < 2; ++gu) {
+            const uint32_t wq = *reinterpret_cast<const uint32_t*>(sl + lw[gu] * 128 + ((kp ^ (lw[gu] & 7)) << 4) + 4 * qq);
+            const uint32_t b0 = q4_pair_bf16(wq), b1 = q4_pair_bf16(wq >> 4);
+            const uint32_t b2 = q4_pair_bf16(wq >> 8), b3 = q4_pair_bf16(wq >> 12);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(d, xv.x, 0u, xv.y, 0u, b0, b1);
+            mma_bf16(d, xv.z, 0u, xv.w, 0u, b2, b3);
+            acc[gu][0] = fmaf(half_at(sc[gu][0], kp), d[0], acc[gu][0]);
+            acc[gu][1] = fmaf(half_at(sc[gu][1], kp), d[1], acc[gu][1]);
+          }
+        }
+      }
+      if (gq < TMAX) {
+        float* pw = part + (size_t)warp * NV;
+#pragma unroll
+        for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = acc[gu][e];
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // every warp is done with this stage's gate + up box and with the
+      // previous stage's downT box: both slots take their next stages
+      if (s + NS < n_stages) {
+        advance(ci, NS);
+        if (tid == kRowThreads - 1) issue(ci);
+      }
+      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+        advance(cd, P.nsd);
+        if (tid == kRowThreads - 1) issue_d(cd);
+      }
+      // -- A2: value j = (row, token) = r * TMAX + t on thread j
+      {
+        const int j = tid;
+        if (j < n * TMAX) {
+          const int t = j % TMAX;
+          float g = 0.f, u = 0.f;
+#pragma unroll
+          for (int w = 0; w < kRowWarps; ++w) {
+            g += part[w * NV + j];
+            u += part[w * NV + RSM * TMAX + j];
+          }
+          float h = 0.f;
+          if (su < 0)
+            h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
+          else
+            h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
+          hb[j] = h;
+        }
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // -- C.  Box lines: chunk * 8 + row.
+      if (++dslot == P.nsd) {
+        dslot = 0;
+        dph ^= 1u;
+      }
+      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
+      if constexpr (!Q4MC) {
+        // CUDA cores (one or two tokens): thread j owns columns 8j .. 8j+7,
+        // one 32-bit word of nibbles (chunk j/32, unit (j%32)/4) and the
+        // scale of block j/4 (scale chunk, unit j/32, value (j%32)/4)
+        const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
+#pragma unroll
+        for (int r = 0; r < kRsMaxQ4; ++r) {
+          if (r < n) {
+            const int lw = warp * kRsMaxQ4 + r, ls = 8 * kRsMaxQ4 + r;
+            const uint32_t wq =
+                *reinterpret_cast<const uint32_t*>(dbox + lw * 128 + (((lane >> 2) ^ (lw & 7)) << 4) + 4 * (lane & 3));
+            const float d = __half2float(*reinterpret_cast<const __half*>(
+                dbox + ls * 128 + ((warp ^ (ls & 7)) << 4) + 2 * (lane >> 2)));
+            float w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = nib_f32(wq, e);
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              const float hv = hb[r * TMAX + t] * d;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(hv, w[e], y[t][0][e]);
+            }
+          }
+        }
+      } else {
+        const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
+        // B: h d_b for rows 2q, 2q + 1 (k) and token lane/4 (n)
+        const float h0 = (2 * qq < n && gq < TMAX) ? hb[(2 * qq) * TMAX + gq] : 0.f;
+        const float h1 = (2 * qq + 1 < n && gq < TMAX) ? hb[(2 * qq + 1) * TMAX + gq] : 0.f;
+        const int l0 = 8 * kRsMaxQ4 + 2 * qq;
+        const uint4 s0 = *reinterpret_cast<const uint4*>(dbox + l0 * 128 + ((warp ^ (l0 & 7)) << 4));
+        const uint4 s1 = *reinterpret_cast<const uint4*>(dbox + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
+        const int lr = warp * kRsMaxQ4 + 2 * qq;  // nibble chunk w, row 2q
+        const uint8_t* r0p = dbox + lr * 128 + 2 * gq;
+        const uint8_t* r1p = dbox + (lr + 1) * 128 + 2 * gq;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const float v0 = h0 * half_at(s0, b), v1 = h1 * half_at(s1, b);
+          const uint32_t bh = pack_bf16(v0, v1);
+          const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
+          // codes of rows 2q, 2q + 1 at columns 32b + 4g .. + 3 of the slice
+          const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0p + ((b ^ (lr & 7)) << 4));
+          const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1p + ((b ^ ((lr + 1) & 7)) << 4));
+          const uint32_t X = u0 | (u1 << 16);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t a0 = q4_pair_bf16(X >> (8 * i)), a1 = q4_pair_bf16(X >> (8 * i + 4));
+            mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
+            mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
+          }
         }
       }
     }
@@ -1094,6 +1283,18 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         P.partial[((size_t)cta * T + t0 + 1) * H + c] = yc[j][1];
         P.partial[((size_t)cta * T + t0 + 1) * H + c + 8] = yc[j][3];
       }
+    }
+  } else if constexpr (Q4MC) {
+    // tile 2b + i: columns 256w + 32b + 4g + 2i (and + 1), tokens 2q (and + 1)
+    const int g = lane >> 2, t0 = 2 * (lane & 3);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = 256 * warp + 32 * (j >> 1) + 4 * g + 2 * (j & 1);
+      if (t0 < T)
+        *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0) * H + c) = make_float2(yc4[j][0], yc4[j][2]);
+      if (t0 + 1 < T)
+        *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0 + 1) * H + c) =
+            make_float2(yc4[j][1], yc4[j][3]);
     }
   } else {
 #pragma unroll
