@@ -283,7 +283,9 @@ MOE_DEV int swz_off(int line, int k) { return line * 128 + ((((k >> 3) & 7) ^ (l
 
 // Two floats -> bf16 pair (round to nearest even), low element first.
 MOE_DEV uint32_t pack_bf16(float lo, float hi) {
-  return (uint32_t)float_to_bf16_rne(lo) | ((uint32_t)float_to_bf16_rne(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 MOE_DEV float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
@@ -750,7 +752,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         float dq[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.f;
-#pragma unroll 1
+#pragma unroll
         for (int kp2 = 0; kp2 < 8; kp2 += 2) {
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
@@ -907,19 +909,32 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           sc[gu][1] = *reinterpret_cast<const uint4*>(sl + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
           lw[gu] = (2 * warp + gu) * kRsMaxQ4 + gq;
         }
-#pragma unroll 2
-        for (int kp = 0; kp < 8; ++kp) {
-          const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
+        // blocks in two halves of four (the scale words of a half picked once)
+#pragma unroll(Q4MC ? 1 : 2)
+        for (int kh = 0; kh < 2; ++kh) {
+          uint4 sh[2];  // (row 2q, row 2q + 1) scale words of blocks 4kh .. 4kh+3, per tile
 #pragma unroll
-          for (int gu = 0; gu < 2; ++gu) {
-            const uint32_t wq = *reinterpret_cast<const uint32_t*>(sl + lw[gu] * 128 + ((kp ^ (lw[gu] & 7)) << 4) + 4 * qq);
-            const uint32_t b0 = q4_pair_bf16(wq), b1 = q4_pair_bf16(wq >> 4);
-            const uint32_t b2 = q4_pair_bf16(wq >> 8), b3 = q4_pair_bf16(wq >> 12);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_bf16(d, xv.x, 0u, xv.y, 0u, b0, b1);
-            mma_bf16(d, xv.z, 0u, xv.w, 0u, b2, b3);
-            acc[gu][0] = fmaf(half_at(sc[gu][0], kp), d[0], acc[gu][0]);
-            acc[gu][1] = fmaf(half_at(sc[gu][1], kp), d[1], acc[gu][1]);
+          for (int gu = 0; gu < 2; ++gu)
+            sh[gu] = kh ? make_uint4(sc[gu][0].z, sc[gu][0].w, sc[gu][1].z, sc[gu][1].w)
+                        : make_uint4(sc[gu][0].x, sc[gu][0].y, sc[gu][1].x, sc[gu][1].y);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const int kp = 4 * kh + e4;
+            const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int gu = 0; gu < 2; ++gu) {
+              const uint32_t wq = *reinterpret_cast<const uint32_t*>(sl + lw[gu] * 128 + ((kp ^ (lw[gu] & 7)) << 4) + 4 * qq);
+              const uint32_t b0 = q4_pair_bf16(wq), b1 = q4_pair_bf16(wq >> 4);
+              const uint32_t b2 = q4_pair_bf16(wq >> 8), b3 = q4_pair_bf16(wq >> 12);
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16(d, xv.x, 0u, xv.y, 0u, b0, b1);
+              mma_bf16(d, xv.z, 0u, xv.w, 0u, b2, b3);
+              const uint32_t w0 = (e4 >> 1) ? sh[gu].y : sh[gu].x, w1 = (e4 >> 1) ? sh[gu].w : sh[gu].z;
+              const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (w0 >> 16) : (w0 & 0xFFFFu))));
+              const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (w1 >> 16) : (w1 & 0xFFFFu))));
+              acc[gu][0] = fmaf(s0, d[0], acc[gu][0]);
+              acc[gu][1] = fmaf(s1, d[1], acc[gu][1]);
+            }
           }
         }
       }
