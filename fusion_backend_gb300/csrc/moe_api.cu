@@ -23,6 +23,8 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct WsLayout {
   size_t ctrl, logits, partial, counts, offsets, perm, active, nactive, total;
+  // batched path
+  size_t ids, p, bitmap, slot_of, slot_w, x_perm, h_ws, y_ws;
 };
 
 }  // namespace
@@ -31,7 +33,7 @@ struct moe_ffn_plan {
   uint32_t magic;
   moe_ffn_shapes s;
   int act, wfmt;
-  int path;  // 0 decode
+  int path;  // 0 decode (row kernel), 1 batched (grouped GEMMs)
   WsLayout ws;
 };
 
@@ -122,6 +124,51 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   int rc = device_info(&dev);
   if (rc != MOE_FFN_OK) return rc;
 
+  if (plan->path == 1) {
+    const moe_ffn_shapes& s = plan->s;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const WsLayout& L = plan->ws;
+    BatchParams B;
+    memset(&B, 0, sizeof(B));
+    B.T = s.T;
+    B.H = s.H;
+    B.E = s.E;
+    B.K = s.top_k;
+    B.I = s.I;
+    B.Is = s.Is;
+    B.G = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
+    B.x = static_cast<const uint16_t*>(x);
+    B.router_w = static_cast<const uint16_t*>(router_w);
+    B.gate_w = static_cast<const uint16_t*>(shexp_gate_w);
+    B.expert_w = static_cast<const uint8_t*>(expert_w);
+    B.shexp_w = static_cast<const uint8_t*>(shexp_w);
+    B.out = out;
+    B.topk_ids = topk_ids;
+    B.topk_w = topk_w;
+    B.ctrl = reinterpret_cast<uint32_t*>(w + L.ctrl);
+    B.logits = reinterpret_cast<float*>(w + L.logits);
+    B.ls = (s.E + 1 + 3) / 4 * 4;
+    B.ids = reinterpret_cast<int32_t*>(w + L.ids);
+    B.p = reinterpret_cast<float*>(w + L.p);
+    B.bitmap = reinterpret_cast<uint32_t*>(w + L.bitmap);
+    B.tw = (s.T + 31) / 32;
+    B.slot_of = reinterpret_cast<int32_t*>(w + L.slot_of);
+    B.slot_w = reinterpret_cast<float*>(w + L.slot_w);
+    B.x_perm = reinterpret_cast<uint16_t*>(w + L.x_perm);
+    B.h_ws = reinterpret_cast<uint16_t*>(w + L.h_ws);
+    B.hw = s.I > s.Is ? s.I : s.Is;
+    B.y_ws = reinterpret_cast<float*>(w + L.y_ws);
+    B.r_counts = reinterpret_cast<int32_t*>(w + L.counts);
+    B.r_offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+    B.r_perm = reinterpret_cast<int32_t*>(w + L.perm);
+    B.r_active = reinterpret_cast<int32_t*>(w + L.active);
+    B.r_nactive = reinterpret_cast<int32_t*>(w + L.nactive);
+    if (kGemmSmem > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
+    cudaError_t err = batch_tensor_maps(B);
+    if (err != cudaSuccess) return cuda_status(err);
+    return cuda_status(launch_batch(B, reinterpret_cast<cudaStream_t>(stream)));
+  }
+
   LayerParams P;
   fill_params(plan, P, workspace);
   P.x = x;
@@ -153,14 +200,23 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   const moe_ffn_shapes s = *shapes;
   if (dtype.act != MOE_FFN_ACT_F32 && dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_INVALID_ARG;
   if (dtype.wfmt != MOE_FFN_W_BF16 && dtype.wfmt != MOE_FFN_W_Q4B32) return MOE_FFN_ERR_INVALID_ARG;
-  if (s.T < 1 || s.T > 256 || s.E < 1 || s.E > kMaxExperts || s.top_k < 1 || s.top_k > s.E ||
+  if (s.T < 1 || s.T > kBatchMaxT || s.E < 1 || s.E > kMaxExperts || s.top_k < 1 || s.top_k > s.E ||
       s.top_k > kMaxTopK || s.H < 1 || s.I < 1 || s.Is < 1)
     return MOE_FFN_ERR_UNSUPPORTED;
-  // Decode path: T <= 8; stored rows of H elements (bf16: H a multiple of 8,
-  // 4-bit: of 256, so that rows are 16-byte multiples); H <= 4096.
-  if (s.T > kDecodeMaxT || s.H > kMaxH) return MOE_FFN_ERR_UNSUPPORTED;
-  if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256)) return MOE_FFN_ERR_UNSUPPORTED;
   if (s.I > (1 << 20) || s.Is > (1 << 20)) return MOE_FFN_ERR_UNSUPPORTED;
+  const int path = s.T > kDecodeMaxT ? 1 : 0;
+  if (path == 0) {
+    // Decode path: T <= 8; stored rows of H elements (bf16: H a multiple of
+    // 8, 4-bit: of 256, so that rows are 16-byte multiples); H <= 4096.
+    if (s.H > kMaxH) return MOE_FFN_ERR_UNSUPPORTED;
+    if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256)) return MOE_FFN_ERR_UNSUPPORTED;
+  } else {
+    // Batched path (grouped GEMMs): bf16 weights and activation, E <= 256,
+    // tiles of 256 columns of H and 128 rows of I and Is.
+    if (dtype.wfmt != MOE_FFN_W_BF16 || dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_UNSUPPORTED;
+    if (s.E > kBatchMaxE || s.H % 256 || s.I % 128 || s.Is % 128) return MOE_FFN_ERR_UNSUPPORTED;
+    if ((long long)s.E * 3 * s.I >= (1LL << 31) || 3LL * s.Is >= (1LL << 31)) return MOE_FFN_ERR_UNSUPPORTED;
+  }
 
   moe_ffn_plan* p = new (std::nothrow) moe_ffn_plan();
   if (!p) return MOE_FFN_ERR_INVALID_ARG;
@@ -168,7 +224,7 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   p->s = s;
   p->act = dtype.act;
   p->wfmt = dtype.wfmt;
-  p->path = 0;
+  p->path = path;
   size_t off = 0;
   WsLayout& L = p->ws;
   const size_t T = s.T, E = s.E, K = s.top_k;
@@ -177,7 +233,26 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   L.logits = off;
   off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
   L.partial = off;
-  off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * 4);
+  if (path == 0) off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * 4);
+  if (path == 1) {
+    const size_t TK = T * K, H = s.H, hw = s.I > s.Is ? s.I : s.Is;
+    L.ids = off;
+    off = align256(off + TK * 4);
+    L.p = off;
+    off = align256(off + TK * 4);
+    L.bitmap = off;
+    off = align256(off + E * ((T + 31) / 32) * 4);
+    L.slot_of = off;
+    off = align256(off + TK * 4);
+    L.slot_w = off;
+    off = align256(off + (TK + T) * 4);
+    L.x_perm = off;
+    off = align256(off + TK * H * 2);
+    L.h_ws = off;
+    off = align256(off + (TK + T) * hw * 2);
+    L.y_ws = off;
+    off = align256(off + (TK + T) * H * 4);
+  }
   L.counts = off;
   off = align256(off + E * 4);
   L.offsets = off;
@@ -254,7 +329,7 @@ int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value) {
       *value = plan->path;
       return MOE_FFN_OK;
     case MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE:
-      *value = kLaunchesPerExecute;
+      *value = plan->path == 1 ? kBatchLaunches : kLaunchesPerExecute;
       return MOE_FFN_OK;
     default:
       return MOE_FFN_ERR_INVALID_ARG;

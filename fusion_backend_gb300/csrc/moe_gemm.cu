@@ -1,0 +1,423 @@
+// Grouped GEMMs of the batched MoE FFN layer on the 5th-generation tensor
+// cores (tcgen05), sm_103a.
+//
+// A group is one active expert (its slots offsets[e] .. + counts[e], x rows
+// gathered in x_perm) or the shared expert (slot T K + t for every token t,
+// x itself).  Groups are cut into units of at most kGemmNC slots (the MMA N)
+// and a 256-row (gate / up) or 256-column (down) tile of the weights; the
+// persistent blocks take units round robin.
+//
+//   gate / up (PHASE 0):  G = W_g X^T, U = W_u X^T over K = H, 128 rows of I
+//     per unit for each of the two matrices; h = silu(G) * U * w(slot),
+//     stored as bf16 rows h_ws[slot][I].
+//   down (PHASE 1):  Y^T = downT^T H^T over K = I (Is for the shared expert),
+//     256 output columns per unit (two 128-column accumulators); the downT
+//     tile is the MN-major A operand, straight from its [I][H] rows;
+//     y_ws[slot][H] in fp32.
+//
+// Block roles: warp 0 lane 0 moves tiles with TMA into a ring of
+// kGemmStages slots (two 128 x 64 A tiles + an NC x 64 B tile, 128-byte
+// swizzled); warp 1 owns the tensor memory (256 columns: two fp32
+// accumulators of up to 128 columns) and lane 0 issues the MMAs (M = 128,
+// N = slots rounded up to 16, K = 16), committing each ring slot back to the
+// producer and each finished unit to the epilogue; warps 2..5 read the
+// accumulators (warp w reads lanes 32 (w % 4) ..) and write the unit's rows.
+// Every wait is bounded; a wait that gives up sets the status word and the
+// block winds down without leaving copies or tensor-core work in flight.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kS = kGemmStages;
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets, descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A
+// MN-major if a_mn, B K-major, N and M.
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, int a_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+// 32 lanes x 16 columns of 32 bits (this warp's lane quarter)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ bool aborted(const int* f) { return *reinterpret_cast<const volatile int*>(f) != 0; }
+__device__ __forceinline__ void set_abort(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
+
+// One unit of work.
+struct Unit {
+  int shared;  // the shared expert
+  int e;       // expert (routed)
+  int slot0;   // first slot (row of h_ws / y_ws; of x_perm for routed gate / up)
+  int brow0;   // first row of the B operand
+  int n;       // slots (1 .. kGemmNC)
+  int tile;    // row tile (gate / up: 128 rows of I) or column tile (down: 256 columns of H)
+};
+
+}  // namespace
+
+template <int PHASE>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant__ BatchParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = sm;  // kS x kGemmStageBytes, 1024-byte aligned slots
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kS * kGemmStageBytes);
+  uint64_t* empty = full + kS;
+  uint64_t* acc_full = empty + kS;
+  uint64_t* acc_empty = acc_full + 1;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_cum[kBatchMaxE + 2];  // units before group g
+  __shared__ int s_grp[kBatchMaxE + 1][3];  // group g: expert (-1 shared), first slot, slots
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = P.T, K = P.K;
+  // row / column tiles per slot chunk
+  const int MT = PHASE == 0 ? P.I / 128 : P.H / 256;
+  const int MT_s = PHASE == 0 ? P.Is / 128 : P.H / 256;
+
+  // ---- groups and their unit counts (warp 0), barriers (thread 64), tensor memory (warp 1)
+  if (warp == 0) {
+    const int U = *P.r_nactive;
+    // lane l sums groups [9l, 9l + 9) (U + 1 <= 257 groups)
+    int sum = 0;
+    int cnt[9];
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+      const int g = 9 * lane + q;
+      cnt[q] = 0;
+      if (g < U) {
+        const int e = P.r_active[g];
+        const int c = P.r_counts[e];
+        s_grp[g][0] = e;
+        s_grp[g][1] = P.r_offsets[e];
+        s_grp[g][2] = c;
+        cnt[q] = (c + kGemmNC - 1) / kGemmNC * MT;
+      } else if (g == U) {
+        s_grp[g][0] = -1;
+        s_grp[g][1] = T * K;
+        s_grp[g][2] = T;
+        cnt[q] = (T + kGemmNC - 1) / kGemmNC * MT_s;
+      }
+      sum += cnt[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+      const int g = 9 * lane + q;
+      if (g <= U + 1 && g < kBatchMaxE + 2) s_cum[g] = run;
+      run += cnt[q];
+    }
+  }
+  if (tid == 64) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)), "r"(256)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int U = *P.r_nactive;
+  const int n_units = s_cum[U + 1];
+
+  // unit u -> its group and tile, scanning forward from the last group
+  int gscan = 0;
+  auto unit_of = [&](int u, Unit& w) {
+    while (gscan < U && s_cum[gscan + 1] <= u) ++gscan;
+    const int local = u - s_cum[gscan];
+    const int mt = s_grp[gscan][0] < 0 ? MT_s : MT;
+    const int chunk = local / mt;
+    w.tile = local - chunk * mt;
+    w.shared = s_grp[gscan][0] < 0;
+    w.e = w.shared ? 0 : s_grp[gscan][0];
+    w.slot0 = s_grp[gscan][1] + chunk * kGemmNC;
+    w.n = min(kGemmNC, s_grp[gscan][2] - chunk * kGemmNC);
+    // B rows: gate / up read x_perm (routed) or x (shared, row = token);
+    // down reads h_ws at the slot rows
+    w.brow0 = (PHASE == 0 && w.shared) ? chunk * kGemmNC : w.slot0;
+  };
+  const int nk_r = PHASE == 0 ? P.H / 64 : P.I / 64;
+  const int nk_s = PHASE == 0 ? P.H / 64 : P.Is / 64;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+        Unit w;
+        unit_of(u, w);
+        const int nk = w.shared ? nk_s : nk_r;
+        const int npad = (w.n + 15) & ~15;
+        const uint32_t bytes = 2 * 128 * 128 + (uint32_t)npad * 128;
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u)) {
+            set_abort(&s_abort);
+            break;
+          }
+          uint8_t* slot = ring + (size_t)stage * kGemmStageBytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          if (PHASE == 0) {
+            // gate and up tiles: rows tile*128 .. of matrices 0 and 1, k columns kc*64 ..
+            const CUtensorMap* m = w.shared ? &P.tm_w128_s : &P.tm_w128_e;
+            const int I = w.shared ? P.Is : P.I;
+            const int rb = w.e * 3 * I + w.tile * 128;
+            tma_load_2d(slot, m, kc * 64, rb, &full[stage], pol_w);
+            tma_load_2d(slot + 16384, m, kc * 64, rb + I, &full[stage], pol_w);
+            const CUtensorMap* bm = w.shared ? &P.tm_x : &P.tm_xp;
+            for (int j = 0; j < npad; j += 16)
+              tma_load_2d(slot + 32768 + j * 128, bm, kc * 64, w.brow0 + j, &full[stage], pol_x);
+          } else {
+            // downT rows kc*64 .. (k) x columns tile*256 .. (m), four 64-column boxes
+            const CUtensorMap* m = w.shared ? &P.tm_w64_s : &P.tm_w64_e;
+            const int I = w.shared ? P.Is : P.I;
+            const int r = (w.e * 3 + 2) * I + kc * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tma_load_2d(slot + q * 8192, m, w.tile * 256 + 64 * q, r, &full[stage], pol_w);
+            for (int j = 0; j < npad; j += 16)
+              tma_load_2d(slot + 32768 + j * 128, &P.tm_h, kc * 64, w.brow0 + j, &full[stage], pol_x);
+          }
+          if (++stage == kS) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // wind down: every issued copy has landed before the block exits
+      for (int i = 0; i < kS; ++i) {
+        // slot i was last filled in phase ph' where (stage, ph) is the next fill
+        const uint32_t last = i < stage ? ph : ph ^ 1u;
+        mbar_wait(&full[i], last);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      bool pending = false;  // MMAs issued for a unit whose accumulator is not committed
+      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+        Unit w;
+        unit_of(u, w);
+        const int nk = w.shared ? nk_s : nk_r;
+        const int npad = (w.n + 15) & ~15;
+        const uint32_t idesc = instr_desc(128, npad, PHASE);
+        if (!mbar_wait(acc_empty, acc_ph ^ 1u)) {
+          set_abort(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(&full[stage], ph)) {
+            set_abort(&s_abort);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + (size_t)stage * kGemmStageBytes);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = smem_desc(sa + 32768 + ks * 32, 16, 1024);
+            uint64_t a0, a1;
+            if (PHASE == 0) {
+              a0 = smem_desc(sa + ks * 32, 16, 1024);
+              a1 = smem_desc(sa + 16384 + ks * 32, 16, 1024);
+            } else {
+              a0 = smem_desc(sa + ks * 2048, 8192, 1024);
+              a1 = smem_desc(sa + 16384 + ks * 2048, 8192, 1024);
+            }
+            const uint32_t acc = (kc > 0 || ks > 0) ? 1u : 0u;
+            umma(tmem, a0, bd, idesc, acc);
+            umma(tmem + 128, a1, bd, idesc, acc);
+          }
+          umma_commit(&empty[stage]);
+          pending = true;
+          if (++stage == kS) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (aborted(&s_abort)) break;
+        umma_commit(acc_full);
+        pending = false;
+        acc_ph ^= 1u;
+      }
+      // after a wait that gave up: the tensor cores finish the MMAs in
+      // flight before the tensor memory is released
+      if (pending) {
+        umma_commit(acc_full);
+        mbar_wait(acc_full, acc_ph);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int m = 32 * (warp & 3) + lane;  // accumulator row (TMEM lane) of this thread
+    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+    uint32_t acc_ph = 0;
+    for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+      Unit w;
+      unit_of(u, w);
+      if (!mbar_wait(acc_full, acc_ph)) {
+        set_abort(&s_abort);
+        break;
+      }
+      tc_fence_after();
+      for (int j0 = 0; j0 < w.n; j0 += 16) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tmem + lane_addr + (uint32_t)j0, r0);
+        tmem_ld16(tmem + lane_addr + 128u + (uint32_t)j0, r1);
+        if (PHASE == 0) {
+          const int i = w.tile * 128 + m;
+          // h rows of the shared slots start at T K
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = j0 + jj;
+            if (j < w.n) {
+              const int slot = w.slot0 + j;
+              const float g = __uint_as_float(r0[jj]), up = __uint_as_float(r1[jj]);
+              const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
+              P.h_ws[(size_t)slot * (size_t)P.hw + i] = float_to_bf16_rne(h);
+            }
+          }
+        } else {
+          const int c = w.tile * 256 + m;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = j0 + jj;
+            if (j < w.n) {
+              float* dst = P.y_ws + (size_t)(w.slot0 + j) * P.H + c;
+              dst[0] = __uint_as_float(r0[jj]);
+              dst[128] = __uint_as_float(r1[jj]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_ph ^= 1u;
+    }
+  }
+  __syncthreads();
+  if (aborted(&s_abort) && tid == 0) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+// 2-D bf16 view [rows][cols] (row pitch cols * 2 bytes) with a box of
+// bcols x brows, 128-byte swizzled in shared memory.
+bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, long long rows, int cols,
+               int bcols, int brows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)bcols, (cuuint32_t)brows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t batch_tensor_maps(BatchParams& p) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = gemm_encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const long long er = (long long)p.E * 3 * p.I, sr = 3LL * p.Is, TK = (long long)p.T * p.K;
+  if (!encode_2d(fn, &p.tm_w128_e, p.expert_w, er, p.H, 64, 128) ||
+      !encode_2d(fn, &p.tm_w128_s, p.shexp_w, sr, p.H, 64, 128) ||
+      !encode_2d(fn, &p.tm_w64_e, p.expert_w, er, p.H, 64, 64) ||
+      !encode_2d(fn, &p.tm_w64_s, p.shexp_w, sr, p.H, 64, 64) ||
+      !encode_2d(fn, &p.tm_xp, p.x_perm, TK, p.H, 64, 16) || !encode_2d(fn, &p.tm_x, p.x, p.T, p.H, 64, 16) ||
+      !encode_2d(fn, &p.tm_h, p.h_ws, TK + p.T, p.hw, 64, 16))
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+template <int PHASE>
+static cudaError_t launch_gemm(const BatchParams& p, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(k_gemm<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (err != cudaSuccess) return err;
+  k_gemm<PHASE><<<p.G, kGemmThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gate_up(const BatchParams& p, cudaStream_t stream) { return launch_gemm<0>(p, stream); }
+cudaError_t launch_gemm_down(const BatchParams& p, cudaStream_t stream) { return launch_gemm<1>(p, stream); }
+
+}  // namespace moe

@@ -71,11 +71,69 @@ struct LayerParams {
   // Tensor maps of the tensor-core path (bf16 weights, H = 2048): boxes of
   // one stage's gate + up rows (gu) and downT rows (d) of the routed experts
   // (e) and of the shared expert (s), 128-byte swizzled in shared memory.
-  alignas(64) CUtensorMap tm_gu_e;
-  alignas(64) CUtensorMap tm_d_e;
-  alignas(64) CUtensorMap tm_gu_s;
-  alignas(64) CUtensorMap tm_d_s;
+  CUtensorMap tm_gu_e;
+  CUtensorMap tm_d_e;
+  CUtensorMap tm_gu_s;
+  CUtensorMap tm_d_s;
 };
+
+// ---- batched path (T > kDecodeMaxT): routing, a gather of x by expert, two
+// grouped GEMMs on the tcgen05 tensor cores and a fixed-order combine.
+constexpr int kBatchMaxT = 1024;
+constexpr int kBatchMaxE = 256;
+constexpr int kGemmNC = 128;      // slots (tokens) per GEMM unit: the MMA N, at most
+constexpr int kGemmStages = 4;    // shared-memory ring depth of the GEMM kernels
+constexpr int kGemmThreads = 192; // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+
+struct BatchParams {
+  int T, H, E, K, I, Is, G;
+  const uint16_t* x;         // [T][H] bf16
+  const uint16_t* router_w;  // [E][H]
+  const uint16_t* gate_w;    // [H] shared-expert gate vector
+  const uint8_t* expert_w;   // E x (gate[I][H] | up[I][H] | downT[I][H]) bf16
+  const uint8_t* shexp_w;    // gate[Is][H] | up[Is][H] | downT[Is][H] bf16
+  float* out;                // [T][H]
+  int32_t* topk_ids;         // optional [T][K]
+  float* topk_w;             // optional [T][K]
+  // workspace
+  uint32_t* ctrl;
+  float* logits;  // [T][ls]
+  int ls;
+  int32_t* ids;       // [T][K] chosen experts, rank order
+  float* p;           // [T][K] their weights
+  uint32_t* bitmap;   // [E][tw] tokens of each expert
+  int tw;             // bitmap words per expert: ceil(T / 32)
+  int32_t* slot_of;   // [T][K] slot (row of the expert-sorted order) of each choice
+  float* slot_w;      // [T K + T] weight of each slot (routed p, then the shared gate per token)
+  uint16_t* x_perm;   // [T K][H] bf16, x of each routed slot
+  uint16_t* h_ws;     // [T K + T][hw] bf16, h of each slot (weight applied)
+  int hw;             // h_ws row length: max(I, Is)
+  float* y_ws;        // [T K + T][H] fp32, expert output of each slot
+  int32_t* r_counts;  // [E]
+  int32_t* r_offsets; // [E + 1]
+  int32_t* r_perm;    // [T K] token-major choice index of each slot
+  int32_t* r_active;  // [E] active experts ascending
+  int32_t* r_nactive; // [1]
+  // Tensor maps (bf16, 128-byte swizzle): weight rows of the expert blocks
+  // and of the shared block with boxes of 64 x 128 (gate / up tiles) and
+  // 64 x 64 (downT tiles, MN-major), and the B operands: x_perm, x, h_ws
+  // rows with boxes of 64 x 16.
+  CUtensorMap tm_w128_e;
+  CUtensorMap tm_w128_s;
+  CUtensorMap tm_w64_e;
+  CUtensorMap tm_w64_s;
+  CUtensorMap tm_xp;
+  CUtensorMap tm_x;
+  CUtensorMap tm_h;
+};
+// Encodes the tensor maps; cudaSuccess or an error.
+cudaError_t batch_tensor_maps(BatchParams& p);
+// Enqueues the whole batched layer (kBatchLaunches kernels).
+cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream);
+constexpr int kBatchLaunches = 6;
+// Shared-memory bytes of the GEMM kernels.
+constexpr int kGemmStageBytes = 2 * 128 * 128 + kGemmNC * 128;  // two 128 x 64 A tiles + an NC x 64 B tile
+constexpr int kGemmSmem = kGemmStages * kGemmStageBytes + 1024 + 256;
 
 // Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
 // Launched behind the previous kernel of the stream with programmatic

@@ -1,0 +1,95 @@
+"""GPU parity of the batched path (T > 8 tokens: routing, expert-sorted gather,
+two grouped GEMMs on the tcgen05 tensor cores, fixed-order combine) against
+the oracle.
+
+Bar as for the decode path: top-k ids bit-exact, output max|d| <= 1e-2
+rms(oracle) + 1e-5, bucketing equal to the oracle's stable counting sort,
+repeated runs bitwise identical.  At the full layer size the oracle runs on a
+sample of tokens (tokens are independent: each is routed on its own), the
+ids of every token are checked against the oracle's router and top-k, and the
+bucketing against the oracle's bucketing of those ids.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from datagen import ACT_BF16, WFMT_BF16, Shapes
+from tests.cases import DECODE, draw_tokens, with_T, x_as_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _layer(seed, shapes):
+    return datagen.make_layer(seed, Shapes(1, shapes.H, shapes.E, shapes.top_k, shapes.I, shapes.Is), WFMT_BF16)
+
+
+@pytest.mark.parametrize(
+    "shapes",
+    [
+        Shapes(T=9, H=256, E=8, top_k=2, I=128, Is=128),      # the smallest batch
+        Shapes(T=40, H=512, E=16, top_k=4, I=256, Is=128),    # several row / column tiles, ragged groups
+        Shapes(T=300, H=256, E=4, top_k=2, I=128, Is=256),    # groups and the shared expert past 128 slots
+        Shapes(T=64, H=768, E=32, top_k=8, I=384, Is=256),    # three column-tile pairs, three row tiles
+        Shapes(T=33, H=256, E=64, top_k=1, I=128, Is=128),    # top-1, most experts idle
+    ],
+)
+def test_batched_small(shapes):
+    from tests.test_gpu_parity import check_case
+
+    layer = _layer(4001, shapes)
+    x, _ = draw_tokens(4001, layer, shapes.T, ACT_BF16)
+    check_case(layer, x, ACT_BF16, str(shapes))
+
+
+def test_batched_repeat_bitwise():
+    from tests.devlayer import DevLayer
+
+    shapes = Shapes(T=40, H=512, E=16, top_k=4, I=256, Is=128)
+    layer = _layer(4002, shapes)
+    x, _ = draw_tokens(4002, layer, shapes.T, ACT_BF16)
+    dl = DevLayer(layer)
+    a = dl.run(x, ACT_BF16)
+    b = dl.run(x, ACT_BF16, ws_fill=0x5A)
+    assert a["status"] == 0 and b["status"] == 0
+    assert a["out"].tobytes() == b["out"].tobytes()
+    assert a["ids"].tobytes() == b["ids"].tobytes()
+
+
+@pytest.fixture(scope="module")
+def full_layer():
+    return datagen.make_layer(2024, DECODE, WFMT_BF16)
+
+
+@pytest.mark.parametrize("T", [64, 256])
+def test_batched_full_size_sampled(full_layer, T):
+    from tests.devlayer import DevLayer, tolerance_ok
+
+    s = with_T(DECODE, T)
+    x, _ = draw_tokens(2024, full_layer, T, ACT_BF16, first_token=1000 + T)
+    got = DevLayer(full_layer).run(x, ACT_BF16)
+    assert got["status"] == 0
+    # ids and weights of every token against the oracle's router and top-k
+    for t in range(T):
+        lg = oracle.router_logits(full_layer.router_w, s.E, s.H, x_as_f64(x[t], ACT_BF16))
+        ids, p = oracle.topk(lg, s.top_k)
+        np.testing.assert_array_equal(got["ids"][t], ids, err_msg=f"token {t}")
+        np.testing.assert_allclose(got["p"][t], p, rtol=1e-5, atol=1e-7)
+    counts, offsets, perm, active = oracle.bucketing(got["ids"], s.E)
+    g_counts, g_offsets, g_perm, g_active = got["routing"]
+    np.testing.assert_array_equal(g_counts, counts)
+    np.testing.assert_array_equal(g_offsets, offsets)
+    np.testing.assert_array_equal(g_perm, perm)
+    np.testing.assert_array_equal(g_active, active)
+    # outputs of a sample of tokens
+    idx = np.array(sorted({0, 1, T // 3, T // 2, T - 2, T - 1}))
+    ref = oracle.moe_ffn(with_T(DECODE, idx.size), ACT_BF16, WFMT_BF16, x[idx], full_layer.router_w,
+                         full_layer.expert_w, full_layer.shexp_w, full_layer.shexp_gate_w)
+    np.testing.assert_array_equal(got["ids"][idx], ref["ids"])
+    ok, err, rms = tolerance_ok(got["out"][idx], ref["out"])
+    assert ok, f"T={T}: max|d| = {err:.3e} > 1e-2 * rms({rms:.3e}) + 1e-5"
