@@ -10,7 +10,11 @@ CUDA graph and replayed; CUDA events on the launching stream time them.
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (the reference arm).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4] [--T T]
+With ``--config batched_bf16 --T 64`` (or 256) the same layer runs on the
+batched path (routing, expert-sorted gather, grouped GEMMs on the tensor
+cores, combine).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4|batched_bf16] [--T T]
 """
 
 from __future__ import annotations
@@ -41,7 +45,7 @@ SEED = 20261202
 # dram__bytes_read.sum + dram__bytes_write.sum of one k_rows launch from the
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
-NCU_TRAFFIC_BYTES = {"decode_bf16": None, "decode_q4": None}
+NCU_TRAFFIC_BYTES = {"decode_bf16": None, "decode_q4": None, "batched_bf16": None}
 
 
 def peaks():
@@ -55,11 +59,12 @@ def peaks():
 
 
 def workload(cfg: str, T: int):
-    wfmt = datagen.WFMT_BF16 if cfg == "decode_bf16" else datagen.WFMT_Q4B32
+    wfmt = datagen.WFMT_Q4B32 if cfg == "decode_q4" else datagen.WFMT_BF16
     shapes = datagen.Shapes(T=T, H=H, E=E, top_k=K_TOP, I=I, Is=IS)
     name = {
         "decode_bf16": f"decode bf16 MoE FFN layer: T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "decode_q4": f"decode 4-bit MoE FFN layer (blocks of 32, fp16 scale): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
+        "batched_bf16": f"batched bf16 MoE FFN layer (grouped GEMMs): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
     }[cfg]
     return shapes, wfmt, name
 
@@ -184,7 +189,7 @@ def main():
     ap.add_argument("--steps", type=int, default=64000)
     ap.add_argument("--warmup", type=int, default=1600)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4"])
+    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4", "batched_bf16"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_LAYER_COPIES, help="layer copies rotated (profiling: fewer)")
@@ -344,7 +349,8 @@ def main():
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "traffic": NCU_TRAFFIC_BYTES.get(args.config),
                          "algorithmic_bytes_per_step": bytes_per_step,
-                         "kernel": "k_rows (+ k_route, programmatic dependent launch); duration = step time"},
+                         "kernel": ("k_gemm<0>, k_gemm<1> (+ routing, gather, combine); duration = step time"
+                                    if T > 8 else "k_rows (+ k_route, programmatic dependent launch); duration = step time")},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4,
                     "steps": e2e_steps, "how": "eager public-API calls: pinned H2D of x, execute, D2H of out"},
