@@ -163,7 +163,7 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
     B.r_perm = reinterpret_cast<int32_t*>(w + L.perm);
     B.r_active = reinterpret_cast<int32_t*>(w + L.active);
     B.r_nactive = reinterpret_cast<int32_t*>(w + L.nactive);
-    if (kGemmSmem > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
+    if (kGemmSmem0 + 8192 > dev->smem_optin || kGemmSmem1 + 8192 > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
     cudaError_t err = batch_tensor_maps(B);
     if (err != cudaSuccess) return cuda_status(err);
     return cuda_status(launch_batch(B, reinterpret_cast<cudaStream_t>(stream)));

@@ -22,12 +22,13 @@ cudaError_t launch_gemm_down(const BatchParams& p, cudaStream_t stream);
 namespace {
 
 constexpr int kRouteTokens = 8;   // tokens per router block
-constexpr int kRouteRows = 16;    // router rows per block (2 per warp)
+constexpr int kRouteRows = 8;     // router rows per block (1 per warp)
+constexpr int kGatherSplit = 4;   // blocks per expert in the bucketing kernel
 
 // Router logits, error-free accumulated as in the decode router: the
 // products of bf16 weights and bf16 activations are exact in fp32, their
 // sum is kept as a (sum, compensation) pair and rounded once.  Block
-// (token group, row group): 8 warps x 2 rows x 8 tokens.  The first block
+// (token group, row group): 8 warps x 1 row x 8 tokens.  The first block
 // also clears the control words and every block a share of the bitmap.
 __global__ void __launch_bounds__(256) k_route_b(const __grid_constant__ BatchParams P) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -35,22 +36,23 @@ __global__ void __launch_bounds__(256) k_route_b(const __grid_constant__ BatchPa
   for (int i = bid * 256 + tid; i < P.E * P.tw; i += nblk * 256) P.bitmap[i] = 0u;
   if (bid == 0 && tid < kCtrlWords) P.ctrl[tid] = 0u;
   const int t0 = blockIdx.x * kRouteTokens;
-  const int r0 = blockIdx.y * kRouteRows + 2 * warp;
-  const uint16_t* w[2];
+  constexpr int RPW = kRouteRows / 8;  // rows per warp
+  const int r0 = blockIdx.y * kRouteRows + RPW * warp;
+  const uint16_t* w[RPW];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < RPW; ++j) {
     const int r = r0 + j;
     w[j] = r < P.E ? P.router_w + (size_t)r * P.H : (r == P.E ? P.gate_w : nullptr);
   }
-  float s[2][kRouteTokens], c[2][kRouteTokens];
+  float s[RPW][kRouteTokens], c[RPW][kRouteTokens];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int j = 0; j < RPW; ++j)
 #pragma unroll
     for (int t = 0; t < kRouteTokens; ++t) s[j][t] = c[j][t] = 0.f;
   for (int c0 = lane * 8; c0 < P.H; c0 += 256) {
-    float wf[2][8];
+    float wf[RPW][8];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < RPW; ++j) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (w[j]) v = *reinterpret_cast<const uint4*>(w[j] + c0);
       wf[j][0] = bf16_lo(v.x); wf[j][1] = bf16_hi(v.x); wf[j][2] = bf16_lo(v.y); wf[j][3] = bf16_hi(v.y);
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(256) k_route_b(const __grid_constant__ BatchPa
       const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                            bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < RPW; ++j)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float tt, e2;
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(256) k_route_b(const __grid_constant__ BatchPa
     }
   }
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int j = 0; j < RPW; ++j)
 #pragma unroll
     for (int t = 0; t < kRouteTokens; ++t) {
       warp_sum2(s[j][t], c[j][t]);
@@ -100,13 +102,14 @@ __global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchPar
   if (lane == 0) P.slot_w[(size_t)P.T * P.K + t] = 1.0f / (1.0f + expf(-sl));
 }
 
-// Block e: the expert's count, offset (counts of the experts below) and
-// active index, the slots of its tokens (ascending), their weights and
-// choice indices, and the gather of their x rows into x_perm.
+// Blocks (e, 0 .. kGatherSplit-1): the expert's count, offset (counts of the
+// experts below) and active index; block (e, 0) writes them and the slots of
+// its tokens (ascending), their weights and choice indices; every block
+// gathers its share of the x rows into x_perm.
 __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchParams P) {
   __shared__ int s_red[3][8];
   __shared__ int16_t s_tok[kBatchMaxT];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, e = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, e = blockIdx.x, part = blockIdx.y;
   const uint32_t* row = P.bitmap + (size_t)e * P.tw;
   int cb = 0, nb = 0;
   for (int e2 = tid; e2 < e; e2 += 256) {
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchP
     ub += s_red[1][w];
     cnt += s_red[2][w];
   }
-  if (tid == 0) {
+  if (tid == 0 && part == 0) {
     P.r_counts[e] = cnt;
     P.r_offsets[e] = off;
     if (cnt > 0) P.r_active[ub] = e;
@@ -153,15 +156,18 @@ __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchP
       int k = 0;
       while (k < P.K - 1 && P.ids[(size_t)t * P.K + k] != e) ++k;
       const int slot = off + rank;
-      P.slot_of[(size_t)t * P.K + k] = slot;
-      P.slot_w[slot] = P.p[(size_t)t * P.K + k];
-      P.r_perm[slot] = t * P.K + k;
+      if (part == 0) {
+        P.slot_of[(size_t)t * P.K + k] = slot;
+        P.slot_w[slot] = P.p[(size_t)t * P.K + k];
+        P.r_perm[slot] = t * P.K + k;
+      }
       s_tok[rank] = static_cast<int16_t>(t);
     }
   }
   __syncthreads();
   const int chunks = P.H / 8;  // 16-byte chunks of a row
-  for (int i = tid; i < cnt * chunks; i += 256) {
+  const int j0 = cnt * part / kGatherSplit, j1 = cnt * (part + 1) / kGatherSplit;
+  for (int i = j0 * chunks + tid; i < j1 * chunks; i += 256) {
     const int j = i / chunks, q = i - j * chunks;
     reinterpret_cast<uint4*>(P.x_perm + (size_t)(off + j) * P.H)[q] =
         reinterpret_cast<const uint4*>(P.x + (size_t)s_tok[j] * P.H)[q];
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(256) k_combine_b(const __grid_constant__ Batch
 cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream) {
   k_route_b<<<dim3((p.T + kRouteTokens - 1) / kRouteTokens, (p.E + 1 + kRouteRows - 1) / kRouteRows), 256, 0, stream>>>(p);
   k_topk_b<<<(p.T + 7) / 8, 256, 0, stream>>>(p);
-  k_bucket_b<<<p.E, 256, 0, stream>>>(p);
+  k_bucket_b<<<dim3(p.E, kGatherSplit), 256, 0, stream>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   err = launch_gemm_gate_up(p, stream);

@@ -4,21 +4,21 @@
 // A group is one active expert (its slots offsets[e] .. + counts[e], x rows
 // gathered in x_perm) or the shared expert (slot T K + t for every token t,
 // x itself).  Groups are cut into units of at most kGemmNC slots (the MMA N)
-// and a 256-row (gate / up) or 256-column (down) tile of the weights; the
-// persistent blocks take units round robin.
+// and a tile of the weights; the persistent blocks take units round robin.
 //
-//   gate / up (PHASE 0):  G = W_g X^T, U = W_u X^T over K = H, 128 rows of I
-//     per unit for each of the two matrices; h = silu(G) * U * w(slot),
-//     stored as bf16 rows h_ws[slot][I].
+//   gate / up (PHASE 0):  [G; U] = [W_g; W_u] X^T over K = H: 64 rows of I
+//     of the gate matrix over the same 64 rows of the up matrix form one
+//     128-row A tile, so one accumulator holds both; h = silu(G) * U *
+//     w(slot), stored as bf16 rows h_ws[slot][hw].
 //   down (PHASE 1):  Y^T = downT^T H^T over K = I (Is for the shared expert),
 //     256 output columns per unit (two 128-column accumulators); the downT
 //     tile is the MN-major A operand, straight from its [I][H] rows;
 //     y_ws[slot][H] in fp32.
 //
-// Block roles: warp 0 lane 0 moves tiles with TMA into a ring of
-// kGemmStages slots (two 128 x 64 A tiles + an NC x 64 B tile, 128-byte
-// swizzled); warp 1 owns the tensor memory (256 columns: two fp32
-// accumulators of up to 128 columns) and lane 0 issues the MMAs (M = 128,
+// Block roles: warp 0 lane 0 moves tiles with TMA into a ring of stages
+// (one or two 128 x 64 A tiles + an NC x 64 B tile, 128-byte swizzled);
+// warp 1 owns the tensor memory (two fp32 accumulators of up to kGemmNC
+// columns) and lane 0 issues the MMAs (M = 128,
 // N = slots rounded up to 16, K = 16), committing each ring slot back to the
 // producer and each finished unit to the epilogue; warps 2..5 read the
 // accumulators (warp w reads lanes 32 (w % 4) ..) and write the unit's rows.
@@ -35,8 +35,6 @@
 namespace moe {
 
 namespace {
-
-constexpr int kS = kGemmStages;
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets, descriptor version 1, 128-byte swizzle.
@@ -84,6 +82,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Barrier of the four epilogue warps (named barrier 1), and the same
+// barrier reducing a flag (true if it holds in every thread), so that the
+// four warps always leave their loop together.
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ bool aborted(const int* f) { return *reinterpret_cast<const volatile int*>(f) != 0; }
 __device__ __forceinline__ void set_abort(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
 
@@ -101,23 +112,27 @@ struct Unit {
 
 template <int PHASE>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant__ BatchParams P) {
+  constexpr int kS = PHASE == 0 ? kGemmStages0 : kGemmStages1;
+  constexpr int kSB = PHASE == 0 ? kGemmStageBytes0 : kGemmStageBytes1;
+  constexpr int kA = PHASE == 0 ? 128 * 128 : 2 * 128 * 128;  // A bytes of a stage; the B tile follows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* ring = sm;  // kS x kGemmStageBytes, 1024-byte aligned slots
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kS * kGemmStageBytes);
+  uint8_t* ring = sm;  // kS x kSB, 1024-byte aligned slots
+  float* exch = reinterpret_cast<float*>(sm + kS * kSB);  // gate / up: [NC][64] gate values
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kS * kSB + (PHASE == 0 ? kGemmExch : 0));
   uint64_t* empty = full + kS;
   uint64_t* acc_full = empty + kS;
   uint64_t* acc_empty = acc_full + 1;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_cum[kBatchMaxE + 2];  // units before group g
+  __shared__ int s_cum[kBatchMaxE + 2];     // units before group g
   __shared__ int s_grp[kBatchMaxE + 1][3];  // group g: expert (-1 shared), first slot, slots
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = P.T, K = P.K;
-  // row / column tiles per slot chunk
-  const int MT = PHASE == 0 ? P.I / 128 : P.H / 256;
-  const int MT_s = PHASE == 0 ? P.Is / 128 : P.H / 256;
+  // weight tiles per slot chunk: gate / up 64 rows of I (Is), down 256 columns of H
+  const int MT = PHASE == 0 ? P.I / 64 : P.H / 256;
+  const int MT_s = PHASE == 0 ? P.Is / 64 : P.H / 256;
 
   // ---- groups and their unit counts (warp 0), barriers (thread 64), tensor memory (warp 1)
   if (warp == 0) {
@@ -169,7 +184,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
     mbar_fence_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)), "r"(256)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(2 * kGemmNC)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -210,33 +226,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
         unit_of(u, w);
         const int nk = w.shared ? nk_s : nk_r;
         const int npad = (w.n + 15) & ~15;
-        const uint32_t bytes = 2 * 128 * 128 + (uint32_t)npad * 128;
+        const uint32_t bytes = kA + (uint32_t)npad * 128;
+        const CUtensorMap* m = w.shared ? &P.tm_w64_s : &P.tm_w64_e;
+        const int I = w.shared ? P.Is : P.I;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(&empty[stage], ph ^ 1u)) {
             set_abort(&s_abort);
             break;
           }
-          uint8_t* slot = ring + (size_t)stage * kGemmStageBytes;
+          uint8_t* slot = ring + (size_t)stage * kSB;
           mbar_arrive_expect_tx(&full[stage], bytes);
           if (PHASE == 0) {
-            // gate and up tiles: rows tile*128 .. of matrices 0 and 1, k columns kc*64 ..
-            const CUtensorMap* m = w.shared ? &P.tm_w128_s : &P.tm_w128_e;
-            const int I = w.shared ? P.Is : P.I;
-            const int rb = w.e * 3 * I + w.tile * 128;
+            // 64 gate rows over the same 64 up rows (one 128-row A tile), k columns kc*64 ..
+            const int rb = w.e * 3 * I + w.tile * 64;
             tma_load_2d(slot, m, kc * 64, rb, &full[stage], pol_w);
-            tma_load_2d(slot + 16384, m, kc * 64, rb + I, &full[stage], pol_w);
+            tma_load_2d(slot + 8192, m, kc * 64, rb + I, &full[stage], pol_w);
             const CUtensorMap* bm = w.shared ? &P.tm_x : &P.tm_xp;
             for (int j = 0; j < npad; j += 16)
-              tma_load_2d(slot + 32768 + j * 128, bm, kc * 64, w.brow0 + j, &full[stage], pol_x);
+              tma_load_2d(slot + kA + j * 128, bm, kc * 64, w.brow0 + j, &full[stage], pol_x);
           } else {
             // downT rows kc*64 .. (k) x columns tile*256 .. (m), four 64-column boxes
-            const CUtensorMap* m = w.shared ? &P.tm_w64_s : &P.tm_w64_e;
-            const int I = w.shared ? P.Is : P.I;
             const int r = (w.e * 3 + 2) * I + kc * 64;
 #pragma unroll
             for (int q = 0; q < 4; ++q) tma_load_2d(slot + q * 8192, m, w.tile * 256 + 64 * q, r, &full[stage], pol_w);
             for (int j = 0; j < npad; j += 16)
-              tma_load_2d(slot + 32768 + j * 128, &P.tm_h, kc * 64, w.brow0 + j, &full[stage], pol_x);
+              tma_load_2d(slot + kA + j * 128, &P.tm_h, kc * 64, w.brow0 + j, &full[stage], pol_x);
           }
           if (++stage == kS) {
             stage = 0;
@@ -246,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
       }
       // wind down: every issued copy has landed before the block exits
       for (int i = 0; i < kS; ++i) {
-        // slot i was last filled in phase ph' where (stage, ph) is the next fill
+        // slot i was last filled in the phase before (stage, ph), the next fill
         const uint32_t last = i < stage ? ph : ph ^ 1u;
         mbar_wait(&full[i], last);
       }
@@ -274,21 +288,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(ring + (size_t)stage * kGemmStageBytes);
+          const uint32_t sa = smem_u32(ring + (size_t)stage * kSB);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(sa + 32768 + ks * 32, 16, 1024);
-            uint64_t a0, a1;
-            if (PHASE == 0) {
-              a0 = smem_desc(sa + ks * 32, 16, 1024);
-              a1 = smem_desc(sa + 16384 + ks * 32, 16, 1024);
-            } else {
-              a0 = smem_desc(sa + ks * 2048, 8192, 1024);
-              a1 = smem_desc(sa + 16384 + ks * 2048, 8192, 1024);
-            }
+            const uint64_t bd = smem_desc(sa + kA + ks * 32, 16, 1024);
             const uint32_t acc = (kc > 0 || ks > 0) ? 1u : 0u;
-            umma(tmem, a0, bd, idesc, acc);
-            umma(tmem + 128, a1, bd, idesc, acc);
+            if (PHASE == 0) {
+              umma(tmem, smem_desc(sa + ks * 32, 16, 1024), bd, idesc, acc);
+            } else {
+              umma(tmem, smem_desc(sa + ks * 2048, 8192, 1024), bd, idesc, acc);
+              umma(tmem + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bd, idesc, acc);
+            }
           }
           umma_commit(&empty[stage]);
           pending = true;
@@ -311,36 +321,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int m = 32 * (warp & 3) + lane;  // accumulator row (TMEM lane) of this thread
-    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+    const int q = warp & 3;  // lane quarter of the accumulator this warp reads
+    const int m = 32 * q + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     uint32_t acc_ph = 0;
-    for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit w;
       unit_of(u, w);
-      if (!mbar_wait(acc_full, acc_ph)) {
+      const bool ok = mbar_wait(acc_full, acc_ph) && !aborted(&s_abort);
+      if (!epilogue_all(ok)) {
         set_abort(&s_abort);
         break;
       }
       tc_fence_after();
-      for (int j0 = 0; j0 < w.n; j0 += 16) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tmem + lane_addr + (uint32_t)j0, r0);
-        tmem_ld16(tmem + lane_addr + 128u + (uint32_t)j0, r1);
-        if (PHASE == 0) {
-          const int i = w.tile * 128 + m;
-          // h rows of the shared slots start at T K
+      if (PHASE == 0) {
+        // rows 0..63 of the accumulator are gate rows, 64..127 the same up
+        // rows: the gate half goes through shared memory to the up half
+        const int r = m & 63;
+        if (q < 2) {
+          for (int j0 = 0; j0 < w.n; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = j0 + jj;
-            if (j < w.n) {
-              const int slot = w.slot0 + j;
-              const float g = __uint_as_float(r0[jj]), up = __uint_as_float(r1[jj]);
-              const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
-              P.h_ws[(size_t)slot * (size_t)P.hw + i] = float_to_bf16_rne(h);
+            for (int jj = 0; jj < 16; ++jj) exch[(j0 + jj) * 64 + r] = __uint_as_float(v[jj]);
+          }
+        }
+        epilogue_sync();
+        if (q >= 2) {
+          const int i = w.tile * 64 + r;
+          for (int j0 = 0; j0 < w.n; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = j0 + jj;
+              if (j < w.n) {
+                const int slot = w.slot0 + j;
+                const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
+                const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
+                P.h_ws[(size_t)slot * (size_t)P.hw + i] = float_to_bf16_rne(h);
+              }
             }
           }
-        } else {
-          const int c = w.tile * 256 + m;
+        }
+        epilogue_sync();  // the exchange buffer is free for the next unit
+      } else {
+        const int c = w.tile * 256 + m;
+        for (int j0 = 0; j0 < w.n; j0 += 16) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tmem + lane_addr + (uint32_t)j0, r0);
+          tmem_ld16(tmem + lane_addr + (uint32_t)kGemmNC + (uint32_t)j0, r1);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
@@ -361,7 +391,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
   if (aborted(&s_abort) && tid == 0) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kGemmNC) : "memory");
 }
 
 namespace {
@@ -399,9 +430,7 @@ cudaError_t batch_tensor_maps(BatchParams& p) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = gemm_encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const long long er = (long long)p.E * 3 * p.I, sr = 3LL * p.Is, TK = (long long)p.T * p.K;
-  if (!encode_2d(fn, &p.tm_w128_e, p.expert_w, er, p.H, 64, 128) ||
-      !encode_2d(fn, &p.tm_w128_s, p.shexp_w, sr, p.H, 64, 128) ||
-      !encode_2d(fn, &p.tm_w64_e, p.expert_w, er, p.H, 64, 64) ||
+  if (!encode_2d(fn, &p.tm_w64_e, p.expert_w, er, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_w64_s, p.shexp_w, sr, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_xp, p.x_perm, TK, p.H, 64, 16) || !encode_2d(fn, &p.tm_x, p.x, p.T, p.H, 64, 16) ||
       !encode_2d(fn, &p.tm_h, p.h_ws, TK + p.T, p.hw, 64, 16))
@@ -411,9 +440,10 @@ cudaError_t batch_tensor_maps(BatchParams& p) {
 
 template <int PHASE>
 static cudaError_t launch_gemm(const BatchParams& p, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(k_gemm<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  constexpr int smem = PHASE == 0 ? kGemmSmem0 : kGemmSmem1;
+  cudaError_t err = cudaFuncSetAttribute(k_gemm<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  k_gemm<PHASE><<<p.G, kGemmThreads, kGemmSmem, stream>>>(p);
+  k_gemm<PHASE><<<p.G, kGemmThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

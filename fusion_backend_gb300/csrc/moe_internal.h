@@ -81,8 +81,7 @@ struct LayerParams {
 // grouped GEMMs on the tcgen05 tensor cores and a fixed-order combine.
 constexpr int kBatchMaxT = 1024;
 constexpr int kBatchMaxE = 256;
-constexpr int kGemmNC = 128;      // slots (tokens) per GEMM unit: the MMA N, at most
-constexpr int kGemmStages = 4;    // shared-memory ring depth of the GEMM kernels
+constexpr int kGemmNC = 64;       // slots (tokens) per GEMM unit: the MMA N, at most
 constexpr int kGemmThreads = 192; // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
 
 struct BatchParams {
@@ -115,11 +114,9 @@ struct BatchParams {
   int32_t* r_active;  // [E] active experts ascending
   int32_t* r_nactive; // [1]
   // Tensor maps (bf16, 128-byte swizzle): weight rows of the expert blocks
-  // and of the shared block with boxes of 64 x 128 (gate / up tiles) and
-  // 64 x 64 (downT tiles, MN-major), and the B operands: x_perm, x, h_ws
-  // rows with boxes of 64 x 16.
-  CUtensorMap tm_w128_e;
-  CUtensorMap tm_w128_s;
+  // and of the shared block with boxes of 64 x 64 (gate / up half tiles and
+  // downT tiles), and the B operands: x_perm, x, h_ws rows with boxes of
+  // 64 x 16.
   CUtensorMap tm_w64_e;
   CUtensorMap tm_w64_s;
   CUtensorMap tm_xp;
@@ -131,9 +128,14 @@ cudaError_t batch_tensor_maps(BatchParams& p);
 // Enqueues the whole batched layer (kBatchLaunches kernels).
 cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream);
 constexpr int kBatchLaunches = 6;
-// Shared-memory bytes of the GEMM kernels.
-constexpr int kGemmStageBytes = 2 * 128 * 128 + kGemmNC * 128;  // two 128 x 64 A tiles + an NC x 64 B tile
-constexpr int kGemmSmem = kGemmStages * kGemmStageBytes + 1024 + 256;
+// Ring depth and stage bytes of the GEMM kernels: gate / up stages hold a
+// 128 x 64 A tile (64 gate rows over 64 up rows) and an NC x 64 B tile;
+// down stages two 128 x 64 A tiles (MN-major) and an NC x 64 B tile.
+constexpr int kGemmStages0 = 8, kGemmStageBytes0 = 128 * 128 + kGemmNC * 128;
+constexpr int kGemmStages1 = 5, kGemmStageBytes1 = 2 * 128 * 128 + kGemmNC * 128;
+constexpr int kGemmExch = 64 * kGemmNC * 4;  // gate / up epilogue: the gate half of the accumulator
+constexpr int kGemmSmem0 = kGemmStages0 * kGemmStageBytes0 + kGemmExch + 1024 + 256;
+constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;
 
 // Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
 // Launched behind the previous kernel of the stream with programmatic
