@@ -114,7 +114,9 @@ template <int PHASE>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant__ BatchParams P) {
   constexpr int kS = PHASE == 0 ? kGemmStages0 : kGemmStages1;
   constexpr int kSB = PHASE == 0 ? kGemmStageBytes0 : kGemmStageBytes1;
-  constexpr int kA = PHASE == 0 ? 128 * 128 : 2 * 128 * 128;  // A bytes of a stage; the B tile follows
+  constexpr int kA = PHASE == 0 ? 128 * 128 : 2 * 128 * 128;  // A bytes of a 64-wide K sub-chunk; its B tile follows
+  constexpr int kKSub = PHASE == 0 ? kGemmKSub0 : 1;            // K sub-chunks per stage
+  constexpr int kSub = kA + kGemmNC * 128;                       // bytes of one sub-chunk
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = sm;  // kS x kSB, 1024-byte aligned slots
@@ -211,8 +213,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
     // down reads h_ws at the slot rows
     w.brow0 = (PHASE == 0 && w.shared) ? chunk * kGemmNC : w.slot0;
   };
-  const int nk_r = PHASE == 0 ? P.H / 64 : P.I / 64;
-  const int nk_s = PHASE == 0 ? P.H / 64 : P.Is / 64;
+  // stages per unit (K / (64 kKSub))
+  const int nk_r = PHASE == 0 ? P.H / (64 * kKSub) : P.I / 64;
+  const int nk_s = PHASE == 0 ? P.H / (64 * kKSub) : P.Is / 64;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
         unit_of(u, w);
         const int nk = w.shared ? nk_s : nk_r;
         const int npad = (w.n + 15) & ~15;
-        const uint32_t bytes = kA + (uint32_t)npad * 128;
+        const uint32_t bytes = kKSub * (kA + (uint32_t)npad * 128);
         const CUtensorMap* m = w.shared ? &P.tm_w64_s : &P.tm_w64_e;
         const int I = w.shared ? P.Is : P.I;
         for (int kc = 0; kc < nk; ++kc) {
@@ -237,13 +240,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
           uint8_t* slot = ring + (size_t)stage * kSB;
           mbar_arrive_expect_tx(&full[stage], bytes);
           if (PHASE == 0) {
-            // 64 gate rows over the same 64 up rows (one 128-row A tile), k columns kc*64 ..
+            // per sub-chunk: 64 gate rows over the same 64 up rows (one
+            // 128-row A tile) and the B rows, k columns (kKSub kc + sc) * 64 ..
             const int rb = w.e * 3 * I + w.tile * 64;
-            tma_load_2d(slot, m, kc * 64, rb, &full[stage], pol_w);
-            tma_load_2d(slot + 8192, m, kc * 64, rb + I, &full[stage], pol_w);
             const CUtensorMap* bm = w.shared ? &P.tm_x : &P.tm_xp;
-            for (int j = 0; j < npad; j += 16)
-              tma_load_2d(slot + kA + j * 128, bm, kc * 64, w.brow0 + j, &full[stage], pol_x);
+#pragma unroll
+            for (int sc = 0; sc < kKSub; ++sc) {
+              const int k0 = (kc * kKSub + sc) * 64;
+              uint8_t* sub = slot + sc * kSub;
+              tma_load_2d(sub, m, k0, rb, &full[stage], pol_w);
+              tma_load_2d(sub + 8192, m, k0, rb + I, &full[stage], pol_w);
+              for (int j = 0; j < npad; j += 16)
+                tma_load_2d(sub + kA + j * 128, bm, k0, w.brow0 + j, &full[stage], pol_x);
+            }
           } else {
             // downT rows kc*64 .. (k) x columns tile*256 .. (m), four 64-column boxes
             const int r = (w.e * 3 + 2) * I + kc * 64;
@@ -290,11 +299,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * kSB);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(sa + kA + ks * 32, 16, 1024);
+          for (int ks = 0; ks < 4 * kKSub; ++ks) {
+            const uint32_t sub = sa + (ks >> 2) * kSub;  // sub-chunk base
+            const uint64_t bd = smem_desc(sub + kA + (ks & 3) * 32, 16, 1024);
             const uint32_t acc = (kc > 0 || ks > 0) ? 1u : 0u;
             if (PHASE == 0) {
-              umma(tmem, smem_desc(sa + ks * 32, 16, 1024), bd, idesc, acc);
+              umma(tmem, smem_desc(sub + (ks & 3) * 32, 16, 1024), bd, idesc, acc);
             } else {
               umma(tmem, smem_desc(sa + ks * 2048, 8192, 1024), bd, idesc, acc);
               umma(tmem + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bd, idesc, acc);

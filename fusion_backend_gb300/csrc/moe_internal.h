@@ -128,10 +128,12 @@ cudaError_t batch_tensor_maps(BatchParams& p);
 // Enqueues the whole batched layer (kBatchLaunches kernels).
 cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream);
 constexpr int kBatchLaunches = 6;
-// Ring depth and stage bytes of the GEMM kernels: gate / up stages hold a
-// 128 x 64 A tile (64 gate rows over 64 up rows) and an NC x 64 B tile;
+// Ring depth and stage bytes of the GEMM kernels: gate / up stages hold
+// kGemmKSub0 pairs of a 128 x 64 A tile (64 gate rows over 64 up rows) and
+// an NC x 64 B tile;
 // down stages two 128 x 64 A tiles (MN-major) and an NC x 64 B tile.
-constexpr int kGemmStages0 = 8, kGemmStageBytes0 = 128 * 128 + kGemmNC * 128;
+constexpr int kGemmKSub0 = 2;  // gate / up: 64-wide K sub-chunks per stage (256 bytes of each weight row)
+constexpr int kGemmStages0 = 4, kGemmStageBytes0 = kGemmKSub0 * (128 * 128 + kGemmNC * 128);
 constexpr int kGemmStages1 = 5, kGemmStageBytes1 = 2 * 128 * 128 + kGemmNC * 128;
 constexpr int kGemmExch = 64 * kGemmNC * 4;  // gate / up epilogue: the gate half of the accumulator
 constexpr int kGemmSmem0 = kGemmStages0 * kGemmStageBytes0 + kGemmExch + 1024 + 256;
