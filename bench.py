@@ -12,9 +12,12 @@ the host cores instead (the reference arm).
 
 With ``--config batched_bf16 --T 64`` (or 256) the same layer runs on the
 batched path (routing, expert-sorted gather, grouped GEMMs on the tensor
-cores, combine).
+cores, combine).  ``--config stack_q4`` runs the 48-layer 4-bit decode stack
+(pre-norm RMSNorm and residual add per layer, independent seeded layers);
+a step is one token through all 48 layers, and each token's output feeds the
+next token's input (128 sequential tokens by default).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4|batched_bf16] [--T T]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4|batched_bf16|stack_q4] [--T T]
 """
 
 from __future__ import annotations
@@ -45,7 +48,8 @@ SEED = 20261202
 # dram__bytes_read.sum + dram__bytes_write.sum of one k_rows launch from the
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
-NCU_TRAFFIC_BYTES = {"decode_bf16": 83_148_800, "decode_q4": 23_104_768, "batched_bf16": None}
+NCU_TRAFFIC_BYTES = {"decode_bf16": 83_148_800, "decode_q4": 23_104_768, "batched_bf16": None, "stack_q4": 23_104_768}
+STACK_LAYERS = 48
 
 
 def peaks():
@@ -65,6 +69,8 @@ def workload(cfg: str, T: int):
         "decode_bf16": f"decode bf16 MoE FFN layer: T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "decode_q4": f"decode 4-bit MoE FFN layer (blocks of 32, fp16 scale): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_bf16": f"batched bf16 MoE FFN layer (grouped GEMMs): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
+        "stack_q4": f"{STACK_LAYERS}-layer 4-bit decode stack (pre-norm RMSNorm + residual per layer, independent seeded "
+                    f"layers), T=1, sequential tokens; layer H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
     }[cfg]
     return shapes, wfmt, name
 
@@ -180,23 +186,143 @@ def run_reference(args, shapes, wfmt, name):
     return 0
 
 
+# ----------------------------------------------------------------------------- 48-layer stack (config 4)
+
+
+def run_stack(args, shapes, wfmt, name):
+    """One step = one token through STACK_LAYERS layers in block form (x_res updated in place); the timed
+    steps are consecutive tokens, each starting from the previous token's output."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import torch
+
+    import fusion_backend_gb300 as fb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s1 = datagen.Shapes(1, H, E, K_TOP, I, IS)
+
+    def gen(l):
+        lay = datagen.make_layer(SEED + 1000 + l, s1, wfmt)
+        return (torch.from_numpy(lay.router_w.view(np.int16)).to(dev), torch.from_numpy(lay.expert_w).to(dev),
+                torch.from_numpy(lay.shexp_w).to(dev), torch.from_numpy(lay.shexp_gate_w.view(np.int16)).to(dev))
+
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as pool:
+        layers = list(pool.map(gen, range(STACK_LAYERS)))
+    plan, ws_bytes = fb.moe_ffn_prepare(s1, fb.ACT_BF16, wfmt)
+    launches = fb.moe_ffn_query(plan, fb.QUERY_LAUNCHES_PER_EXECUTE) * STACK_LAYERS
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    x0 = torch.from_numpy(datagen.normal_f32(SEED, 7, H, 1.0).reshape(1, H)).to(dev)
+    x_res = x0.clone()
+    stream = torch.cuda.Stream(device=dev)
+
+    def token_pass():
+        for r, ew, sw, gv in layers:
+            fb.moe_ffn_execute_block(plan, ws, x_res, r, ew, sw, gv, eps=1e-6, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            token_pass()
+    torch.cuda.synchronize()
+    if fb.moe_ffn_read_status(plan, ws, stream) != 0:
+        raise RuntimeError("device status after warm-up")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        token_pass()
+    x_res.copy_(x0)
+    torch.cuda.synchronize()
+    steps = args.steps
+    clocks = ClockSampler(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    time.sleep(0.2)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if fb.moe_ffn_read_status(plan, ws, stream) != 0:
+        raise RuntimeError("device status after the timed region")
+    final = x_res.cpu().numpy()
+    if not np.all(np.isfinite(final)):
+        raise RuntimeError("non-finite stack output")
+    value = steps * world / (ms / 1000.0)
+    ms_per_step = ms / steps
+    bytes_per_step = STACK_LAYERS * algorithmic_bytes(s1, wfmt, float(K_TOP))
+    peak, peak_kind = peaks()
+    achieved = bytes_per_step / (ms_per_step / 1000.0) / 1e9
+    # end to end: each token's input from pinned host memory, its output back
+    e2e_steps = min(steps, 64)
+    x_pin = torch.from_numpy(final.copy()).pin_memory()
+    out_pin = torch.empty((e2e_steps, 1, H), dtype=torch.float32).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            x_res.copy_(x_pin if i == 0 else out_pin[i - 1], non_blocking=True)
+            token_pass()
+            out_pin[i].copy_(x_res, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value = e2e_steps * world / (e0.elapsed_time(e1) / 1000.0)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1000.0 / STACK_LAYERS, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "q4b32 weights, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": name, "layers": STACK_LAYERS, "tokens": steps,
+                       "l2": f"inputs larger than L2: {STACK_LAYERS} layers of {datagen.expert_bytes(wfmt, H, I) * E / 1e9:.2f} GB",
+                       "parallelism": "replicas only" if world == 1 else f"{world} replicas"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": NCU_TRAFFIC_BYTES.get(args.config),
+                         "algorithmic_bytes_per_step": bytes_per_step,
+                         "kernel": "k_rows (+ k_route) per layer; duration = step time / layers"},
+            "cpu_baseline": None,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
+                    "steps": e2e_steps, "how": "eager public-API calls per token: pinned H2D of x, 48 layers, D2H"},
+            "gpu_launches": steps * launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    fb.moe_ffn_destroy(plan)
+    return 0
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64000)
-    ap.add_argument("--warmup", type=int, default=1600)
+    ap.add_argument("--steps", type=int, default=None, help="default: 64000 decode, 2000 batched, 128 stack")
+    ap.add_argument("--warmup", type=int, default=None, help="default: 1600 decode, 20 batched, 8 stack")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4", "batched_bf16"])
+    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4", "batched_bf16", "stack_q4"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_LAYER_COPIES, help="layer copies rotated (profiling: fewer)")
     args = ap.parse_args()
+    if args.config == "stack_q4":
+        args.T = 1
+    kind = "stack" if args.config == "stack_q4" else ("batched" if args.T > 8 else "decode")
+    if args.steps is None:
+        args.steps = {"decode": 64000, "batched": 2000, "stack": 128}[kind]
+    if args.warmup is None:
+        args.warmup = {"decode": 1600, "batched": 20, "stack": 8}[kind]
     shapes, wfmt, name = workload(args.config, args.T)
     if args.impl == "reference":
         return run_reference(args, shapes, wfmt, name)
+    if args.config == "stack_q4":
+        return run_stack(args, shapes, wfmt, name)
 
     import torch
 

@@ -24,7 +24,7 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 struct WsLayout {
   size_t ctrl, logits, partial, counts, offsets, perm, active, nactive, total;
   // batched path
-  size_t ids, p, bitmap, slot_of, slot_w, x_perm, h_ws, y_ws;
+  size_t ids, p, bitmap, slot_of, slot_w, x_perm, h_ws, y_ws, lbound;
 };
 
 }  // namespace
@@ -148,6 +148,7 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
     B.ctrl = reinterpret_cast<uint32_t*>(w + L.ctrl);
     B.logits = reinterpret_cast<float*>(w + L.logits);
     B.ls = (s.E + 1 + 3) / 4 * 4;
+    B.lbound = reinterpret_cast<float*>(w + L.lbound);
     B.ids = reinterpret_cast<int32_t*>(w + L.ids);
     B.p = reinterpret_cast<float*>(w + L.p);
     B.bitmap = reinterpret_cast<uint32_t*>(w + L.bitmap);
@@ -236,6 +237,8 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   if (path == 0) off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * 4);
   if (path == 1) {
     const size_t TK = T * K, H = s.H, hw = s.I > s.Is ? s.I : s.Is;
+    L.lbound = off;
+    off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
     L.ids = off;
     off = align256(off + TK * 4);
     L.p = off;

@@ -22,84 +22,216 @@ cudaError_t launch_gemm_down(const BatchParams& p, cudaStream_t stream);
 namespace {
 
 constexpr int kRouteTokens = 8;   // tokens per router block
-constexpr int kRouteRows = 8;     // router rows per block (1 per warp)
+constexpr int kRouteRows = 4;     // router rows per block (1 per warp, 4 warps)
 constexpr int kGatherSplit = 4;   // blocks per expert in the bucketing kernel
 
-// Router logits, error-free accumulated as in the decode router: the
-// products of bf16 weights and bf16 activations are exact in fp32, their
-// sum is kept as a (sum, compensation) pair and rounded once.  Block
-// (token group, row group): 8 warps x 1 row x 8 tokens.  The first block
-// also clears the control words and every block a share of the bitmap.
-__global__ void __launch_bounds__(256) k_route_b(const __grid_constant__ BatchParams P) {
+// Router logits in two passes.  Pass 1 (this kernel): plain fp32 sums of
+// the exact bf16 x bf16 products, with a bound on their error from the sum of
+// |w||x| -- each lane adds n = H/32 products and the warp tree adds 5
+// levels, so |l - exact| <= ((n + 5) u / (1 - (n + 5) u)) sum|w x| (u =
+// 2^-24); the bound kept is (n + 8) 2^-22 sum|w x| + 2^-20 |l|, about 4x
+// that (and it covers the final rounding of the exact value to fp32).  Pass 2 (the top-k kernel)
+// recomputes exactly every logit whose interval can reach the top-k.  Block
+// (token group, row group): 4 warps x 1 row x 8 tokens, small blocks so that
+// the whole grid is resident at once.  The first block also clears the
+// control words and every block a share of the bitmap.
+__global__ void __launch_bounds__(128, 7) k_route_b(const __grid_constant__ BatchParams P) {
+  extern __shared__ __align__(128) uint8_t route_smem[];  // the block's x rows (kRouteTokens x H bf16)
+  __shared__ uint64_t s_bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nblk = gridDim.x * gridDim.y, bid = blockIdx.y * gridDim.x + blockIdx.x;
-  for (int i = bid * 256 + tid; i < P.E * P.tw; i += nblk * 256) P.bitmap[i] = 0u;
+  pdl_launch_dependents();
+  pdl_wait();  // x and the workspace belong to the previous kernels of the stream until here
+  for (int i = bid * 128 + tid; i < P.E * P.tw; i += nblk * 128) P.bitmap[i] = 0u;
   if (bid == 0 && tid < kCtrlWords) P.ctrl[tid] = 0u;
   const int t0 = blockIdx.x * kRouteTokens;
-  constexpr int RPW = kRouteRows / 8;  // rows per warp
-  const int r0 = blockIdx.y * kRouteRows + RPW * warp;
-  const uint16_t* w[RPW];
-#pragma unroll
-  for (int j = 0; j < RPW; ++j) {
-    const int r = r0 + j;
-    w[j] = r < P.E ? P.router_w + (size_t)r * P.H : (r == P.E ? P.gate_w : nullptr);
+  const int nt = min(kRouteTokens, P.T - t0);
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    mbar_fence_init();
+    const uint32_t bytes = (uint32_t)nt * (uint32_t)P.H * 2u;
+    mbar_arrive_expect_tx(&s_bar, bytes);
+    bulk_g2s(route_smem, P.x + (size_t)t0 * P.H, bytes, &s_bar, policy_evict_last());
   }
-  float s[RPW][kRouteTokens], c[RPW][kRouteTokens];
+  const int r = blockIdx.y * kRouteRows + warp;
+  const uint16_t* w = r < P.E ? P.router_w + (size_t)r * P.H : P.gate_w;
+  float s[kRouteTokens], a[kRouteTokens];
 #pragma unroll
-  for (int j = 0; j < RPW; ++j)
+  for (int t = 0; t < kRouteTokens; ++t) s[t] = a[t] = 0.f;
+  __syncthreads();  // the barrier is initialised before any thread waits on it
+  const bool ok = mbar_wait(&s_bar, 0);
+  if (!ok && lane == 0) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  if (r <= P.E && ok) {
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(route_smem);
+    // the router row in chunks of 8 x 8 elements per lane, loaded ahead of use
+    for (int cb = 0; cb < P.H; cb += 8 * 256) {
+      uint4 wv[8];
 #pragma unroll
-    for (int t = 0; t < kRouteTokens; ++t) s[j][t] = c[j][t] = 0.f;
-  for (int c0 = lane * 8; c0 < P.H; c0 += 256) {
-    float wf[RPW][8];
+      for (int it = 0; it < 8; ++it) {
+        const int c0 = cb + it * 256 + lane * 8;
+        wv[it] = c0 < P.H ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int j = 0; j < RPW; ++j) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (w[j]) v = *reinterpret_cast<const uint4*>(w[j] + c0);
-      wf[j][0] = bf16_lo(v.x); wf[j][1] = bf16_hi(v.x); wf[j][2] = bf16_lo(v.y); wf[j][3] = bf16_hi(v.y);
-      wf[j][4] = bf16_lo(v.z); wf[j][5] = bf16_hi(v.z); wf[j][6] = bf16_lo(v.w); wf[j][7] = bf16_hi(v.w);
-    }
+      for (int it = 0; it < 8; ++it) {
+        const int c0 = cb + it * 256 + lane * 8;
+        if (c0 >= P.H) break;
+        const uint4 v = wv[it];
+        const float wf[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                             bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
-    for (int t = 0; t < kRouteTokens; ++t) {
-      if (t0 + t >= P.T) break;
-      const uint4 xv = *reinterpret_cast<const uint4*>(P.x + (size_t)(t0 + t) * P.H + c0);
-      const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
-                           bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+        for (int t = 0; t < kRouteTokens; ++t) {
+          if (t >= nt) break;
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * P.H + c0);
+          const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                               bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
-      for (int j = 0; j < RPW; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float tt, e2;
-          two_sum(s[j][t], __fmul_rn(wf[j][e], xf[e]), tt, e2);
-          s[j][t] = tt;
-          c[j][t] = __fadd_rn(c[j][t], e2);
+          for (int e = 0; e < 8; ++e) {
+            s[t] = fmaf(wf[e], xf[e], s[t]);
+            a[t] = fmaf(fabsf(wf[e]), fabsf(xf[e]), a[t]);
+          }
         }
+      }
     }
-  }
-#pragma unroll
-  for (int j = 0; j < RPW; ++j)
 #pragma unroll
     for (int t = 0; t < kRouteTokens; ++t) {
-      warp_sum2(s[j][t], c[j][t]);
-      if (lane == 0 && w[j] && t0 + t < P.T) P.logits[(size_t)(t0 + t) * P.ls + r0 + j] = __fadd_rn(s[j][t], c[j][t]);
+      const float st = warp_sum(s[t]), at = warp_sum(a[t]);
+      if (lane == 0 && t < nt) {
+        P.logits[(size_t)(t0 + t) * P.ls + r] = st;
+        P.lbound[(size_t)(t0 + t) * P.ls + r] = at * ((float)(P.H / 32 + 8) * 0x1p-22f) + fabsf(st) * 0x1p-20f;
+      }
     }
+  }
 }
 
-// Top-k of token t on warp t % 8 of block t / 8; the chosen experts' bits in
-// the selection bitmap and the shared-gate weight of the token's shared slot.
-__global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchParams P) {
-  const int lane = threadIdx.x & 31, t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= P.T) return;
-  const float* lg = P.logits + (size_t)t * P.ls;
-  float sl = 0.f;
-  if (lane == 0) sl = __ldcg(lg + P.E);
-  warp_topk<kBatchMaxE / 32>(lg, P.E, P.K, P.ids + (size_t)t * P.K, P.p + (size_t)t * P.K);
-  if (lane < P.K) {
-    const int e = P.ids[(size_t)t * P.K + lane];
-    atomicOr(&P.bitmap[(size_t)e * P.tw + (t >> 5)], 1u << (t & 31));
-    if (P.topk_ids) P.topk_ids[(size_t)t * P.K + lane] = e;
-    if (P.topk_w) P.topk_w[(size_t)t * P.K + lane] = P.p[(size_t)t * P.K + lane];
+// Exact logit of router row r (r == E: the shared-gate vector) for token t
+// by one warp: error-free sums as in the decode router; every lane returns it.
+__device__ float exact_logit(const BatchParams& P, int t, int r) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* w = r < P.E ? P.router_w + (size_t)r * P.H : P.gate_w;
+  const uint16_t* x = P.x + (size_t)t * P.H;
+  float s0 = 0.f, c0 = 0.f, s1 = 0.f, c1 = 0.f;  // two independent error-free sums (even / odd elements)
+  for (int cb = 0; cb < P.H; cb += 4 * 256) {
+    uint4 wv[4], xv[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int c = cb + it * 256 + lane * 8;
+      wv[it] = c < P.H ? *reinterpret_cast<const uint4*>(w + c) : make_uint4(0u, 0u, 0u, 0u);
+      xv[it] = c < P.H ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const uint4 v = wv[it], u = xv[it];
+      const float wf[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      const float xf[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float tt, e2;
+        two_sum(s0, __fmul_rn(wf[e], xf[e]), tt, e2);
+        s0 = tt;
+        c0 = __fadd_rn(c0, e2);
+        two_sum(s1, __fmul_rn(wf[e + 1], xf[e + 1]), tt, e2);
+        s1 = tt;
+        c1 = __fadd_rn(c1, e2);
+      }
+    }
   }
-  if (lane == 0) P.slot_w[(size_t)P.T * P.K + t] = 1.0f / (1.0f + expf(-sl));
+  float s, e;
+  two_sum(s0, s1, s, e);
+  float c = __fadd_rn(__fadd_rn(c0, c1), e);
+  warp_sum2(s, c);
+  return __fadd_rn(s, c);
+}
+
+// Top-k of token t (block t, 8 warps).  L = the k-th largest
+// lower end (l - b) of the logit intervals; the candidates are the experts
+// whose upper end (l + b) reaches L -- at least k of them, and every expert
+// of the exact top-k is among them (an expert outside has exact logit < L <=
+// the k-th exact logit).  Every warp finds the same candidate list; the warps
+// recompute the candidates' logits (and the shared-gate logit) exactly, in
+// turn; warp 0 takes the top-k over them (the others at -inf), marks the
+// selection bitmap and the token's shared-slot weight.
+__global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchParams P) {
+  constexpr int EPL = kBatchMaxE / 32;
+  __shared__ float s_ex[kBatchMaxE + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, t = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int E = P.E, K = P.K;
+  for (int e = tid; e <= E; e += 256) s_ex[e] = -INFINITY;
+  // every warp derives the same candidate list (registers; no barrier)
+  int cand_n = 0;
+  uint32_t cmask[EPL];
+  {
+    const float* lg = P.logits + (size_t)t * P.ls;
+    const float* bd = P.lbound + (size_t)t * P.ls;
+    float hi[EPL];
+    uint32_t key[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      const float l = e < E ? __ldcg(lg + e) : 0.f, b = e < E ? __ldcg(bd + e) : 0.f;
+      const float lo = __fsub_rd(l, b);
+      hi[i] = __fadd_ru(l, b);
+      key[i] = e < E ? float_order_key(lo != lo ? -INFINITY : lo) : 0u;
+    }
+    // the k-th largest lower end (order keys, one maximum removed per round)
+    uint32_t kth = 0u;
+    for (int j = 0; j < K; ++j) {
+      uint32_t best = 0u, bi = 0xFFFFFFFFu;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (key[i] > best) {
+          best = key[i];
+          bi = (uint32_t)(lane + 32 * i);
+        }
+      const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+      const uint32_t win = __reduce_min_sync(0xffffffffu, best == m ? bi : 0xFFFFFFFFu);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if ((uint32_t)(lane + 32 * i) == win) key[i] = 0u;
+      kth = m;
+    }
+    // candidates: upper end >= L (compared on order keys); ballot masks per slot
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      const bool c = e < E && float_order_key(hi[i] != hi[i] ? INFINITY : hi[i]) >= kth;
+      cmask[i] = __ballot_sync(0xffffffffu, c);
+      cand_n += __popc(cmask[i]);
+    }
+  }
+  // candidate c (expert order), and c == cand_n the shared-gate logit, on warp c % 8
+  for (int c = warp; c <= cand_n; c += 8) {
+    int e = E;
+    if (c < cand_n) {
+      int rem = c;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int pc = __popc(cmask[i]);
+        if (rem >= 0 && rem < pc) {
+          uint32_t m = cmask[i];
+          for (int q = 0; q < rem; ++q) m &= m - 1u;
+          e = 32 * i + __ffs((int)m) - 1;
+        }
+        rem -= pc;
+      }
+    }
+    const float v = exact_logit(P, t, e);
+    if (lane == 0) s_ex[e] = v;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    warp_topk<EPL, true>(s_ex, E, K, P.ids + (size_t)t * K, P.p + (size_t)t * K);
+    if (lane < K) {
+      const int e = P.ids[(size_t)t * K + lane];
+      atomicOr(&P.bitmap[(size_t)e * P.tw + (t >> 5)], 1u << (t & 31));
+      if (P.topk_ids) P.topk_ids[(size_t)t * K + lane] = e;
+      if (P.topk_w) P.topk_w[(size_t)t * K + lane] = P.p[(size_t)t * K + lane];
+    }
+    if (lane == 0) P.slot_w[(size_t)P.T * K + t] = 1.0f / (1.0f + expf(-s_ex[E]));
+  }
 }
 
 // Blocks (e, 0 .. kGatherSplit-1): the expert's count, offset (counts of the
@@ -110,6 +242,8 @@ __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchP
   __shared__ int s_red[3][8];
   __shared__ int16_t s_tok[kBatchMaxT];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, e = blockIdx.x, part = blockIdx.y;
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t* row = P.bitmap + (size_t)e * P.tw;
   int cb = 0, nb = 0;
   for (int e2 = tid; e2 < e; e2 += 256) {
@@ -178,6 +312,8 @@ __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchP
 // y of its shared slot; 8 columns per thread.
 __global__ void __launch_bounds__(256) k_combine_b(const __grid_constant__ BatchParams P) {
   const int t = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   for (int c = 8 * threadIdx.x; c < P.H; c += 8 * 256) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k <= P.K; ++k) {
@@ -195,18 +331,43 @@ __global__ void __launch_bounds__(256) k_combine_b(const __grid_constant__ Batch
 
 }  // namespace
 
+// Launch behind the previous kernel of the stream with programmatic stream
+// serialisation: every kernel of the batched path calls
+// griddepcontrol.launch_dependents at entry and griddepcontrol.wait before
+// its first access to memory, so only the launch latencies overlap.
+template <typename Kern>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, int threads, size_t smem, cudaStream_t stream,
+                              const BatchParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream) {
-  k_route_b<<<dim3((p.T + kRouteTokens - 1) / kRouteTokens, (p.E + 1 + kRouteRows - 1) / kRouteRows), 256, 0, stream>>>(p);
-  k_topk_b<<<(p.T + 7) / 8, 256, 0, stream>>>(p);
-  k_bucket_b<<<dim3(p.E, kGatherSplit), 256, 0, stream>>>(p);
-  cudaError_t err = cudaGetLastError();
+  const size_t route_smem = (size_t)kRouteTokens * p.H * 2;
+  if (route_smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(k_route_b, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t err = launch_pdl(k_route_b,
+                               dim3((p.T + kRouteTokens - 1) / kRouteTokens, (p.E + 1 + kRouteRows - 1) / kRouteRows),
+                               128, route_smem, stream, p);
+  if (err == cudaSuccess) err = launch_pdl(k_topk_b, dim3(p.T), 256, 0, stream, p);
+  if (err == cudaSuccess) err = launch_pdl(k_bucket_b, dim3(p.E, kGatherSplit), 256, 0, stream, p);
   if (err != cudaSuccess) return err;
   err = launch_gemm_gate_up(p, stream);
   if (err != cudaSuccess) return err;
   err = launch_gemm_down(p, stream);
   if (err != cudaSuccess) return err;
-  k_combine_b<<<p.T, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_combine_b, dim3(p.T), 256, 0, stream, p);
 }
 
 }  // namespace moe

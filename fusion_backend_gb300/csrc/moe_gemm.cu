@@ -136,7 +136,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
   const int MT = PHASE == 0 ? P.I / 64 : P.H / 256;
   const int MT_s = PHASE == 0 ? P.Is / 64 : P.H / 256;
 
-  // ---- groups and their unit counts (warp 0), barriers (thread 64), tensor memory (warp 1)
+  pdl_launch_dependents();
+  // ---- barriers (thread 64) and tensor memory (warp 1) before the wait on
+  // the previous kernel; then the groups and their unit counts (warp 0)
+  if (tid == 64) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(2 * kGemmNC)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_wait();
   if (warp == 0) {
     const int U = *P.r_nactive;
     // lane l sums groups [9l, 9l + 9) (U + 1 <= 257 groups)
@@ -174,22 +193,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
       if (g <= U + 1 && g < kBatchMaxE + 2) s_cum[g] = run;
       run += cnt[q];
     }
-  }
-  if (tid == 64) {
-    for (int i = 0; i < kS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
-    s_abort = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(2 * kGemmNC)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   __syncthreads();
   tc_fence_after();
@@ -453,8 +456,19 @@ static cudaError_t launch_gemm(const BatchParams& p, cudaStream_t stream) {
   constexpr int smem = PHASE == 0 ? kGemmSmem0 : kGemmSmem1;
   cudaError_t err = cudaFuncSetAttribute(k_gemm<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  k_gemm<PHASE><<<p.G, kGemmThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  // behind the previous kernel with programmatic stream serialisation (the
+  // kernel waits on it after its set-up)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm<PHASE>, p);
 }
 
 cudaError_t launch_gemm_gate_up(const BatchParams& p, cudaStream_t stream) { return launch_gemm<0>(p, stream); }

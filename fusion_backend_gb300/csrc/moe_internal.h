@@ -96,7 +96,8 @@ struct BatchParams {
   float* topk_w;             // optional [T][K]
   // workspace
   uint32_t* ctrl;
-  float* logits;  // [T][ls]
+  float* logits;  // [T][ls] fp32 logits (plain sums)
+  float* lbound;  // [T][ls] bound on |logit - exact logit|
   int ls;
   int32_t* ids;       // [T][K] chosen experts, rank order
   float* p;           // [T][K] their weights

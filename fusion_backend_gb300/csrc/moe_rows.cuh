@@ -164,14 +164,14 @@ MOE_DEV float warp_reduce8(const float* v) {
 // reduction) and, among lanes holding it, the lowest expert index, so equal
 // logits go to the lower index.  NaN ranks as -inf.  ids[0..K) in rank
 // order; pout = softmax over the K chosen logits.  E <= 32 * EPL, K <= 32.
-template <int EPL>
+template <int EPL, bool SMEM = false>
 MOE_DEV void warp_topk(const float* lg, int E, int K, int32_t* ids, float* pout) {
   const int lane = threadIdx.x & 31;
   uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    float v = e < E ? __ldcg(lg + e) : 0.f;
+    float v = e < E ? (SMEM ? lg[e] : __ldcg(lg + e)) : 0.f;
     v = v != v ? -INFINITY : v;
     key[i] = e < E ? float_order_key(v) : 0u;  // every real key is >= key(-inf) > 0
   }
