@@ -48,7 +48,7 @@ SEED = 20261202
 # dram__bytes_read.sum + dram__bytes_write.sum of one k_rows launch from the
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
-NCU_TRAFFIC_BYTES = {"decode_bf16": 83_148_800, "decode_q4": 23_104_768, "batched_bf16": None, "stack_q4": 23_104_768}
+NCU_TRAFFIC_BYTES = {"decode_bf16": 83_148_800, "decode_q4": 23_104_768, "batched_bf16": 823_113_984, "stack_q4": 23_104_768}
 STACK_LAYERS = 48
 
 
