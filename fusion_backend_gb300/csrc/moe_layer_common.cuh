@@ -35,25 +35,100 @@ MOE_DEV void warp_sum2(float& s, float& c) {
   }
 }
 
-// RMSNorm factor of one fp32 row: inv = 1/sqrt(mean(x^2) + eps), computed
-// from an error-free sum of squares and returned as hi + lo floats.  All
-// lanes of the warp return the same value.
-MOE_DEV void warp_norm_factor(const float* row, int H, float eps, float& hi, float& lo) {
+// Error-free sum of squares of row[h] for h in [h_begin, h_end) (multiples
+// of 4; the row 16-byte aligned) by one warp, as a (sum, compensation) pair
+// held by every lane; eight float4 loads in flight per lane.
+MOE_DEV void warp_sumsq(const float* row, int h_begin, int h_end, float& s, float& c) {
   const int lane = threadIdx.x & 31;
-  float s = 0.f, c = 0.f;
-  for (int h = lane; h < H; h += 32) {
-    const float v = row[h];
-    float p, e1, t, e2;
-    two_prod(v, v, p, e1);
-    two_sum(s, p, t, e2);
-    s = t;
-    c = __fadd_rn(c, __fadd_rn(e1, e2));
+  s = 0.f;
+  c = 0.f;
+  for (int h0 = h_begin + 4 * lane; h0 < h_end; h0 += 128 * 8) {
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int h = h0 + 128 * j;
+      v[j] = h < h_end ? *reinterpret_cast<const float4*>(row + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float p, e1, t, e2;
+        two_prod(e4[q], e4[q], p, e1);
+        two_sum(s, p, t, e2);
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(e1, e2));
+      }
+    }
   }
   warp_sum2(s, c);
-  const double ss = (double)s + (double)c;
-  const double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
-  hi = (float)inv;
-  lo = (float)(inv - (double)hi);
+}
+
+// inv = 1/sqrt((s + c)/H + eps) as hi + lo floats, in float-float
+// arithmetic (no fp64): the mean as a float-float, an fp32 estimate y of the
+// inverse square root and one Newton step y (1 + e/2), e = 1 - m y^2 formed
+// from exact products (relative error about 2^-46).
+MOE_DEV void norm_factor_ff(float s, float c, int H, float eps, float& hi, float& lo) {
+  float mh, ml;
+  {
+    const float q = __fdiv_rn(s, (float)H);
+    const float r = __fmaf_rn(-q, (float)H, s);  // s - q H, exact
+    const float q2 = __fdiv_rn(__fadd_rn(r, c), (float)H);
+    float th, tl;
+    two_sum(q, q2, th, tl);
+    two_sum(th, eps, mh, ml);
+    ml = __fadd_rn(ml, tl);
+  }
+  const float y = __frsqrt_rn(mh);
+  float y2h, y2l, ph, pl;
+  two_prod(y, y, y2h, y2l);
+  two_prod(mh, y2h, ph, pl);
+  const float e = __fsub_rn(__fsub_rn(__fsub_rn(1.0f, ph), pl), __fmaf_rn(mh, y2l, __fmul_rn(ml, y2h)));
+  const float corr = __fmul_rn(__fmul_rn(y, e), 0.5f);
+  two_sum(y, corr, hi, lo);
+}
+
+// RMSNorm factors of T fp32 rows (row t at x + t H) by all W warps of the
+// block: warp w sums squares over its H/W slice of every row, the W pairs
+// of a row meet in shared memory (red[W][T][2]), and thread t < T combines
+// them error-free in warp order and writes inv[2t], inv[2t+1].  Ends with a
+// block barrier.
+MOE_DEV void block_norm_factors(const float* x, int T, int H, float eps, float* red, float* inv, int W) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slice = (H / W + 3) & ~3;
+  const int hb = min(H, warp * slice), he = min(H, hb + slice);
+  for (int t = 0; t < T; ++t) {
+    float s, c;
+    warp_sumsq(x + (size_t)t * H, hb, he, s, c);
+    if (lane == 0) {
+      red[(warp * T + t) * 2] = s;
+      red[(warp * T + t) * 2 + 1] = c;
+    }
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < T) {
+    const int t = threadIdx.x;
+    float S = red[t * 2], C = red[t * 2 + 1];
+    for (int w = 1; w < W; ++w) {
+      float tt, e;
+      two_sum(S, red[(w * T + t) * 2], tt, e);
+      S = tt;
+      C = __fadd_rn(__fadd_rn(C, red[(w * T + t) * 2 + 1]), e);
+    }
+    float hi, lo;
+    norm_factor_ff(S, C, H, eps, hi, lo);
+    inv[2 * t] = hi;
+    inv[2 * t + 1] = lo;
+  }
+  __syncthreads();
+}
+
+// RMSNorm factor of one fp32 row by one warp (see block_norm_factors).
+MOE_DEV void warp_norm_factor(const float* row, int H, float eps, float& hi, float& lo) {
+  float s, c;
+  warp_sumsq(row, 0, H, s, c);
+  norm_factor_ff(s, c, H, eps, hi, lo);
 }
 
 // bf16(fp32(x * inv)) for the pre-norm block form, inv given as hi + lo.

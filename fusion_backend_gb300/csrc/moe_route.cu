@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(LayerParams P) {
   __shared__ float red_s[kWarps][TMAX];
   __shared__ float red_c[kWarps][TMAX];
   __shared__ float s_inv[TMAX][2];
+  __shared__ float s_red[kWarps * TMAX * 2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   const uint16_t* w = row < P.E ? P.router_w + (size_t)row * P.H : P.gate_w;
@@ -33,23 +34,25 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(LayerParams P) {
   pdl_launch_dependents();
   pdl_wait();
   if (row == 0 && tid < kCtrlWords) P.ctrl[tid] = 0u;
-  if (P.block_mode) {
-    for (int t = warp; t < P.T; t += kWarps) {
-      float hi, lo;
-      warp_norm_factor(static_cast<const float*>(P.x) + (size_t)t * P.H, P.H, P.eps, hi, lo);
-      if (lane == 0) {
-        s_inv[t][0] = hi;
-        s_inv[t][1] = lo;
-      }
-    }
-    __syncthreads();
+  // this thread's weight chunks, loaded ahead of the norm factors (H <= 4096:
+  // at most four 8-element chunks a thread)
+  constexpr int kChunks = kMaxH / (kRouteThreads * 8);
+  uint4 wreg[kChunks];
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) {
+    const int c0 = tid * 8 + i * kRouteThreads * 8;
+    wreg[i] = c0 < P.H ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
   }
+  if (P.block_mode) block_norm_factors(static_cast<const float*>(P.x), P.T, P.H, P.eps, s_red, &s_inv[0][0], kWarps);
   float s[TMAX], c[TMAX];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) s[t] = c[t] = 0.f;
   const bool exact_products = P.block_mode || P.act == 1;  // bf16 x bf16 is exact in fp32
-  for (int c0 = tid * 8; c0 < P.H; c0 += kRouteThreads * 8) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(w + c0);
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) {
+    const int c0 = tid * 8 + i * kRouteThreads * 8;
+    if (c0 >= P.H) break;
+    const uint4 wv = wreg[i];
     const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                          bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
 #pragma unroll

@@ -528,17 +528,11 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   }
   if (!mbar_wait(xbar, 0)) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
-  // block form: RMSNorm factors of the fp32 rows (warp t)
-  if (P.block_mode) {
-    for (int t = warp; t < T; t += kRowWarps) {
-      float hi, lo;
-      warp_norm_factor(reinterpret_cast<const float*>(xs) + (size_t)t * H, H, P.eps, hi, lo);
-      if (lane == 0) {
-        tb.inv[2 * t] = hi;
-        tb.inv[2 * t + 1] = lo;
-      }
-    }
-  }
+  // block form: RMSNorm factors of the fp32 rows, all warps (scratch: the
+  // partials region, unused before the stage loop)
+  if (P.block_mode)
+    block_norm_factors(reinterpret_cast<const float*>(xs), T, H, P.eps, reinterpret_cast<float*>(sm + P.off_part),
+                       tb.inv, kRowWarps);
   __syncthreads();
   if (warp == 0) {
     // active experts in ascending order (active index u): bitmap word l on
