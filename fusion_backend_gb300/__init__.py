@@ -42,6 +42,7 @@ EXPORTS = (
     "moe_ffn_execute_block",
     "moe_ffn_read_status",
     "moe_ffn_read_routing",
+    "moe_ffn_probe_timeout",
     "moe_ffn_query",
     "moe_ffn_destroy",
     "moe_ffn_strerror",
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.moe_ffn_execute_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_ffn_strerror.restype = ctypes.c_char_p
         L.moe_ffn_strerror.argtypes = [ctypes.c_int]
+        L.moe_ffn_probe_timeout.restype = ctypes.c_int
+        L.moe_ffn_probe_timeout.argtypes = [vp, vp, vp, sz, i32]
         L.moe_ffn_last_cuda_error.restype = ctypes.c_char_p
         L.moe_ffn_last_cuda_error.argtypes = []
         _lib = L
@@ -193,6 +196,11 @@ def moe_ffn_read_routing(plan, workspace, E: int, T: int, top_k: int, stream=Non
     _check(lib().moe_ffn_read_routing(plan, _ptr(workspace), _stream(stream), counts.ctypes.data, offsets.ctypes.data,
                                       perm.ctypes.data, active.ctypes.data, ctypes.byref(n)), "moe_ffn_read_routing")
     return counts, offsets, perm, active[: n.value].copy()
+
+
+def moe_ffn_probe_timeout(plan, workspace, which: int, stream=None, workspace_bytes=None) -> None:
+    nbytes = workspace_bytes if workspace_bytes is not None else workspace.numel() * workspace.element_size()
+    _check(lib().moe_ffn_probe_timeout(plan, _stream(stream), _ptr(workspace), nbytes, which), "moe_ffn_probe_timeout")
 
 
 def moe_ffn_query(plan, what: int) -> int:

@@ -325,6 +325,18 @@ int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_str
   return MOE_FFN_OK;
 }
 
+int moe_ffn_probe_timeout(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                          int32_t which) {
+  if (!valid_plan(plan) || !workspace || (which != 0 && which != 1)) return MOE_FFN_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws.total) return MOE_FFN_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MOE_FFN_ERR_MISALIGNED;
+  DeviceInfo* dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MOE_FFN_OK) return rc;
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan->ws.ctrl);
+  return cuda_status(launch_probe_timeout(ctrl, which, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value) {
   if (!valid_plan(plan) || !value) return MOE_FFN_ERR_INVALID_ARG;
   switch (what) {

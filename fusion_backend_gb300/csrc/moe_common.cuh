@@ -13,6 +13,16 @@ namespace moe {
 // Bound for every spin-wait in these kernels: iterations of a polling loop
 // that sleeps between polls.  Far above any legitimate wait (~0.5 s).
 constexpr uint32_t kSpinLimit = 1u << 22;
+// mbarrier waits: a wall-clock bound (the global nanosecond timer), since one
+// try_wait may itself suspend the thread for microseconds; plus an iteration
+// cap in case the timer did not advance.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+MOE_DEV unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+  return t;
+}
 
 MOE_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -43,8 +53,11 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // false when the bound ran out (the caller records an error and carries on
 // without blocking again).
 MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     if (i > 64) __nanosleep(32);
   }
   return false;

@@ -23,7 +23,7 @@ constexpr int kXPitch = 4160;            // tensor-core loops: bytes per token r
 
 // Control words at the start of the workspace.  The router kernel of each
 // call zeroes them before the row kernel of that call reads them.
-enum : int { kCtrlStatus = 0, kCtrlDone = 1, kCtrlWords = 64 };
+enum : int { kCtrlStatus = 0, kCtrlDone = 1, kCtrlProbe = 2, kCtrlWords = 64 };
 
 struct LayerParams {
   // shapes
@@ -144,6 +144,11 @@ constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;
 // Launched behind the previous kernel of the stream with programmatic
 // stream serialisation.
 cudaError_t launch_route(const LayerParams& p, cudaStream_t stream);
+
+// The failure-path probe (moe_route.cu): one thread waits, bounded, on an
+// mbarrier phase that never completes (which = 0) or on a control word that
+// never reaches its target (which = 1), then records the timeout.
+cudaError_t launch_probe_timeout(uint32_t* ctrl, int which, cudaStream_t stream);
 
 // Row kernel (moe_rows_*.cu).  rows_layout fills the layout fields and
 // returns the dynamic shared-memory bytes, or -1 when the shapes do not fit.

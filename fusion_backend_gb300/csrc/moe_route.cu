@@ -109,6 +109,35 @@ static cudaError_t launch_route_t(const LayerParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, k_route<TMAX>, p);
 }
 
+// The waits of the layer's kernels, each on a condition nothing satisfies:
+// the status word must end as the timeout status, and the kernel returns.
+__global__ void k_probe_timeout(uint32_t* ctrl, int which) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  ctrl[kCtrlStatus] = 0u;
+  ctrl[kCtrlProbe] = 0u;
+  bool ok = false;
+  if (which == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    ok = mbar_wait(&bar, 0);  // nothing arrives: phase 0 never completes
+  } else {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {  // the grid barrier's spin; the target is never reached
+      if (ld_acquire_gpu(&ctrl[kCtrlProbe]) >= 0xFFFFFFFFu) {
+        ok = true;
+        break;
+      }
+      if (i > 256) __nanosleep(32);
+    }
+  }
+  if (!ok) atomicExch(reinterpret_cast<int*>(&ctrl[kCtrlStatus]), kStatusTimeout);
+}
+
+cudaError_t launch_probe_timeout(uint32_t* ctrl, int which, cudaStream_t stream) {
+  k_probe_timeout<<<1, 32, 0, stream>>>(ctrl, which);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const LayerParams& p, cudaStream_t stream) {
   switch (tmax_for(p.T)) {
     case 1: return launch_route_t<1>(p, stream);

@@ -78,8 +78,9 @@ typedef enum { MOE_FFN_ACT_F32 = 0, MOE_FFN_ACT_BF16 = 1 } moe_ffn_act_dtype;
  * and the shared-gate vector are bf16 in both formats. */
 typedef enum {
   MOE_FFN_W_BF16 = 0,
-  /* 4-bit blocks of 32 along each row (the reduction dimension): one fp16
-   * scale d per block and 4-bit codes n in 0..15 with weight = d * (n - 8).
+  /* 4-bit blocks of 32 along each stored row (H elements for every matrix,
+   * see expert_w): one fp16 scale d per block and 4-bit codes n in 0..15
+   * with weight = d * (n - 8).
    * Row layout: C/2 bytes of codes (element 2j in the low nibble of byte j,
    * element 2j+1 in the high nibble), then C/32 little-endian fp16 scales;
    * 9*C/16 bytes per row of C elements. */
@@ -97,13 +98,14 @@ typedef struct moe_ffn_plan* moe_ffn_plan_t;
  * Validate `shapes` and `dtype`, build a plan and report the workspace size.
  * Host only: no device call, no launch, no device allocation.
  * Supported:
- *   1 <= T <= 256; 1 <= E <= 1024; 1 <= top_k <= min(E, 32); H, I, Is >= 1;
- *   bf16 weights: H, I, Is multiples of 8 (16-byte rows);
- *   4-bit weights: H, I, Is multiples of 256 (16-byte rows in the 4-bit
- *   layout) and T <= 8 (the grouped-GEMM regime is bf16 only);
- *   x fp32 or bf16.
- * Tokens T <= 8 take the decode path (router kernel + persistent expert
- * kernel); larger T take the tensor-core grouped-GEMM path.
+ *   decode path, 1 <= T <= 8: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
+ *     H <= 4096 and a multiple of 8 (bf16 weights) or of 256 (4-bit
+ *     weights), I, Is >= 1; x fp32 or bf16;
+ *   batched path, 9 <= T <= 1024 (routing, expert-sorted gather, grouped
+ *     GEMMs on the tcgen05 tensor cores, fixed-order combine): bf16 weights
+ *     and bf16 x, E <= 256, top_k <= 32, H a multiple of 256, I and Is
+ *     multiples of 128.
+ * moe_ffn_query(MOE_FFN_QUERY_PATH) reports the path taken.
  * Returns MOE_FFN_ERR_UNSUPPORTED otherwise, MOE_FFN_ERR_INVALID_ARG for null
  * pointers.  On success *plan is owned by the caller (moe_ffn_destroy).
  */
@@ -116,9 +118,12 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
  *   workspace     >= workspace_bytes from prepare, 256-byte aligned, scratch
  *   x             [T,H] fp32 or bf16 (plan dtype), row-major
  *   router_w      bf16 [E,H]
- *   expert_w      E consecutive blocks, block e = gate[I,H] | up[I,H] | down[H,I]
- *                 in the plan's weight format (each matrix row-major [out,in])
- *   shexp_w       gate[Is,H] | up[Is,H] | down[H,Is]
+ *   expert_w      E consecutive blocks, block e = gate[I,H] | up[I,H] | downT[I,H]
+ *                 in the plan's weight format, each matrix row-major with
+ *                 H-element rows: gate and up are [out,in]; downT is the down
+ *                 projection stored transposed (row i holds the weights from
+ *                 intermediate unit i to all H outputs)
+ *   shexp_w       gate[Is,H] | up[Is,H] | downT[Is,H]
  *   shexp_gate_w  bf16 [H]
  *   out           fp32 [T,H]; may alias x exactly (the layer reads all of x
  *                 before it writes out); any other overlap is undefined.
@@ -196,6 +201,22 @@ int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_str
 #define MOE_FFN_STATIC_SCRATCH_BYTES (1 << 24)
 int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream, const void* x, const void* router_w,
                                    const void* expert_w, const void* shexp_w, const void* shexp_gate_w, float* out);
+
+/*
+ * Test: the in-kernel failure path, without a fault.  Enqueues on `stream` one
+ * small kernel that waits, with the bounded waits the layer's kernels use, on
+ * a condition that nothing ever satisfies: which = 0 an mbarrier phase that
+ * never completes (the wait of a shared-memory copy that never lands), which
+ * = 1 a workspace counter that never reaches its target (the grid barrier
+ * before the combine).  The wait gives up after its iteration cap, records
+ * MOE_FFN_ERR_TIMEOUT in the workspace status word (read it with
+ * moe_ffn_read_status) and the kernel returns; the CUDA context stays usable
+ * and the next execute on the workspace clears the word.  Returns a host-side
+ * status (MOE_FFN_ERR_INVALID_ARG for a bad `which` or null pointers,
+ * MOE_FFN_ERR_WORKSPACE if workspace_bytes is below the plan's size).
+ */
+int moe_ffn_probe_timeout(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
+                          int32_t which);
 
 /* Queries on a plan. */
 typedef enum {
