@@ -17,7 +17,7 @@ cores, combine).  ``--config stack_q4`` runs the 48-layer 4-bit decode stack
 a step is one token through all 48 layers, and each token's output feeds the
 next token's input (128 sequential tokens by default).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4|batched_bf16|stack_q4] [--T T]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode_bf16|decode_q4|batched_bf16|batched_q4|stack_q4] [--T T]
 """
 
 from __future__ import annotations
@@ -63,12 +63,14 @@ def peaks():
 
 
 def workload(cfg: str, T: int):
-    wfmt = datagen.WFMT_Q4B32 if cfg == "decode_q4" else datagen.WFMT_BF16
+    wfmt = datagen.WFMT_Q4B32 if cfg in ("decode_q4", "batched_q4", "stack_q4") else datagen.WFMT_BF16
     shapes = datagen.Shapes(T=T, H=H, E=E, top_k=K_TOP, I=I, Is=IS)
     name = {
         "decode_bf16": f"decode bf16 MoE FFN layer: T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "decode_q4": f"decode 4-bit MoE FFN layer (blocks of 32, fp16 scale): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_bf16": f"batched bf16 MoE FFN layer (grouped GEMMs): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
+        "batched_q4": f"batched 4-bit MoE FFN layer (grouped GEMMs, fp16 operands): T={T}, H={H}, E={E}, top_k={K_TOP}, "
+                      f"I={I}, Is={IS}",
         "stack_q4": f"{STACK_LAYERS}-layer 4-bit decode stack (pre-norm RMSNorm + residual per layer, independent seeded "
                     f"layers), T=1, sequential tokens; layer H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
     }[cfg]
@@ -306,7 +308,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="default: 64000 decode, 2000 batched, 128 stack")
     ap.add_argument("--warmup", type=int, default=None, help="default: 1600 decode, 20 batched, 8 stack")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4", "batched_bf16", "stack_q4"])
+    ap.add_argument("--config", default="decode_bf16", choices=["decode_bf16", "decode_q4", "batched_bf16", "batched_q4", "stack_q4"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_LAYER_COPIES, help="layer copies rotated (profiling: fewer)")
@@ -475,7 +477,8 @@ def main():
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "traffic": NCU_TRAFFIC_BYTES.get(args.config),
                          "algorithmic_bytes_per_step": bytes_per_step,
-                         "kernel": ("k_gemm<0>, k_gemm<1> (+ routing, gather, combine); duration = step time"
+                         "kernel": (("k_gemm_q4<0>, k_gemm_q4<1>" if wfmt else "k_gemm<0>, k_gemm<1>")
+                                    + " (+ routing, gather, combine); duration = step time"
                                     if T > 8 else "k_rows (+ k_route, programmatic dependent launch); duration = step time")},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4,

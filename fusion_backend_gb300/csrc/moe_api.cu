@@ -158,13 +158,16 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
     B.x_perm = reinterpret_cast<uint16_t*>(w + L.x_perm);
     B.h_ws = reinterpret_cast<uint16_t*>(w + L.h_ws);
     B.hw = s.I > s.Is ? s.I : s.Is;
+    B.wfmt = plan->wfmt;
+    B.rb = plan->wfmt == MOE_FFN_W_Q4B32 ? (long long)s.H / 2 + s.H / 16 : 2LL * s.H;
     B.y_ws = reinterpret_cast<float*>(w + L.y_ws);
     B.r_counts = reinterpret_cast<int32_t*>(w + L.counts);
     B.r_offsets = reinterpret_cast<int32_t*>(w + L.offsets);
     B.r_perm = reinterpret_cast<int32_t*>(w + L.perm);
     B.r_active = reinterpret_cast<int32_t*>(w + L.active);
     B.r_nactive = reinterpret_cast<int32_t*>(w + L.nactive);
-    if (kGemmSmem0 + 8192 > dev->smem_optin || kGemmSmem1 + 8192 > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
+    const int smem0 = B.wfmt == 1 ? kQ4Smem0 : kGemmSmem0, smem1 = B.wfmt == 1 ? kQ4Smem1 : kGemmSmem1;
+    if (smem0 + 4608 > dev->smem_optin || smem1 + 4608 > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
     cudaError_t err = batch_tensor_maps(B);
     if (err != cudaSuccess) return cuda_status(err);
     return cuda_status(launch_batch(B, reinterpret_cast<cudaStream_t>(stream)));
@@ -212,9 +215,9 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
     if (s.H > kMaxH) return MOE_FFN_ERR_UNSUPPORTED;
     if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256)) return MOE_FFN_ERR_UNSUPPORTED;
   } else {
-    // Batched path (grouped GEMMs): bf16 weights and activation, E <= 256,
+    // Batched path (grouped GEMMs): bf16 or 4-bit weights, bf16 activation, E <= 256,
     // tiles of 256 columns of H and 128 rows of I and Is.
-    if (dtype.wfmt != MOE_FFN_W_BF16 || dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_UNSUPPORTED;
+    if (dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_UNSUPPORTED;
     if (s.E > kBatchMaxE || s.H % 256 || s.I % 128 || s.Is % 128) return MOE_FFN_ERR_UNSUPPORTED;
     if ((long long)s.E * 3 * s.I >= (1LL << 31) || 3LL * s.Is >= (1LL << 31)) return MOE_FFN_ERR_UNSUPPORTED;
   }
@@ -250,7 +253,7 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
     L.slot_w = off;
     off = align256(off + (TK + T) * 4);
     L.x_perm = off;
-    off = align256(off + TK * H * 2);
+    off = align256(off + (dtype.wfmt == MOE_FFN_W_Q4B32 ? TK + T : TK) * H * 2);
     L.h_ws = off;
     off = align256(off + (TK + T) * hw * 2);
     L.y_ws = off;

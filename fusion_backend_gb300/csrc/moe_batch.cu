@@ -8,6 +8,7 @@
 // e are rows offsets[e] .. offsets[e] + counts[e] - 1, its tokens ascending;
 // the shared expert's slot for token t is row T K + t.  Every output is a
 // pure function of the router's logits, so the layer is deterministic.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,12 +19,30 @@ namespace moe {
 
 cudaError_t launch_gemm_gate_up(const BatchParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_down(const BatchParams& p, cudaStream_t stream);
+cudaError_t launch_gemm_gate_up_q4(const BatchParams& p, cudaStream_t stream);
+cudaError_t launch_gemm_down_q4(const BatchParams& p, cudaStream_t stream);
 
 namespace {
 
 constexpr int kRouteTokens = 8;   // tokens per router block
 constexpr int kRouteRows = 4;     // router rows per block (1 per warp, 4 warps)
 constexpr int kGatherSplit = 4;   // blocks per expert in the bucketing kernel
+
+// Eight bf16 of x (elements 0..7) -> eight fp16 in the operand order of the
+// 4-bit GEMMs, e0 e4 e1 e5 e2 e6 e3 e7 (the order their dequantisation
+// gives the weights along K).
+__device__ __forceinline__ uint4 x8_f16_order(uint4 v) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = in[i >> 1], b = in[2 + (i >> 1)];  // (e 2(i/2), e 2(i/2)+1), (e 4+.., ..)
+    const float lo = (i & 1) ? bf16_hi(a) : bf16_lo(a), hi = (i & 1) ? bf16_hi(b) : bf16_lo(b);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // Router logits in two passes.  Pass 1 (this kernel): plain fp32 sums of
 // the exact bf16 x bf16 products, with a bound on their error from the sum of
@@ -232,6 +251,12 @@ __global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchPar
     }
     if (lane == 0) P.slot_w[(size_t)P.T * K + t] = 1.0f / (1.0f + expf(-s_ex[E]));
   }
+  if (P.wfmt == 1) {
+    // 4-bit weights: the shared slot's B row (x in fp16, operand order)
+    const uint4* src = reinterpret_cast<const uint4*>(P.x + (size_t)t * P.H);
+    uint4* dst = reinterpret_cast<uint4*>(P.x_perm + ((size_t)P.T * K + t) * P.H);
+    for (int q = tid; q < P.H / 8; q += 256) dst[q] = x8_f16_order(src[q]);
+  }
 }
 
 // Blocks (e, 0 .. kGatherSplit-1): the expert's count, offset (counts of the
@@ -303,8 +328,8 @@ __global__ void __launch_bounds__(256) k_bucket_b(const __grid_constant__ BatchP
   const int j0 = cnt * part / kGatherSplit, j1 = cnt * (part + 1) / kGatherSplit;
   for (int i = j0 * chunks + tid; i < j1 * chunks; i += 256) {
     const int j = i / chunks, q = i - j * chunks;
-    reinterpret_cast<uint4*>(P.x_perm + (size_t)(off + j) * P.H)[q] =
-        reinterpret_cast<const uint4*>(P.x + (size_t)s_tok[j] * P.H)[q];
+    const uint4 v = reinterpret_cast<const uint4*>(P.x + (size_t)s_tok[j] * P.H)[q];
+    reinterpret_cast<uint4*>(P.x_perm + (size_t)(off + j) * P.H)[q] = P.wfmt == 1 ? x8_f16_order(v) : v;
   }
 }
 
@@ -363,9 +388,9 @@ cudaError_t launch_batch(const BatchParams& p, cudaStream_t stream) {
   if (err == cudaSuccess) err = launch_pdl(k_topk_b, dim3(p.T), 256, 0, stream, p);
   if (err == cudaSuccess) err = launch_pdl(k_bucket_b, dim3(p.E, kGatherSplit), 256, 0, stream, p);
   if (err != cudaSuccess) return err;
-  err = launch_gemm_gate_up(p, stream);
+  err = p.wfmt == 1 ? launch_gemm_gate_up_q4(p, stream) : launch_gemm_gate_up(p, stream);
   if (err != cudaSuccess) return err;
-  err = launch_gemm_down(p, stream);
+  err = p.wfmt == 1 ? launch_gemm_down_q4(p, stream) : launch_gemm_down(p, stream);
   if (err != cudaSuccess) return err;
   return launch_pdl(k_combine_b, dim3(p.T), 256, 0, stream, p);
 }

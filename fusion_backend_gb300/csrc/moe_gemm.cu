@@ -31,72 +31,13 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_tc.cuh"
 
 namespace moe {
 
 namespace {
 
-// Shared-memory matrix descriptor (tcgen05): start address, leading and
-// stride byte offsets, descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A
-// MN-major if a_mn, B K-major, N and M.
-__device__ __forceinline__ uint32_t instr_desc(int m, int n, int a_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-// 32 lanes x 16 columns of 32 bits (this warp's lane quarter)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-// Barrier of the four epilogue warps (named barrier 1), and the same
-// barrier reducing a flag (true if it holds in every thread), so that the
-// four warps always leave their loop together.
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ bool epilogue_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ bool aborted(const int* f) { return *reinterpret_cast<const volatile int*>(f) != 0; }
-__device__ __forceinline__ void set_abort(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
+using namespace tc;
 
 // One unit of work.
 struct Unit {
@@ -437,12 +378,37 @@ bool encode_2d(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void*
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte view [rows][row_bytes] of stored 4-bit weight rows with a box of
+// bbytes x 64 rows: 128-byte swizzled (codes) or plain (scales).
+bool encode_q4(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, long long rows,
+               long long row_bytes, int bbytes, bool swizzle) {
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)bbytes, 64u};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t batch_tensor_maps(BatchParams& p) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = gemm_encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const long long er = (long long)p.E * 3 * p.I, sr = 3LL * p.Is, TK = (long long)p.T * p.K;
+  if (p.wfmt == 1) {
+    // 4-bit rows: codes and scales of the expert and shared blocks; B rows
+    // in fp16: x_perm (routed slots, then the shared slots T K + t) and h_ws
+    if (!encode_q4(fn, &p.tm_qn_e, p.expert_w, er, p.rb, 128, true) ||
+        !encode_q4(fn, &p.tm_qs_e, p.expert_w, er, p.rb, 16, false) ||
+        !encode_q4(fn, &p.tm_qn_s, p.shexp_w, sr, p.rb, 128, true) ||
+        !encode_q4(fn, &p.tm_qs_s, p.shexp_w, sr, p.rb, 16, false) ||
+        !encode_2d(fn, &p.tm_xp, p.x_perm, TK + p.T, p.H, 64, 16) ||
+        !encode_2d(fn, &p.tm_h, p.h_ws, TK + p.T, p.hw, 64, 16))
+      return cudaErrorInvalidValue;
+    return cudaSuccess;
+  }
   if (!encode_2d(fn, &p.tm_w64_e, p.expert_w, er, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_w64_s, p.shexp_w, sr, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_xp, p.x_perm, TK, p.H, 64, 16) || !encode_2d(fn, &p.tm_x, p.x, p.T, p.H, 64, 16) ||

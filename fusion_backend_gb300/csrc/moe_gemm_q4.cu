@@ -1,0 +1,497 @@
+// Grouped GEMMs of the batched MoE FFN layer for 4-bit weights (blocks of 32
+// along each stored row, one fp16 scale d per block, weight d (code - 8)),
+// on the tcgen05 tensor cores, sm_103a.  Same groups, units and epilogues as
+// the bf16 kernels (moe_gemm.cu); the weights reach the tensor cores through
+// eight dequantising warps, and the MMAs are kind::f16 with fp16 A and B (x
+// and h are carried in fp16 on this path).
+//
+// Each weight is fp16(d (code - 8)), rounded once: (0x6400 | code) is the
+// fp16 of 1024 + code, minus 1032 is code - 8 exactly, times d rounds once.
+// Eight codes of a 32-bit word give four half2 (e0,e4) (e1,e5) (e2,e6)
+// (e3,e7): in every group of eight the operands are stored in the order
+// e0 e4 e1 e5 e2 e6 e3 e7.  gate / up take that order along K, so x_perm
+// holds x in the same order (k_bucket_b); down takes it along M, so the
+// epilogue maps accumulator row P to output column 8 (P / 8) + (P % 8) / 2
+// + 4 (P % 2).
+//
+// gate / up (PHASE 0): one TMA transaction per raw stage (64 gate + 64 up
+// rows x 256 K of codes and scales, and the B rows); the dequant warps write
+// A straight into tensor memory (tcgen05.st, one row per lane), and the MMA
+// reads A from there (the .ts form) and B from the raw stage.
+// down (PHASE 1): the raw stage is 64 downT rows (K) x 256 columns (M) and
+// the B rows; A is M-contiguous, so the dequant warps write the fp16 tile
+// to shared memory in the MN-major 128-byte-swizzled layout and the MMA
+// reads both operands from shared memory.
+//
+// Block roles (14 warps): warp 0 lane 0 streams raw stages; warp 1 owns the
+// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise; warps
+// 10..13 are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4)
+// .. + 31.  Every wait is bounded; on a timeout the roles leave their loops
+// and the status word records it.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "moe_tc.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+struct UnitQ {
+  int shared, e, slot0, n, tile;
+};
+
+// Barrier of the eight dequant warps (named barrier 2), reducing a flag, so
+// that they leave their loop together (tcgen05.st is warp-collective).
+__device__ __forceinline__ bool dequant_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 2, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// D (tensor memory) += A (tensor memory, 128 lanes x 8 columns of fp16
+// pairs) x B (shared-memory descriptor)
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 columns of 32 bits into this warp's lane quarter
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Eight codes (element j in bits 4j..4j+3 of w) with the block scale pair dd
+// -> four half2 (e0,e4) (e1,e5) (e2,e6) (e3,e7) of fp16(d (code - 8)).
+__device__ __forceinline__ void dequant8(uint32_t w, __half2 dd, uint32_t* o) {
+  const __half2 k1032 = __half2half2(__ushort_as_half((unsigned short)0x6408u));  // 1032.0
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;  // 1024 + code, two at a time
+    const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&q), k1032);  // code - 8, exact
+    const __half2 r = __hmul2(c, dd);
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// fp16 scale of a raw stage (little-endian, 2-byte aligned) as a half2 pair
+__device__ __forceinline__ __half2 scale2(const uint8_t* p) {
+  return __half2half2(*reinterpret_cast<const __half*>(p));
+}
+
+}  // namespace
+
+template <int PHASE>
+__global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
+  constexpr int kRS = PHASE == 0 ? kQ4RawStages0 : kQ4RawStages1;
+  constexpr int kRB = PHASE == 0 ? kQ4Raw0 : kQ4Raw1;
+  constexpr int kBOff = PHASE == 0 ? kQ4BOff0 : kQ4BOff1;
+  constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared)
+  constexpr int kSubs = PHASE == 0 ? 4 : 1;                         // A stages per raw stage
+  constexpr uint32_t kCols = PHASE == 0 ? kQ4TmemCols0 : 2 * kGemmNC;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* tiles = sm;                                            // down: kTS x kQ4Tile1
+  uint8_t* raws = sm + (PHASE == 0 ? 0 : kTS * kQ4Tile1);         // kRS x kRB
+  float* exch = reinterpret_cast<float*>(raws + kRS * kRB);       // gate / up: [NC][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raws + kRS * kRB + (PHASE == 0 ? kGemmExch : 0));
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + kRS;
+  uint64_t* a_full = raw_empty + kRS;
+  uint64_t* a_empty = a_full + kTS;
+  uint64_t* acc_full = a_empty + kTS;
+  uint64_t* acc_empty = acc_full + 1;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_cum[kBatchMaxE + 2];
+  __shared__ int s_grp[kBatchMaxE + 1][3];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = P.T, K = P.K;
+  const int MT = PHASE == 0 ? P.I / 64 : P.H / 256;
+  const int MT_s = PHASE == 0 ? P.Is / 64 : P.H / 256;
+
+  pdl_launch_dependents();
+  if (tid == 64) {
+    for (int i = 0; i < kRS; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kQ4Dequant + 1);  // the dequant threads + the MMA commit (B is read there)
+    }
+    for (int i = 0; i < kTS; ++i) {
+      mbar_init(&a_full[i], kQ4Dequant);
+      mbar_init(&a_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_wait();
+  if (warp == 0) {
+    // groups (active experts ascending, then the shared expert) and the
+    // prefix sums of their units
+    const int U = *P.r_nactive;
+    int sum = 0;
+    int cnt[9];
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+      const int g = 9 * lane + q;
+      cnt[q] = 0;
+      if (g < U) {
+        const int e = P.r_active[g];
+        const int c = P.r_counts[e];
+        s_grp[g][0] = e;
+        s_grp[g][1] = P.r_offsets[e];
+        s_grp[g][2] = c;
+        cnt[q] = (c + kGemmNC - 1) / kGemmNC * MT;
+      } else if (g == U) {
+        s_grp[g][0] = -1;
+        s_grp[g][1] = T * K;
+        s_grp[g][2] = T;
+        cnt[q] = (T + kGemmNC - 1) / kGemmNC * MT_s;
+      }
+      sum += cnt[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+      const int g = 9 * lane + q;
+      if (g <= U + 1 && g < kBatchMaxE + 2) s_cum[g] = run;
+      run += cnt[q];
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int U = *P.r_nactive;
+  const int n_units = s_cum[U + 1];
+
+  int gscan = 0;
+  auto unit_of = [&](int u, UnitQ& w) {
+    while (gscan < U && s_cum[gscan + 1] <= u) ++gscan;
+    const int local = u - s_cum[gscan];
+    const int mt = s_grp[gscan][0] < 0 ? MT_s : MT;
+    const int chunk = local / mt;
+    w.tile = local - chunk * mt;
+    w.shared = s_grp[gscan][0] < 0;
+    w.e = w.shared ? 0 : s_grp[gscan][0];
+    w.slot0 = s_grp[gscan][1] + chunk * kGemmNC;  // shared slots: T K + token, in x_perm too
+    w.n = min(kGemmNC, s_grp[gscan][2] - chunk * kGemmNC);
+  };
+  // raw stages of a unit: gate / up K = H in chunks of 256; down K = I (Is) in chunks of 64
+  auto raw_chunks = [&](const UnitQ& w) { return PHASE == 0 ? P.H / 256 : (w.shared ? P.Is : P.I) / 64; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------- raw producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int rs = 0;
+      uint32_t ph = 0;
+      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+        UnitQ w;
+        unit_of(u, w);
+        const CUtensorMap* mn = w.shared ? &P.tm_qn_s : &P.tm_qn_e;
+        const CUtensorMap* ms = w.shared ? &P.tm_qs_s : &P.tm_qs_e;
+        const int I = w.shared ? P.Is : P.I;
+        const int npad = (w.n + 15) & ~15;
+        const int nrc = raw_chunks(w);
+        for (int rc = 0; rc < nrc; ++rc) {
+          if (!mbar_wait(&raw_empty[rs], ph ^ 1u)) {
+            set_abort(&s_abort);
+            break;
+          }
+          uint8_t* dst = raws + (size_t)rs * kRB;
+          mbar_arrive_expect_tx(&raw_full[rs], (uint32_t)(kBOff + kSubs * npad * 128));
+          if (PHASE == 0) {
+            const int rg = w.e * 3 * I + w.tile * 64;  // gate rows; the up rows follow I rows later
+            tma_load_2d(dst, mn, rc * 128, rg, &raw_full[rs], pol_w);
+            tma_load_2d(dst + 8192, mn, rc * 128, rg + I, &raw_full[rs], pol_w);
+            tma_load_2d(dst + 16384, ms, P.H / 2 + rc * 16, rg, &raw_full[rs], pol_w);
+            tma_load_2d(dst + 16384 + 1024, ms, P.H / 2 + rc * 16, rg + I, &raw_full[rs], pol_w);
+#pragma unroll
+            for (int sc = 0; sc < 4; ++sc)
+              for (int j = 0; j < npad; j += 16)
+                tma_load_2d(dst + kBOff + sc * (kGemmNC * 128) + j * 128, &P.tm_xp, (rc * 4 + sc) * 64, w.slot0 + j,
+                            &raw_full[rs], pol_x);
+          } else {
+            const int r = (w.e * 3 + 2) * I + rc * 64;  // downT rows (K); columns tile * 256 .. (M)
+            tma_load_2d(dst, mn, w.tile * 128, r, &raw_full[rs], pol_w);
+            tma_load_2d(dst + 8192, ms, P.H / 2 + w.tile * 16, r, &raw_full[rs], pol_w);
+            for (int j = 0; j < npad; j += 16)
+              tma_load_2d(dst + kBOff + j * 128, &P.tm_h, rc * 64, w.slot0 + j, &raw_full[rs], pol_x);
+          }
+          if (++rs == kRS) {
+            rs = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // wind down: every issued copy has landed before the block exits
+      for (int i = 0; i < kRS; ++i) mbar_wait(&raw_full[i], i < rs ? ph : ph ^ 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int rs = 0, ts = 0;
+      uint32_t rph = 0, tph = 0, acc_ph = 0;
+      bool pending = false;
+      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+        UnitQ w;
+        unit_of(u, w);
+        const int nrc = raw_chunks(w);
+        const int npad = (w.n + 15) & ~15;
+        const uint32_t idesc = instr_desc(128, npad, PHASE, true);
+        if (!mbar_wait(acc_empty, acc_ph ^ 1u)) {
+          set_abort(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int rc = 0; rc < nrc && ok; ++rc) {
+          ok = mbar_wait(&raw_full[rs], rph);
+          const uint32_t sb = smem_u32(raws + (size_t)rs * kRB + kBOff);
+          for (int sc = 0; sc < kSubs && ok; ++sc) {
+            ok = mbar_wait(&a_full[ts], tph);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bd = smem_desc(sb + sc * (kGemmNC * 128) + ks * 32, 16, 1024);
+              const uint32_t acc = (rc > 0 || sc > 0 || ks > 0) ? 1u : 0u;
+              if (PHASE == 0) {
+                umma_ts(tmem, tmem + (uint32_t)(kQ4ACol0 + 32 * ts + 8 * ks), bd, idesc, acc);
+              } else {
+                const uint32_t sa = smem_u32(tiles + (size_t)ts * kQ4Tile1);
+                umma(tmem, smem_desc(sa + ks * 2048, 8192, 1024), bd, idesc, acc);
+                umma(tmem + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bd, idesc, acc);
+              }
+            }
+            umma_commit(&a_empty[ts]);
+            pending = true;
+            if (++ts == kTS) {
+              ts = 0;
+              tph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&raw_empty[rs]);
+          if (++rs == kRS) {
+            rs = 0;
+            rph ^= 1u;
+          }
+        }
+        if (!ok) {
+          set_abort(&s_abort);
+          break;
+        }
+        umma_commit(acc_full);
+        pending = false;
+        acc_ph ^= 1u;
+      }
+      if (pending) {
+        // left with MMAs in flight: they complete before the block frees its tensor memory
+        umma_commit(acc_full);
+        mbar_wait(acc_full, acc_ph);
+      }
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ dequant
+    const int dt = tid - 64;  // 0 .. 255
+    int rs = 0, ts = 0;
+    uint32_t rph = 0, tph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      UnitQ w;
+      unit_of(u, w);
+      const int nrc = raw_chunks(w);
+      for (int rc = 0; rc < nrc && ok; ++rc) {
+        ok = dequant_all(mbar_wait(&raw_full[rs], rph) && !aborted(&s_abort));
+        if (!ok) break;
+        const uint8_t* raw = raws + (size_t)rs * kRB;
+        for (int sc = 0; sc < kSubs && ok; ++sc) {
+          ok = dequant_all(mbar_wait(&a_empty[ts], tph ^ 1u));
+          if (!ok) break;
+          if (PHASE == 0) {
+            // this thread: A row m (tensor-memory lane; 64 gate rows over 64
+            // up rows), K sub-chunk sc, half hf (32 K = one scale block)
+            const int q = warp & 3, hf = (warp - 2) >> 2;
+            const int m = 32 * q + lane, rr = m & 63;
+            const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
+            const int un = sc * 2 + hf;  // 16-byte unit of the row (before the swizzle)
+            const uint4 wq = *reinterpret_cast<const uint4*>(nib + ((un ^ (rr & 7)) << 4));
+            const __half2 dd = scale2(raw + 16384 + (m >> 6) * 1024 + rr * 16 + un * 2);
+            uint32_t v[16];
+            dequant8(wq.x, dd, v);
+            dequant8(wq.y, dd, v + 4);
+            dequant8(wq.z, dd, v + 8);
+            dequant8(wq.w, dd, v + 12);
+            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 32 * ts + 16 * hf), v);
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            // 64 rows (K) x 256 columns (M): items (row i, 8-column group uu);
+            // group uu goes to 64-column chunk uu / 8, 16-byte unit uu % 8 of
+            // row i (128-byte swizzle)
+            uint8_t* tile = tiles + (size_t)ts * kQ4Tile1;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
+              const uint32_t wq = *reinterpret_cast<const uint32_t*>(raw + i * 128 + (((uu >> 2) ^ (i & 7)) << 4) +
+                                                                     (uu & 3) * 4);
+              const __half2 dd = scale2(raw + 8192 + i * 16 + (uu >> 2) * 2);
+              uint32_t v[4];
+              dequant8(wq, dd, v);
+              *reinterpret_cast<uint4*>(tile + (uu >> 3) * 8192 + i * 128 + (((uu & 7) ^ (i & 7)) << 4)) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+            fence_async_smem();  // the tile's generic writes, visible to the tensor cores
+          }
+          mbar_arrive(&a_full[ts]);
+          if (++ts == kTS) {
+            ts = 0;
+            tph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
+        if (++rs == kRS) {
+          rs = 0;
+          rph ^= 1u;
+        }
+      }
+    }
+    if (!ok) set_abort(&s_abort);
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int m = 32 * q + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    uint16_t* h_ws = P.h_ws;
+    uint32_t acc_ph = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      UnitQ w;
+      unit_of(u, w);
+      const bool ok = mbar_wait(acc_full, acc_ph) && !aborted(&s_abort);
+      if (!epilogue_all(ok)) {
+        set_abort(&s_abort);
+        break;
+      }
+      tc_fence_after();
+      if (PHASE == 0) {
+        // lanes 0..63 gate, 64..127 up of the same rows tile * 64 ..
+        const int r = m & 63;
+        if (q < 2) {
+          for (int j0 = 0; j0 < w.n; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) exch[(j0 + jj) * 64 + r] = __uint_as_float(v[jj]);
+          }
+        }
+        epilogue_sync();
+        if (q >= 2) {
+          const int i = w.tile * 64 + r;
+          for (int j0 = 0; j0 < w.n; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = j0 + jj;
+              if (j < w.n) {
+                const int slot = w.slot0 + j;
+                const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
+                const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
+                h_ws[(size_t)slot * (size_t)P.hw + i] = __half_as_ushort(__float2half_rn(h));
+              }
+            }
+          }
+        }
+        epilogue_sync();
+      } else {
+        // accumulator row P = 128 half + m holds output column
+        // tile * 256 + 8 (P / 8) + (P % 8) / 2 + 4 (P % 2)
+        const int c0 = w.tile * 256 + 8 * (m >> 3) + ((m & 7) >> 1) + 4 * (m & 1);
+        for (int j0 = 0; j0 < w.n; j0 += 16) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tmem + lane_addr + (uint32_t)j0, r0);
+          tmem_ld16(tmem + lane_addr + (uint32_t)kGemmNC + (uint32_t)j0, r1);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = j0 + jj;
+            if (j < w.n) {
+              float* dst = P.y_ws + (size_t)(w.slot0 + j) * P.H + c0;
+              dst[0] = __uint_as_float(r0[jj]);
+              dst[128] = __uint_as_float(r1[jj]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_ph ^= 1u;
+    }
+  }
+  __syncthreads();
+  if (aborted(&s_abort) && tid == 0) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+}
+
+template <int PHASE>
+static cudaError_t launch_q4(const BatchParams& p, cudaStream_t stream) {
+  constexpr int smem = PHASE == 0 ? kQ4Smem0 : kQ4Smem1;
+  cudaError_t err = cudaFuncSetAttribute(k_gemm_q4<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kQ4Threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm_q4<PHASE>, p);
+}
+
+cudaError_t launch_gemm_gate_up_q4(const BatchParams& p, cudaStream_t stream) { return launch_q4<0>(p, stream); }
+cudaError_t launch_gemm_down_q4(const BatchParams& p, cudaStream_t stream) { return launch_q4<1>(p, stream); }
+
+}  // namespace moe

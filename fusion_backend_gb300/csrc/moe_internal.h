@@ -105,7 +105,7 @@ struct BatchParams {
   int tw;             // bitmap words per expert: ceil(T / 32)
   int32_t* slot_of;   // [T][K] slot (row of the expert-sorted order) of each choice
   float* slot_w;      // [T K + T] weight of each slot (routed p, then the shared gate per token)
-  uint16_t* x_perm;   // [T K][H] bf16, x of each routed slot
+  uint16_t* x_perm;   // [T K][H] bf16, x of each routed slot (4-bit weights: [T K + T][H] fp16)
   uint16_t* h_ws;     // [T K + T][hw] bf16, h of each slot (weight applied)
   int hw;             // h_ws row length: max(I, Is)
   float* y_ws;        // [T K + T][H] fp32, expert output of each slot
@@ -114,6 +114,15 @@ struct BatchParams {
   int32_t* r_perm;    // [T K] token-major choice index of each slot
   int32_t* r_active;  // [E] active experts ascending
   int32_t* r_nactive; // [1]
+  int wfmt;           // 0 bf16 weights, 1 4-bit blocks (then x_perm, h_ws hold fp16)
+  long long rb;       // bytes of one stored weight row (2H, or 9H/16)
+  // 4-bit weights: byte views [rows][rb] of the expert and shared blocks with
+  // boxes of 128 nibble bytes x 64 rows (128-byte swizzle) and 16 scale bytes
+  // x 64 rows
+  CUtensorMap tm_qn_e;
+  CUtensorMap tm_qs_e;
+  CUtensorMap tm_qn_s;
+  CUtensorMap tm_qs_s;
   // Tensor maps (bf16, 128-byte swizzle): weight rows of the expert blocks
   // and of the shared block with boxes of 64 x 64 (gate / up half tiles and
   // downT tiles), and the B operands: x_perm, x, h_ws rows with boxes of
@@ -139,6 +148,28 @@ constexpr int kGemmStages1 = 5, kGemmStageBytes1 = 2 * 128 * 128 + kGemmNC * 128
 constexpr int kGemmExch = 64 * kGemmNC * 4;  // gate / up epilogue: the gate half of the accumulator
 constexpr int kGemmSmem0 = kGemmStages0 * kGemmStageBytes0 + kGemmExch + 1024 + 256;
 constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;
+// 4-bit grouped GEMMs (moe_gemm_q4.cu).  A raw stage holds what one TMA
+// transaction brings: nibbles (128-byte swizzle), scales and the B rows.
+// gate / up: 64 gate + 64 up rows x 256 K (codes 2 x 8 KB, scales 2 x 1 KB)
+// and the B rows of four 64-wide K sub-chunks (4 x NC x 128 bytes); the
+// dequantised A goes to tensor memory (kQ4AStages0 stages of 64 K, 32
+// columns each, behind the 64-column accumulator).  down: 64 downT rows x
+// 256 columns (8 KB + 1 KB) and the B rows of the 64-wide K chunk; the
+// dequantised A (64 K x 256 M, fp16, MN-major) goes to shared tile stages.
+constexpr int kQ4Threads = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
+constexpr int kQ4Dequant = 256;  // dequant threads
+constexpr int kQ4BOff0 = 2 * 64 * 128 + 2 * 64 * 16;  // 18432: B rows of the gate / up raw stage
+constexpr int kQ4Raw0 = kQ4BOff0 + 4 * kGemmNC * 128, kQ4RawStages0 = 4;
+constexpr int kQ4AStages0 = 12, kQ4ACol0 = 128, kQ4TmemCols0 = 512;
+constexpr int kQ4BOff1 = 64 * 128 + 64 * 16;  // 9216
+constexpr int kQ4Raw1 = kQ4BOff1 + kGemmNC * 128, kQ4RawStages1 = 7;
+constexpr int kQ4Tile1 = 64 * 256 * 2, kQ4TileStages1 = 3;
+constexpr int kQ4Smem0 = kQ4RawStages0 * kQ4Raw0 + kGemmExch + 1024 + 512;
+constexpr int kQ4Smem1 = kQ4TileStages1 * kQ4Tile1 + kQ4RawStages1 * kQ4Raw1 + 1024 + 512;
+static_assert(kQ4ACol0 + 32 * kQ4AStages0 <= kQ4TmemCols0, "tensor memory of the gate / up kernel");
+static_assert(kQ4Smem0 <= 232448 && kQ4Smem1 <= 232448, "shared memory of the 4-bit GEMMs");
+static_assert(kQ4BOff0 % 1024 == 0 && kQ4Raw0 % 1024 == 0 && kQ4BOff1 % 1024 == 0 && kQ4Raw1 % 1024 == 0,
+              "swizzled stage alignment");
 
 // Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
 // Launched behind the previous kernel of the stream with programmatic

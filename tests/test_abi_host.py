@@ -51,7 +51,7 @@ def test_prepare_reports_workspace_without_device(lib):
         (datagen.Shapes(1, 256, 2000, 2, 128, 256), fb.W_BF16),   # E > 1024
         (datagen.Shapes(1, 264, 8, 2, 128, 256), fb.W_Q4B32),     # 4-bit rows need H a multiple of 256
         (datagen.Shapes(1, 8192, 8, 2, 128, 256), fb.W_BF16),     # H > 4096 (decode path bound)
-        (datagen.Shapes(9, 256, 8, 2, 128, 256), fb.W_Q4B32),     # T > 8: the grouped GEMMs take bf16 weights
+        (datagen.Shapes(9, 256, 8, 2, 192, 256), fb.W_Q4B32),     # T > 8, 4-bit: I a multiple of 128
         (datagen.Shapes(1025, 256, 8, 2, 128, 256), fb.W_BF16),   # T > 1024
         (datagen.Shapes(64, 128, 8, 2, 128, 256), fb.W_BF16),     # T > 8: H a multiple of 256
         (datagen.Shapes(64, 256, 8, 2, 192, 256), fb.W_BF16),     # T > 8: I a multiple of 128
@@ -78,6 +78,17 @@ def test_prepare_batched_plan_and_workspace(lib):
     TK = s.T * s.top_k
     # at least x by slot (bf16), h by slot (bf16) and y by slot (fp32)
     assert ws >= TK * s.H * 2 + (TK + s.T) * s.I * 2 + (TK + s.T) * s.H * 4
+    fb.moe_ffn_destroy(plan)
+
+
+def test_prepare_batched_q4_plan_and_workspace(lib):
+    s = datagen.Shapes(64, 2048, 128, 8, 768, 512)
+    plan, ws = fb.moe_ffn_prepare(s, fb.ACT_BF16, fb.W_Q4B32)
+    assert fb.moe_ffn_query(plan, fb.QUERY_PATH) == 1
+    assert fb.moe_ffn_query(plan, fb.QUERY_LAUNCHES_PER_EXECUTE) == 6
+    TK = s.T * s.top_k
+    # x by slot incl. the shared slots (fp16), h by slot (fp16), y by slot (fp32)
+    assert ws >= (TK + s.T) * s.H * 2 + (TK + s.T) * s.I * 2 + (TK + s.T) * s.H * 4
     fb.moe_ffn_destroy(plan)
 
 

@@ -17,7 +17,7 @@ import pytest
 
 import datagen
 import oracle
-from datagen import ACT_BF16, WFMT_BF16, Shapes
+from datagen import ACT_BF16, WFMT_BF16, WFMT_Q4B32, Shapes
 from tests.cases import DECODE, draw_tokens, with_T, x_as_f64
 
 pytestmark = pytest.mark.gpu
@@ -25,20 +25,20 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def _layer(seed, shapes):
-    return datagen.make_layer(seed, Shapes(1, shapes.H, shapes.E, shapes.top_k, shapes.I, shapes.Is), WFMT_BF16)
+def _layer(seed, shapes, wfmt=WFMT_BF16):
+    return datagen.make_layer(seed, Shapes(1, shapes.H, shapes.E, shapes.top_k, shapes.I, shapes.Is), wfmt)
 
 
-@pytest.mark.parametrize(
-    "shapes",
-    [
+SMALL = [
         Shapes(T=9, H=256, E=8, top_k=2, I=128, Is=128),      # the smallest batch
         Shapes(T=40, H=512, E=16, top_k=4, I=256, Is=128),    # several row / column tiles, ragged groups
         Shapes(T=300, H=256, E=4, top_k=2, I=128, Is=256),    # groups and the shared expert past 128 slots
         Shapes(T=64, H=768, E=32, top_k=8, I=384, Is=256),    # three column-tile pairs, three row tiles
         Shapes(T=33, H=256, E=64, top_k=1, I=128, Is=128),    # top-1, most experts idle
-    ],
-)
+]
+
+
+@pytest.mark.parametrize("shapes", SMALL)
 def test_batched_small(shapes):
     from tests.test_gpu_parity import check_case
 
@@ -47,11 +47,22 @@ def test_batched_small(shapes):
     check_case(layer, x, ACT_BF16, str(shapes))
 
 
-def test_batched_repeat_bitwise():
+@pytest.mark.parametrize("shapes", SMALL)
+def test_batched_small_q4(shapes):
+    """4-bit block weights on the grouped GEMMs (fp16 operands)."""
+    from tests.test_gpu_parity import check_case
+
+    layer = _layer(4011, shapes, WFMT_Q4B32)
+    x, _ = draw_tokens(4011, layer, shapes.T, ACT_BF16)
+    check_case(layer, x, ACT_BF16, "q4 " + str(shapes))
+
+
+@pytest.mark.parametrize("wfmt", [WFMT_BF16, WFMT_Q4B32])
+def test_batched_repeat_bitwise(wfmt):
     from tests.devlayer import DevLayer
 
     shapes = Shapes(T=40, H=512, E=16, top_k=4, I=256, Is=128)
-    layer = _layer(4002, shapes)
+    layer = _layer(4002, shapes, wfmt)
     x, _ = draw_tokens(4002, layer, shapes.T, ACT_BF16)
     dl = DevLayer(layer)
     a = dl.run(x, ACT_BF16)
@@ -61,9 +72,9 @@ def test_batched_repeat_bitwise():
     assert a["ids"].tobytes() == b["ids"].tobytes()
 
 
-@pytest.fixture(scope="module")
-def full_layer():
-    return datagen.make_layer(2024, DECODE, WFMT_BF16)
+@pytest.fixture(scope="module", params=[WFMT_BF16, WFMT_Q4B32], ids=["bf16", "q4"])
+def full_layer(request):
+    return datagen.make_layer(2024, DECODE, request.param)
 
 
 @pytest.mark.parametrize("T", [64, 256])
@@ -88,7 +99,7 @@ def test_batched_full_size_sampled(full_layer, T):
     np.testing.assert_array_equal(g_active, active)
     # outputs of a sample of tokens
     idx = np.array(sorted({0, 1, T // 3, T // 2, T - 2, T - 1}))
-    ref = oracle.moe_ffn(with_T(DECODE, idx.size), ACT_BF16, WFMT_BF16, x[idx], full_layer.router_w,
+    ref = oracle.moe_ffn(with_T(DECODE, idx.size), ACT_BF16, full_layer.wfmt, x[idx], full_layer.router_w,
                          full_layer.expert_w, full_layer.shexp_w, full_layer.shexp_gate_w)
     np.testing.assert_array_equal(got["ids"][idx], ref["ids"])
     ok, err, rms = tolerance_ok(got["out"][idx], ref["out"])
