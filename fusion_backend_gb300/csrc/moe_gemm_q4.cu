@@ -24,10 +24,11 @@
 // reads both operands from shared memory.
 //
 // Block roles (14 warps): warp 0 lane 0 streams raw stages; warp 1 owns the
-// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise; warps
-// 10..13 are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4)
-// .. + 31.  Every wait is bounded; on a timeout the roles leave their loops
-// and the status word records it.
+// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise, each
+// on its own (a whole raw stage between two synchronisations); warps 10..13
+// are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4) .. + 31.
+// Every wait is bounded; on a timeout the roles leave their loops and the
+// status word records it.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -47,17 +48,6 @@ struct UnitQ {
   int shared, e, slot0, n, tile;
 };
 
-// Barrier of the eight dequant warps (named barrier 2), reducing a flag, so
-// that they leave their loop together (tcgen05.st is warp-collective).
-__device__ __forceinline__ bool dequant_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 2, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // D (tensor memory) += A (tensor memory, 128 lanes x 8 columns of fp16
@@ -106,22 +96,27 @@ template <int PHASE>
 __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
   constexpr int kRS = PHASE == 0 ? kQ4RawStages0 : kQ4RawStages1;
   constexpr int kRB = PHASE == 0 ? kQ4Raw0 : kQ4Raw1;
-  constexpr int kBOff = PHASE == 0 ? kQ4BOff0 : kQ4BOff1;
-  constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared)
-  constexpr int kSubs = PHASE == 0 ? 4 : 1;                         // A stages per raw stage
-  constexpr uint32_t kCols = PHASE == 0 ? kQ4TmemCols0 : 2 * kGemmNC;
+  constexpr int kBS = PHASE == 0 ? kQ4BStages0 : kQ4BStages1;
+  constexpr int kBB = PHASE == 0 ? kQ4B0 : kQ4B1;
+  constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared), one per raw stage
+  constexpr int kSubs = PHASE == 0 ? 4 : 1;                         // 64-wide K sub-chunks of B per raw stage
+  constexpr uint32_t kCols = PHASE == 0 ? kQ4TmemCols0 : kQ4TmemCols1;
+  constexpr uint32_t kAccCols = PHASE == 0 ? kGemmNC : 2 * kGemmNC;  // one accumulator (two buffers)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* tiles = sm;                                            // down: kTS x kQ4Tile1
-  uint8_t* raws = sm + (PHASE == 0 ? 0 : kTS * kQ4Tile1);         // kRS x kRB
-  float* exch = reinterpret_cast<float*>(raws + kRS * kRB);       // gate / up: [NC][64]
+  uint8_t* tiles = sm;                                             // down: kTS x kQ4Tile1
+  uint8_t* bst = sm + (PHASE == 0 ? 0 : kTS * kQ4Tile1);           // kBS x kBB
+  uint8_t* raws = bst + kBS * kBB;                                 // kRS x kRB
+  float* exch = reinterpret_cast<float*>(raws + kRS * kRB);        // gate / up: [NC][64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(raws + kRS * kRB + (PHASE == 0 ? kGemmExch : 0));
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kRS;
-  uint64_t* a_full = raw_empty + kRS;
+  uint64_t* b_full = raw_empty + kRS;
+  uint64_t* b_empty = b_full + kBS;
+  uint64_t* a_full = b_empty + kBS;
   uint64_t* a_empty = a_full + kTS;
-  uint64_t* acc_full = a_empty + kTS;
-  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* acc_full = a_empty + kTS;  // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_cum[kBatchMaxE + 2];
@@ -136,14 +131,20 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
   if (tid == 64) {
     for (int i = 0; i < kRS; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], kQ4Dequant + 1);  // the dequant threads + the MMA commit (B is read there)
+      mbar_init(&raw_empty[i], kQ4Dequant);
+    }
+    for (int i = 0; i < kBS; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < kTS; ++i) {
       mbar_init(&a_full[i], kQ4Dequant);
       mbar_init(&a_empty[i], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
     s_abort = 0;
     mbar_fence_init();
   }
@@ -215,13 +216,16 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
   auto raw_chunks = [&](const UnitQ& w) { return PHASE == 0 ? P.H / 256 : (w.shared ? P.Is : P.I) / 64; };
 
   if (warp == 0) {
-    // ------------------------------------------------------- raw producer
+    // ------------------------------------------------------------ producer
+    // per K chunk: the raw stage (weights), then the B stage (slot rows);
+    // the B ring is shallower, the raw ring runs ahead of it
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      int rs = 0;
-      uint32_t ph = 0;
-      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+      int rs = 0, bs = 0;
+      uint32_t rph = 0, bph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok && !aborted(&s_abort); u += gridDim.x) {
         UnitQ w;
         unit_of(u, w);
         const CUtensorMap* mn = w.shared ? &P.tm_qn_s : &P.tm_qn_e;
@@ -230,106 +234,128 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         const int npad = (w.n + 15) & ~15;
         const int nrc = raw_chunks(w);
         for (int rc = 0; rc < nrc; ++rc) {
-          if (!mbar_wait(&raw_empty[rs], ph ^ 1u)) {
-            set_abort(&s_abort);
+          if (!mbar_wait(&raw_empty[rs], rph ^ 1u)) {
+            ok = false;
             break;
           }
           uint8_t* dst = raws + (size_t)rs * kRB;
-          mbar_arrive_expect_tx(&raw_full[rs], (uint32_t)(kBOff + kSubs * npad * 128));
+          mbar_arrive_expect_tx(&raw_full[rs], (uint32_t)kRB);
           if (PHASE == 0) {
             const int rg = w.e * 3 * I + w.tile * 64;  // gate rows; the up rows follow I rows later
             tma_load_2d(dst, mn, rc * 128, rg, &raw_full[rs], pol_w);
             tma_load_2d(dst + 8192, mn, rc * 128, rg + I, &raw_full[rs], pol_w);
             tma_load_2d(dst + 16384, ms, P.H / 2 + rc * 16, rg, &raw_full[rs], pol_w);
             tma_load_2d(dst + 16384 + 1024, ms, P.H / 2 + rc * 16, rg + I, &raw_full[rs], pol_w);
-#pragma unroll
-            for (int sc = 0; sc < 4; ++sc)
-              for (int j = 0; j < npad; j += 16)
-                tma_load_2d(dst + kBOff + sc * (kGemmNC * 128) + j * 128, &P.tm_xp, (rc * 4 + sc) * 64, w.slot0 + j,
-                            &raw_full[rs], pol_x);
           } else {
             const int r = (w.e * 3 + 2) * I + rc * 64;  // downT rows (K); columns tile * 256 .. (M)
             tma_load_2d(dst, mn, w.tile * 128, r, &raw_full[rs], pol_w);
             tma_load_2d(dst + 8192, ms, P.H / 2 + w.tile * 16, r, &raw_full[rs], pol_w);
-            for (int j = 0; j < npad; j += 16)
-              tma_load_2d(dst + kBOff + j * 128, &P.tm_h, rc * 64, w.slot0 + j, &raw_full[rs], pol_x);
           }
           if (++rs == kRS) {
             rs = 0;
-            ph ^= 1u;
+            rph ^= 1u;
+          }
+          if (!mbar_wait(&b_empty[bs], bph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          uint8_t* bd = bst + (size_t)bs * kBB;
+          mbar_arrive_expect_tx(&b_full[bs], (uint32_t)(kSubs * npad * 128));
+          if (PHASE == 0) {
+#pragma unroll
+            for (int sc = 0; sc < 4; ++sc)
+              for (int j = 0; j < npad; j += 16)
+                tma_load_2d(bd + sc * (kGemmNC * 128) + j * 128, &P.tm_xp, (rc * 4 + sc) * 64, w.slot0 + j,
+                            &b_full[bs], pol_x);
+          } else {
+            for (int j = 0; j < npad; j += 16)
+              tma_load_2d(bd + j * 128, &P.tm_h, rc * 64, w.slot0 + j, &b_full[bs], pol_x);
+          }
+          if (++bs == kBS) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
       }
+      if (!ok) set_abort(&s_abort);
       // wind down: every issued copy has landed before the block exits
-      for (int i = 0; i < kRS; ++i) mbar_wait(&raw_full[i], i < rs ? ph : ph ^ 1u);
+      for (int i = 0; i < kRS; ++i) mbar_wait(&raw_full[i], i < rs ? rph : rph ^ 1u);
+      for (int i = 0; i < kBS; ++i) mbar_wait(&b_full[i], i < bs ? bph : bph ^ 1u);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int rs = 0, ts = 0;
-      uint32_t rph = 0, tph = 0, acc_ph = 0;
+      int bs = 0, ts = 0, nu = 0;
+      uint32_t bph = 0, tph = 0;
       bool pending = false;
-      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x) {
+      for (int u = blockIdx.x; u < n_units && !aborted(&s_abort); u += gridDim.x, ++nu) {
         UnitQ w;
         unit_of(u, w);
         const int nrc = raw_chunks(w);
         const int npad = (w.n + 15) & ~15;
         const uint32_t idesc = instr_desc(128, npad, PHASE, true);
-        if (!mbar_wait(acc_empty, acc_ph ^ 1u)) {
+        const int ab = nu & 1;
+        const uint32_t acc_ph = (uint32_t)(nu >> 1) & 1u;
+        const uint32_t dacc = tmem + (uint32_t)ab * kAccCols;
+        if (!mbar_wait(&acc_empty[ab], acc_ph ^ 1u)) {
           set_abort(&s_abort);
           break;
         }
         tc_fence_after();
         bool ok = true;
-        for (int rc = 0; rc < nrc && ok; ++rc) {
-          ok = mbar_wait(&raw_full[rs], rph);
-          const uint32_t sb = smem_u32(raws + (size_t)rs * kRB + kBOff);
-          for (int sc = 0; sc < kSubs && ok; ++sc) {
-            ok = mbar_wait(&a_full[ts], tph);
-            if (!ok) break;
-            tc_fence_after();
+        for (int rc = 0; rc < nrc; ++rc) {
+          ok = mbar_wait(&b_full[bs], bph) && mbar_wait(&a_full[ts], tph);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sb = smem_u32(bst + (size_t)bs * kBB);
+          if (PHASE == 0) {
+            // 256 K: A columns kQ4ACol0 + 128 ts + 8 ks, B sub-chunk ks / 4
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {
+              const uint64_t bdsc = smem_desc(sb + (ks >> 2) * (kGemmNC * 128) + (ks & 3) * 32, 16, 1024);
+              umma_ts(dacc, tmem + (uint32_t)(kQ4ACol0 + 128 * ts + 8 * ks), bdsc, idesc,
+                      (rc > 0 || ks > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t sa = smem_u32(tiles + (size_t)ts * kQ4Tile1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t bd = smem_desc(sb + sc * (kGemmNC * 128) + ks * 32, 16, 1024);
-              const uint32_t acc = (rc > 0 || sc > 0 || ks > 0) ? 1u : 0u;
-              if (PHASE == 0) {
-                umma_ts(tmem, tmem + (uint32_t)(kQ4ACol0 + 32 * ts + 8 * ks), bd, idesc, acc);
-              } else {
-                const uint32_t sa = smem_u32(tiles + (size_t)ts * kQ4Tile1);
-                umma(tmem, smem_desc(sa + ks * 2048, 8192, 1024), bd, idesc, acc);
-                umma(tmem + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bd, idesc, acc);
-              }
-            }
-            umma_commit(&a_empty[ts]);
-            pending = true;
-            if (++ts == kTS) {
-              ts = 0;
-              tph ^= 1u;
+              const uint64_t bdsc = smem_desc(sb + ks * 32, 16, 1024);
+              const uint32_t acc = (rc > 0 || ks > 0) ? 1u : 0u;
+              umma(dacc, smem_desc(sa + ks * 2048, 8192, 1024), bdsc, idesc, acc);
+              umma(dacc + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bdsc, idesc, acc);
             }
           }
-          if (!ok) break;
-          umma_commit(&raw_empty[rs]);
-          if (++rs == kRS) {
-            rs = 0;
-            rph ^= 1u;
+          umma_commit(&a_empty[ts]);
+          umma_commit(&b_empty[bs]);
+          pending = true;
+          if (++ts == kTS) {
+            ts = 0;
+            tph ^= 1u;
+          }
+          if (++bs == kBS) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
         if (!ok) {
           set_abort(&s_abort);
+          // left with MMAs in flight: they complete before the block frees its tensor memory
+          if (pending) {
+            umma_commit(&acc_full[ab]);
+            mbar_wait(&acc_full[ab], acc_ph);
+          }
+          pending = false;
           break;
         }
-        umma_commit(acc_full);
+        umma_commit(&acc_full[ab]);
         pending = false;
-        acc_ph ^= 1u;
-      }
-      if (pending) {
-        // left with MMAs in flight: they complete before the block frees its tensor memory
-        umma_commit(acc_full);
-        mbar_wait(acc_full, acc_ph);
       }
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ dequant
+    // Each warp runs on its own: the waits are per thread, the exit test
+    // warp-uniform (tcgen05.st is warp-collective).
     const int dt = tid - 64;  // 0 .. 255
     int rs = 0, ts = 0;
     uint32_t rph = 0, tph = 0;
@@ -338,56 +364,69 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       UnitQ w;
       unit_of(u, w);
       const int nrc = raw_chunks(w);
-      for (int rc = 0; rc < nrc && ok; ++rc) {
-        ok = dequant_all(mbar_wait(&raw_full[rs], rph) && !aborted(&s_abort));
+      for (int rc = 0; rc < nrc; ++rc) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[rs], rph) && mbar_wait(&a_empty[ts], tph ^ 1u) &&
+                                         !aborted(&s_abort));
         if (!ok) break;
         const uint8_t* raw = raws + (size_t)rs * kRB;
-        for (int sc = 0; sc < kSubs && ok; ++sc) {
-          ok = dequant_all(mbar_wait(&a_empty[ts], tph ^ 1u));
-          if (!ok) break;
-          if (PHASE == 0) {
-            // this thread: A row m (tensor-memory lane; 64 gate rows over 64
-            // up rows), K sub-chunk sc, half hf (32 K = one scale block)
-            const int q = warp & 3, hf = (warp - 2) >> 2;
-            const int m = 32 * q + lane, rr = m & 63;
-            const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
-            const int un = sc * 2 + hf;  // 16-byte unit of the row (before the swizzle)
-            const uint4 wq = *reinterpret_cast<const uint4*>(nib + ((un ^ (rr & 7)) << 4));
-            const __half2 dd = scale2(raw + 16384 + (m >> 6) * 1024 + rr * 16 + un * 2);
-            uint32_t v[16];
-            dequant8(wq.x, dd, v);
-            dequant8(wq.y, dd, v + 4);
-            dequant8(wq.z, dd, v + 8);
-            dequant8(wq.w, dd, v + 12);
-            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 32 * ts + 16 * hf), v);
-            tmem_wait_st();
-            tc_fence_before();
-          } else {
-            // 64 rows (K) x 256 columns (M): items (row i, 8-column group uu);
-            // group uu goes to 64-column chunk uu / 8, 16-byte unit uu % 8 of
-            // row i (128-byte swizzle)
-            uint8_t* tile = tiles + (size_t)ts * kQ4Tile1;
+        if (PHASE == 0) {
+          // this thread: A row m (tensor-memory lane; 64 gate rows over 64
+          // up rows), K half hf of the stage (128 K: 16-byte units 4 hf ..
+          // 4 hf + 3 of the row, one scale block each)
+          const int q = warp & 3, hf = (warp - 2) >> 2;
+          const int m = 32 * q + lane, rr = m & 63;
+          const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
+          const uint8_t* scl = raw + 16384 + (m >> 6) * 1024 + rr * 16;
+          uint4 wq[4];
+          __half2 dd[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
-              const uint32_t wq = *reinterpret_cast<const uint32_t*>(raw + i * 128 + (((uu >> 2) ^ (i & 7)) << 4) +
-                                                                     (uu & 3) * 4);
-              const __half2 dd = scale2(raw + 8192 + i * 16 + (uu >> 2) * 2);
-              uint32_t v[4];
-              dequant8(wq, dd, v);
-              *reinterpret_cast<uint4*>(tile + (uu >> 3) * 8192 + i * 128 + (((uu & 7) ^ (i & 7)) << 4)) =
-                  make_uint4(v[0], v[1], v[2], v[3]);
-            }
-            fence_async_smem();  // the tile's generic writes, visible to the tensor cores
+          for (int j = 0; j < 4; ++j) {
+            const int un = 4 * hf + j;
+            wq[j] = *reinterpret_cast<const uint4*>(nib + ((un ^ (rr & 7)) << 4));
+            dd[j] = scale2(scl + un * 2);
           }
-          mbar_arrive(&a_full[ts]);
-          if (++ts == kTS) {
-            ts = 0;
-            tph ^= 1u;
+          mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
+          const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 128 * ts + 64 * hf);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t v[16];
+            dequant8(wq[j].x, dd[j], v);
+            dequant8(wq[j].y, dd[j], v + 4);
+            dequant8(wq[j].z, dd[j], v + 8);
+            dequant8(wq[j].w, dd[j], v + 12);
+            tmem_st16(ta + 16 * j, v);
           }
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          // 64 rows (K) x 256 columns (M): items (row i, 8-column group uu);
+          // group uu goes to 64-column chunk uu / 8, 16-byte unit uu % 8 of
+          // row i (128-byte swizzle)
+          uint8_t* tile = tiles + (size_t)ts * kQ4Tile1;
+          uint32_t wq[8];
+          __half2 dd[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
+            wq[j] = *reinterpret_cast<const uint32_t*>(raw + i * 128 + (((uu >> 2) ^ (i & 7)) << 4) + (uu & 3) * 4);
+            dd[j] = scale2(raw + 8192 + i * 16 + (uu >> 2) * 2);
+          }
+          mbar_arrive(&raw_empty[rs]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
+            uint32_t v[4];
+            dequant8(wq[j], dd[j], v);
+            *reinterpret_cast<uint4*>(tile + (uu >> 3) * 8192 + i * 128 + (((uu & 7) ^ (i & 7)) << 4)) =
+                make_uint4(v[0], v[1], v[2], v[3]);
+          }
+          fence_async_smem();  // the tile's generic writes, visible to the tensor cores
         }
-        if (!ok) break;
-        mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
+        mbar_arrive(&a_full[ts]);
+        if (++ts == kTS) {
+          ts = 0;
+          tph ^= 1u;
+        }
         if (++rs == kRS) {
           rs = 0;
           rph ^= 1u;
@@ -401,11 +440,13 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
     const int m = 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     uint16_t* h_ws = P.h_ws;
-    uint32_t acc_ph = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    int nu = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nu) {
       UnitQ w;
       unit_of(u, w);
-      const bool ok = mbar_wait(acc_full, acc_ph) && !aborted(&s_abort);
+      const int ab = nu & 1;
+      const uint32_t acc = tmem + lane_addr + (uint32_t)ab * kAccCols;
+      const bool ok = mbar_wait(&acc_full[ab], (uint32_t)(nu >> 1) & 1u) && !aborted(&s_abort);
       if (!epilogue_all(ok)) {
         set_abort(&s_abort);
         break;
@@ -417,7 +458,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         if (q < 2) {
           for (int j0 = 0; j0 < w.n; j0 += 16) {
             uint32_t v[16];
-            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
+            tmem_ld16(acc + (uint32_t)j0, v);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) exch[(j0 + jj) * 64 + r] = __uint_as_float(v[jj]);
           }
@@ -427,7 +468,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
           const int i = w.tile * 64 + r;
           for (int j0 = 0; j0 < w.n; j0 += 16) {
             uint32_t v[16];
-            tmem_ld16(tmem + lane_addr + (uint32_t)j0, v);
+            tmem_ld16(acc + (uint32_t)j0, v);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int j = j0 + jj;
@@ -440,6 +481,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
             }
           }
         }
+        tc_fence_before();
         epilogue_sync();
       } else {
         // accumulator row P = 128 half + m holds output column
@@ -447,8 +489,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         const int c0 = w.tile * 256 + 8 * (m >> 3) + ((m & 7) >> 1) + 4 * (m & 1);
         for (int j0 = 0; j0 < w.n; j0 += 16) {
           uint32_t r0[16], r1[16];
-          tmem_ld16(tmem + lane_addr + (uint32_t)j0, r0);
-          tmem_ld16(tmem + lane_addr + (uint32_t)kGemmNC + (uint32_t)j0, r1);
+          tmem_ld16(acc + (uint32_t)j0, r0);
+          tmem_ld16(acc + (uint32_t)kGemmNC + (uint32_t)j0, r1);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
@@ -459,10 +501,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
             }
           }
         }
+        tc_fence_before();
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_ph ^= 1u;
+      mbar_arrive(&acc_empty[ab]);
     }
   }
   __syncthreads();

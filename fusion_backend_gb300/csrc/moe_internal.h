@@ -148,27 +148,28 @@ constexpr int kGemmStages1 = 5, kGemmStageBytes1 = 2 * 128 * 128 + kGemmNC * 128
 constexpr int kGemmExch = 64 * kGemmNC * 4;  // gate / up epilogue: the gate half of the accumulator
 constexpr int kGemmSmem0 = kGemmStages0 * kGemmStageBytes0 + kGemmExch + 1024 + 256;
 constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;
-// 4-bit grouped GEMMs (moe_gemm_q4.cu).  A raw stage holds what one TMA
-// transaction brings: nibbles (128-byte swizzle), scales and the B rows.
-// gate / up: 64 gate + 64 up rows x 256 K (codes 2 x 8 KB, scales 2 x 1 KB)
-// and the B rows of four 64-wide K sub-chunks (4 x NC x 128 bytes); the
-// dequantised A goes to tensor memory (kQ4AStages0 stages of 64 K, 32
-// columns each, behind the 64-column accumulator).  down: 64 downT rows x
-// 256 columns (8 KB + 1 KB) and the B rows of the 64-wide K chunk; the
-// dequantised A (64 K x 256 M, fp16, MN-major) goes to shared tile stages.
+// 4-bit grouped GEMMs (moe_gemm_q4.cu).  Three rings: raw stages (codes
+// with the 128-byte swizzle + scales, from TMA), B stages (the slots' fp16
+// rows, from TMA) and A stages (dequantised weights).
+// gate / up: raw stage = 64 gate + 64 up rows x 256 K (codes 2 x 8 KB,
+// scales 2 x 1 KB); B stage = four 64-wide K sub-chunks (4 x NC x 128
+// bytes); A stages in tensor memory (256 K, 128 columns each) behind two
+// 64-column accumulators.  down: raw stage = 64 downT rows x 256 columns
+// (8 KB + 1 KB); B stage = NC x 128 bytes; A stages in shared memory (64 K x
+// 256 M fp16, MN-major); two 128-column accumulators.
 constexpr int kQ4Threads = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
 constexpr int kQ4Dequant = 256;  // dequant threads
-constexpr int kQ4BOff0 = 2 * 64 * 128 + 2 * 64 * 16;  // 18432: B rows of the gate / up raw stage
-constexpr int kQ4Raw0 = kQ4BOff0 + 4 * kGemmNC * 128, kQ4RawStages0 = 4;
-constexpr int kQ4AStages0 = 12, kQ4ACol0 = 128, kQ4TmemCols0 = 512;
-constexpr int kQ4BOff1 = 64 * 128 + 64 * 16;  // 9216
-constexpr int kQ4Raw1 = kQ4BOff1 + kGemmNC * 128, kQ4RawStages1 = 7;
-constexpr int kQ4Tile1 = 64 * 256 * 2, kQ4TileStages1 = 3;
-constexpr int kQ4Smem0 = kQ4RawStages0 * kQ4Raw0 + kGemmExch + 1024 + 512;
-constexpr int kQ4Smem1 = kQ4TileStages1 * kQ4Tile1 + kQ4RawStages1 * kQ4Raw1 + 1024 + 512;
-static_assert(kQ4ACol0 + 32 * kQ4AStages0 <= kQ4TmemCols0, "tensor memory of the gate / up kernel");
-static_assert(kQ4Smem0 <= 232448 && kQ4Smem1 <= 232448, "shared memory of the 4-bit GEMMs");
-static_assert(kQ4BOff0 % 1024 == 0 && kQ4Raw0 % 1024 == 0 && kQ4BOff1 % 1024 == 0 && kQ4Raw1 % 1024 == 0,
+constexpr int kQ4Raw0 = 2 * 64 * 128 + 2 * 64 * 16, kQ4RawStages0 = 6;  // 18432
+constexpr int kQ4B0 = 4 * kGemmNC * 128, kQ4BStages0 = 3;
+constexpr int kQ4AStages0 = 3, kQ4ACol0 = 128, kQ4TmemCols0 = 512;
+constexpr int kQ4Raw1 = 64 * 128 + 64 * 16, kQ4RawStages1 = 10;  // 9216
+constexpr int kQ4B1 = kGemmNC * 128, kQ4BStages1 = 4;
+constexpr int kQ4Tile1 = 64 * 256 * 2, kQ4TileStages1 = 3, kQ4TmemCols1 = 256;
+constexpr int kQ4Smem0 = kQ4BStages0 * kQ4B0 + kQ4RawStages0 * kQ4Raw0 + kGemmExch + 1024 + 512;
+constexpr int kQ4Smem1 = kQ4TileStages1 * kQ4Tile1 + kQ4BStages1 * kQ4B1 + kQ4RawStages1 * kQ4Raw1 + 1024 + 512;
+static_assert(kQ4ACol0 + 128 * kQ4AStages0 <= kQ4TmemCols0 && 2 * kGemmNC <= kQ4ACol0, "tensor memory, gate / up");
+static_assert(kQ4Smem0 + 4608 <= 232448 && kQ4Smem1 + 4608 <= 232448, "shared memory of the 4-bit GEMMs");
+static_assert(kQ4Raw0 % 1024 == 0 && kQ4B0 % 1024 == 0 && kQ4Raw1 % 1024 == 0 && kQ4B1 % 1024 == 0,
               "swizzled stage alignment");
 
 // Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
