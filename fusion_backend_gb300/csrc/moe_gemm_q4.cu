@@ -10,23 +10,24 @@
 // Eight codes of a 32-bit word give four half2 (e0,e4) (e1,e5) (e2,e6)
 // (e3,e7): in every group of eight the operands are stored in the order
 // e0 e4 e1 e5 e2 e6 e3 e7.  gate / up take that order along K, so x_perm
-// holds x in the same order (k_bucket_b); down takes it along M, so the
-// epilogue maps accumulator row P to output column 8 (P / 8) + (P % 8) / 2
-// + 4 (P % 2).
+// holds x in the same order (k_bucket_b).
 //
 // gate / up (PHASE 0): one TMA transaction per raw stage (64 gate + 64 up
 // rows x 256 K of codes and scales, and the B rows); the dequant warps write
 // A straight into tensor memory (tcgen05.st, one row per lane), and the MMA
 // reads A from there (the .ts form) and B from the raw stage.
-// down (PHASE 1): the raw stage is 64 downT rows (K) x 256 columns (M) and
-// the B rows; A is M-contiguous, so the dequant warps write the fp16 tile
-// to shared memory in the MN-major 128-byte-swizzled layout and the MMA
-// reads both operands from shared memory.
+// down (PHASE 1): the raw stage is 64 downT rows (K) x 256 columns (M); the
+// codes run along M, so each dequant thread transposes an 8 x 8 block of
+// codes in registers and writes K-major fp16 tiles (128-byte swizzle) to
+// shared memory (an MN-major A operand costs the tensor core about twice
+// the time per MMA); within each group of 8 the K order is rotated by the
+// group index and interleaved as above, and the gate / up epilogue writes h
+// in that order.
 //
 // Block roles (14 warps): warp 0 lane 0 streams raw stages; warp 1 owns the
-// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise, each
-// on its own (a whole raw stage between two synchronisations); warps 10..13
-// are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4) .. + 31.
+// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise in two
+// groups that take alternate raw stages (a whole stage between two
+// synchronisations); warps 10..13 are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4) .. + 31.
 // Every wait is bounded; on a timeout the roles leave their loops and the
 // status word records it.
 #include <cuda.h>
@@ -83,6 +84,58 @@ __device__ __forceinline__ void dequant8(uint32_t w, __half2 dd, uint32_t* o) {
     const __half2 r = __hmul2(c, dd);
     o[i] = *reinterpret_cast<const uint32_t*>(&r);
   }
+}
+
+// Same with one scale pair per half2: o[q] = (code q, code q + 4) times dd[q].
+__device__ __forceinline__ void dequant8s(uint32_t w, const __half2* dd, uint32_t* o) {
+  const __half2 k1032 = __half2half2(__ushort_as_half((unsigned short)0x6408u));  // 1032.0
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+    const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&q), k1032);
+    const __half2 r = __hmul2(c, dd[i]);
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// 8 x 8 transpose of 4-bit codes: r[s] holds row s (code j in bits 4j ..),
+// c[j] gets column j (row s in bits 4s ..).  Two byte-permute stages swap
+// 16-bit and 8-bit blocks, a mask stage swaps single codes.
+__device__ __forceinline__ void transpose8x8_nibbles(const uint32_t* r, uint32_t* c) {
+  uint32_t a[8], b[8];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    a[s] = __byte_perm(r[s], r[s + 4], 0x5410);      // columns 0-3 of rows s, s + 4
+    a[s + 4] = __byte_perm(r[s], r[s + 4], 0x7632);  // columns 4-7 of rows s, s + 4
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int i = 4 * h + s;
+      b[i] = __byte_perm(a[i], a[i + 2], 0x6240);      // 2 columns, rows s, s + 2, s + 4, s + 6
+      b[i + 2] = __byte_perm(a[i], a[i + 2], 0x7351);  // the next 2 columns, same rows
+    }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t e = b[2 * t], o = b[2 * t + 1];  // even rows, odd rows of columns 2t, 2t + 1
+    c[2 * t] = (e & 0x0F0F0F0Fu) | ((o & 0x0F0F0F0Fu) << 4);
+    c[2 * t + 1] = ((e >> 4) & 0x0F0F0F0Fu) | (o & 0xF0F0F0F0u);
+  }
+}
+
+// Bounded wait that sleeps between polls: for the epilogue warps, which wait
+// a whole unit for their accumulator and would otherwise take issue slots
+// from the dequant warps.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
 }
 
 // fp16 scale of a raw stage (little-endian, 2-byte aligned) as a half2 pair
@@ -293,7 +346,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         unit_of(u, w);
         const int nrc = raw_chunks(w);
         const int npad = (w.n + 15) & ~15;
-        const uint32_t idesc = instr_desc(128, npad, PHASE, true);
+        const uint32_t idesc = instr_desc(128, npad, 0, true);  // A and B K-major
         const int ab = nu & 1;
         const uint32_t acc_ph = (uint32_t)(nu >> 1) & 1u;
         const uint32_t dacc = tmem + (uint32_t)ab * kAccCols;
@@ -322,8 +375,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t bdsc = smem_desc(sb + ks * 32, 16, 1024);
               const uint32_t acc = (rc > 0 || ks > 0) ? 1u : 0u;
-              umma(dacc, smem_desc(sa + ks * 2048, 8192, 1024), bdsc, idesc, acc);
-              umma(dacc + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bdsc, idesc, acc);
+              umma(dacc, smem_desc(sa + ks * 32, 16, 1024), bdsc, idesc, acc);
+              umma(dacc + kGemmNC, smem_desc(sa + 16384 + ks * 32, 16, 1024), bdsc, idesc, acc);
             }
           }
           umma_commit(&a_empty[ts]);
@@ -354,75 +407,98 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ dequant
+    // Two groups of four warps (warps 2-5, 6-9; each covers the four lane
+    // quarters) take alternate raw stages, so two stages are in flight.
     // Each warp runs on its own: the waits are per thread, the exit test
     // warp-uniform (tcgen05.st is warp-collective).
-    const int dt = tid - 64;  // 0 .. 255
-    int rs = 0, ts = 0;
+    const int grp = (warp - 2) >> 2;
+    const int dt = (warp & 3) * 32 + lane;  // 0 .. 127 within the group
+    int rs = 0, ts = 0, cc = 0;
     uint32_t rph = 0, tph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       UnitQ w;
       unit_of(u, w);
       const int nrc = raw_chunks(w);
-      for (int rc = 0; rc < nrc; ++rc) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[rs], rph) && mbar_wait(&a_empty[ts], tph ^ 1u) &&
-                                         !aborted(&s_abort));
-        if (!ok) break;
-        const uint8_t* raw = raws + (size_t)rs * kRB;
-        if (PHASE == 0) {
-          // this thread: A row m (tensor-memory lane; 64 gate rows over 64
-          // up rows), K half hf of the stage (128 K: 16-byte units 4 hf ..
-          // 4 hf + 3 of the row, one scale block each)
-          const int q = warp & 3, hf = (warp - 2) >> 2;
-          const int m = 32 * q + lane, rr = m & 63;
-          const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
-          const uint8_t* scl = raw + 16384 + (m >> 6) * 1024 + rr * 16;
-          uint4 wq[4];
-          __half2 dd[4];
+      for (int rc = 0; rc < nrc; ++rc, ++cc) {
+        if ((cc & 1) == grp) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[rs], rph) && mbar_wait(&a_empty[ts], tph ^ 1u) &&
+                                           !aborted(&s_abort));
+          if (!ok) break;
+          const uint8_t* raw = raws + (size_t)rs * kRB;
+          if (PHASE == 0) {
+            // this thread: A row m (tensor-memory lane; 64 gate rows over 64
+            // up rows), the stage's 256 K: 16-byte units 0..7 of the row,
+            // one scale block each
+            const int q = warp & 3;
+            const int m = 32 * q + lane, rr = m & 63;
+            const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
+            const uint8_t* scl = raw + 16384 + (m >> 6) * 1024 + rr * 16;
+            uint4 wq[8];
+            __half2 dd[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int un = 4 * hf + j;
-            wq[j] = *reinterpret_cast<const uint4*>(nib + ((un ^ (rr & 7)) << 4));
-            dd[j] = scale2(scl + un * 2);
-          }
-          mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
-          const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 128 * ts + 64 * hf);
+            for (int j = 0; j < 8; ++j) {
+              wq[j] = *reinterpret_cast<const uint4*>(nib + ((j ^ (rr & 7)) << 4));
+              dd[j] = scale2(scl + j * 2);
+            }
+            mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 128 * ts);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t v[16];
-            dequant8(wq[j].x, dd[j], v);
-            dequant8(wq[j].y, dd[j], v + 4);
-            dequant8(wq[j].z, dd[j], v + 8);
-            dequant8(wq[j].w, dd[j], v + 12);
-            tmem_st16(ta + 16 * j, v);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-        } else {
-          // 64 rows (K) x 256 columns (M): items (row i, 8-column group uu);
-          // group uu goes to 64-column chunk uu / 8, 16-byte unit uu % 8 of
-          // row i (128-byte swizzle)
-          uint8_t* tile = tiles + (size_t)ts * kQ4Tile1;
-          uint32_t wq[8];
-          __half2 dd[8];
+            for (int j = 0; j < 8; ++j) {
+              uint32_t v[16];
+              dequant8(wq[j].x, dd[j], v);
+              dequant8(wq[j].y, dd[j], v + 4);
+              dequant8(wq[j].z, dd[j], v + 8);
+              dequant8(wq[j].w, dd[j], v + 12);
+              tmem_st16(ta + 16 * j, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            // 64 rows (K) x 256 columns (M) -> two K-major 128-row tiles.
+            // Item (k8, g): rows 8 k8 .. + 7, columns 8 g .. + 7; this thread
+            // takes g and g + 16.  The rows are read rotated by k8 (register s
+            // holds row (s + k8) % 8, which keeps the reads conflict-free),
+            // transposed to one code word per column, and stored as one
+            // 16-byte unit per column: position p holds row
+            // (p / 2 + 4 (p % 2) + k8) % 8 of the group, the order in which
+            // the gate / up epilogue writes h.
+            uint8_t* tile = tiles + (size_t)ts * kQ4Tile1;
+            const int k8 = dt & 7;
+            uint32_t rw[2][8];
+            __half dsc[2][8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
-            wq[j] = *reinterpret_cast<const uint32_t*>(raw + i * 128 + (((uu >> 2) ^ (i & 7)) << 4) + (uu & 3) * 4);
-            dd[j] = scale2(raw + 8192 + i * 16 + (uu >> 2) * 2);
-          }
-          mbar_arrive(&raw_empty[rs]);
+            for (int it = 0; it < 2; ++it) {
+              const int g = (dt >> 3) + 16 * it;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int item = dt + 256 * j, i = item >> 5, uu = item & 31;
-            uint32_t v[4];
-            dequant8(wq[j], dd[j], v);
-            *reinterpret_cast<uint4*>(tile + (uu >> 3) * 8192 + i * 128 + (((uu & 7) ^ (i & 7)) << 4)) =
-                make_uint4(v[0], v[1], v[2], v[3]);
+              for (int s2 = 0; s2 < 8; ++s2) {
+                const int i = 8 * k8 + ((s2 + k8) & 7);
+                rw[it][s2] =
+                    *reinterpret_cast<const uint32_t*>(raw + i * 128 + (((g >> 2) ^ (i & 7)) << 4) + (g & 3) * 4);
+                dsc[it][s2] = *reinterpret_cast<const __half*>(raw + 8192 + i * 16 + (g >> 2) * 2);
+              }
+            }
+            mbar_arrive(&raw_empty[rs]);
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+              const int g = (dt >> 3) + 16 * it;
+              __half2 dd[4];
+#pragma unroll
+              for (int q2 = 0; q2 < 4; ++q2) dd[q2] = __halves2half2(dsc[it][q2], dsc[it][q2 + 4]);
+              uint32_t cw[8];
+              transpose8x8_nibbles(rw[it], cw);
+              uint8_t* dst = tile + (g >> 4) * 16384 + (g & 15) * 1024;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t v[4];
+                dequant8s(cw[j], dd, v);
+                *reinterpret_cast<uint4*>(dst + j * 128 + ((k8 ^ j) << 4)) = make_uint4(v[0], v[1], v[2], v[3]);
+              }
+            }
+            fence_async_smem();  // the tile's generic writes, visible to the tensor cores
           }
-          fence_async_smem();  // the tile's generic writes, visible to the tensor cores
+          mbar_arrive(&a_full[ts]);
         }
-        mbar_arrive(&a_full[ts]);
         if (++ts == kTS) {
           ts = 0;
           tph ^= 1u;
@@ -446,7 +522,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       unit_of(u, w);
       const int ab = nu & 1;
       const uint32_t acc = tmem + lane_addr + (uint32_t)ab * kAccCols;
-      const bool ok = mbar_wait(&acc_full[ab], (uint32_t)(nu >> 1) & 1u) && !aborted(&s_abort);
+      const bool ok = mbar_wait_idle(&acc_full[ab], (uint32_t)(nu >> 1) & 1u) && !aborted(&s_abort);
       if (!epilogue_all(ok)) {
         set_abort(&s_abort);
         break;
@@ -465,7 +541,12 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         }
         epilogue_sync();
         if (q >= 2) {
+          // h row i of the slot goes to position 8 G + p of group G = i / 8,
+          // where (p / 2 + 4 (p % 2) + G) % 8 = i % 8: the K order of the
+          // down kernel's A tiles
           const int i = w.tile * 64 + r;
+          const int xr = ((i & 7) - (i >> 3)) & 7;
+          const int ip = (i & ~7) + 2 * (xr & 3) + (xr >> 2);
           for (int j0 = 0; j0 < w.n; j0 += 16) {
             uint32_t v[16];
             tmem_ld16(acc + (uint32_t)j0, v);
@@ -476,7 +557,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
                 const int slot = w.slot0 + j;
                 const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
                 const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
-                h_ws[(size_t)slot * (size_t)P.hw + i] = __half_as_ushort(__float2half_rn(h));
+                h_ws[(size_t)slot * (size_t)P.hw + ip] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }
@@ -484,9 +565,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         tc_fence_before();
         epilogue_sync();
       } else {
-        // accumulator row P = 128 half + m holds output column
-        // tile * 256 + 8 (P / 8) + (P % 8) / 2 + 4 (P % 2)
-        const int c0 = w.tile * 256 + 8 * (m >> 3) + ((m & 7) >> 1) + 4 * (m & 1);
+        // accumulator row 128 half + m holds output column tile * 256 + 128 half + m
+        const int c0 = w.tile * 256 + m;
         for (int j0 = 0; j0 < w.n; j0 += 16) {
           uint32_t r0[16], r1[16];
           tmem_ld16(acc + (uint32_t)j0, r0);
