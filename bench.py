@@ -48,7 +48,8 @@ SEED = 20261202
 # dram__bytes_read.sum + dram__bytes_write.sum of one k_rows launch from the
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
-NCU_TRAFFIC_BYTES = {"decode_bf16": 83_148_800, "decode_q4": 23_104_768, "batched_bf16": 823_113_984, "stack_q4": 23_104_768}
+NCU_TRAFFIC_BYTES = {"decode_bf16": 83_209_216, "decode_q4": 23_105_792, "batched_bf16": 823_113_984,
+                     "batched_q4": 240_892_928, "stack_q4": None}
 STACK_LAYERS = 48
 
 
@@ -459,7 +460,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, n, dt, used = oracle_rate(shapes, wfmt, 15.0, 400)
+        rate, n, dt, used = oracle_rate(shapes, wfmt, 15.0, 100000)
         cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle",
                "sample": f"{n} layer calls of T={T} on layer seed {SEED} ({dt:.1f} s, all host threads offered)"}
 
