@@ -146,7 +146,7 @@ __device__ __forceinline__ __half2 scale2(const uint8_t* p) {
 }  // namespace
 
 template <int PHASE>
-__global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
+__global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
   constexpr int kRS = PHASE == 0 ? kQ4RawStages0 : kQ4RawStages1;
   constexpr int kRB = PHASE == 0 ? kQ4Raw0 : kQ4Raw1;
   constexpr int kBS = PHASE == 0 ? kQ4BStages0 : kQ4BStages1;
@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
   constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared), one per raw stage
   constexpr int kSubs = PHASE == 0 ? 4 : 1;                         // 64-wide K sub-chunks of B per raw stage
   constexpr uint32_t kCols = PHASE == 0 ? kQ4TmemCols0 : kQ4TmemCols1;
-  constexpr uint32_t kAccCols = PHASE == 0 ? kGemmNC : 2 * kGemmNC;  // one accumulator (two buffers)
+  // one accumulator buffer (two buffers); down: two parity accumulators of
+  // two 64-column halves each, one per MMA issuer
+  constexpr uint32_t kAccCols = PHASE == 0 ? kGemmNC : 4 * kGemmNC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* tiles = sm;                                             // down: kTS x kQ4Tile1
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
   __shared__ int s_abort;
   __shared__ int s_cum[kBatchMaxE + 2];
   __shared__ int s_grp[kBatchMaxE + 1][3];
+  __shared__ float s_sw[kGemmNC];  // gate / up epilogue: the unit's slot weights
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = P.T, K = P.K;
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_full[i], PHASE == 0 ? 1 : 2);
       mbar_init(&acc_empty[i], 128);
     }
     s_abort = 0;
@@ -335,8 +338,13 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       for (int i = 0; i < kRS; ++i) mbar_wait(&raw_full[i], i < rs ? rph : rph ^ 1u);
       for (int i = 0; i < kBS; ++i) mbar_wait(&b_full[i], i < bs ? bph : bph ^ 1u);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 14) {
+    // ---------------------------------------------------------- MMA issuers
+    // gate / up: warp 1 issues everything.  down: warp 1 the even K stages
+    // of a unit, warp 14 the odd ones, each into its own accumulator (the
+    // epilogue adds the two in a fixed order), so that one issuer's waits
+    // and commits overlap the other's MMAs
+    const int par = warp == 14 ? 1 : 0;
     if (lane == 0) {
       int bs = 0, ts = 0, nu = 0;
       uint32_t bph = 0, tph = 0;
@@ -349,7 +357,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         const uint32_t idesc = instr_desc(128, npad, 0, true);  // A and B K-major
         const int ab = nu & 1;
         const uint32_t acc_ph = (uint32_t)(nu >> 1) & 1u;
-        const uint32_t dacc = tmem + (uint32_t)ab * kAccCols;
+        const uint32_t dacc = tmem + (uint32_t)ab * kAccCols + (uint32_t)par * (2 * kGemmNC);
         if (!mbar_wait(&acc_empty[ab], acc_ph ^ 1u)) {
           set_abort(&s_abort);
           break;
@@ -357,6 +365,17 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         tc_fence_after();
         bool ok = true;
         for (int rc = 0; rc < nrc; ++rc) {
+          if (PHASE == 1 && (rc & 1) != par) {  // the other issuer's stage
+            if (++ts == kTS) {
+              ts = 0;
+              tph ^= 1u;
+            }
+            if (++bs == kBS) {
+              bs = 0;
+              bph ^= 1u;
+            }
+            continue;
+          }
           ok = mbar_wait(&b_full[bs], bph) && mbar_wait(&a_full[ts], tph);
           if (!ok) break;
           tc_fence_after();
@@ -370,13 +389,13 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
                       (rc > 0 || ks > 0) ? 1u : 0u);
             }
           } else {
-            const uint32_t sa = smem_u32(tiles + (size_t)ts * kQ4Tile1);
+            const uint64_t adsc = smem_desc(smem_u32(tiles + (size_t)ts * kQ4Tile1), 16, 1024);
+            const uint64_t bdsc = smem_desc(sb, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t bdsc = smem_desc(sb + ks * 32, 16, 1024);
-              const uint32_t acc = (rc > 0 || ks > 0) ? 1u : 0u;
-              umma(dacc, smem_desc(sa + ks * 32, 16, 1024), bdsc, idesc, acc);
-              umma(dacc + kGemmNC, smem_desc(sa + 16384 + ks * 32, 16, 1024), bdsc, idesc, acc);
+            for (int ks = 0; ks < 4; ++ks) {  // +32 bytes of K per step: +2 in the address field
+              const uint32_t acc = (rc >= 2 || ks > 0) ? 1u : 0u;  // this issuer's first stage starts the sum
+              umma(dacc, adsc + 2 * ks, bdsc + 2 * ks, idesc, acc);
+              umma(dacc + kGemmNC, adsc + 1024 + 2 * ks, bdsc + 2 * ks, idesc, acc);  // +16 KB: second half
             }
           }
           umma_commit(&a_empty[ts]);
@@ -405,7 +424,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         pending = false;
       }
     }
-  } else if (warp < 10) {
+  } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ dequant
     // Two groups of four warps (warps 2-5, 6-9; each covers the four lane
     // quarters) take alternate raw stages, so two stages are in flight.
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       }
     }
     if (!ok) set_abort(&s_abort);
-  } else {
+  } else if (warp < 14) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int m = 32 * q + lane;
@@ -532,6 +551,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
         // lanes 0..63 gate, 64..127 up of the same rows tile * 64 ..
         const int r = m & 63;
         if (q < 2) {
+          if (r < w.n) s_sw[r] = P.slot_w[w.slot0 + r];
           for (int j0 = 0; j0 < w.n; j0 += 16) {
             uint32_t v[16];
             tmem_ld16(acc + (uint32_t)j0, v);
@@ -556,7 +576,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
               if (j < w.n) {
                 const int slot = w.slot0 + j;
                 const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
-                const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
+                const float h = __fdividef(g, 1.0f + __expf(-g)) * up * s_sw[j];
                 h_ws[(size_t)slot * (size_t)P.hw + ip] = __half_as_ushort(__float2half_rn(h));
               }
             }
@@ -567,17 +587,20 @@ __global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant
       } else {
         // accumulator row 128 half + m holds output column tile * 256 + 128 half + m
         const int c0 = w.tile * 256 + m;
+        // the even-stage accumulator plus the odd-stage one
         for (int j0 = 0; j0 < w.n; j0 += 16) {
-          uint32_t r0[16], r1[16];
+          uint32_t r0[16], r1[16], s0[16], s1[16];
           tmem_ld16(acc + (uint32_t)j0, r0);
           tmem_ld16(acc + (uint32_t)kGemmNC + (uint32_t)j0, r1);
+          tmem_ld16(acc + (uint32_t)(2 * kGemmNC) + (uint32_t)j0, s0);
+          tmem_ld16(acc + (uint32_t)(3 * kGemmNC) + (uint32_t)j0, s1);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
             if (j < w.n) {
               float* dst = P.y_ws + (size_t)(w.slot0 + j) * P.H + c0;
-              dst[0] = __uint_as_float(r0[jj]);
-              dst[128] = __uint_as_float(r1[jj]);
+              dst[0] = __uint_as_float(r0[jj]) + __uint_as_float(s0[jj]);
+              dst[128] = __uint_as_float(r1[jj]) + __uint_as_float(s1[jj]);
             }
           }
         }
@@ -604,7 +627,7 @@ static cudaError_t launch_q4(const BatchParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(kQ4Threads);
+  cfg.blockDim = dim3(PHASE == 0 ? kQ4Threads : kQ4Threads1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
