@@ -49,7 +49,7 @@ SEED = 20261202
 # committed ncu capture (profiles/), per config; None until captured for the
 # current kernel.
 NCU_TRAFFIC_BYTES = {"decode_bf16": 83_209_216, "decode_q4": 23_105_792, "batched_bf16": 823_113_984,
-                     "batched_q4": 238_458_368, "stack_q4": None}
+                     "batched_q4": 238_398_464, "stack_q4": None}
 STACK_LAYERS = 48
 
 

@@ -146,17 +146,19 @@ __device__ __forceinline__ __half2 scale2(const uint8_t* p) {
 }  // namespace
 
 template <int PHASE>
-__global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
+__global__ void __launch_bounds__(kQ4Threads, 1) k_gemm_q4(const __grid_constant__ BatchParams P) {
   constexpr int kRS = PHASE == 0 ? kQ4RawStages0 : kQ4RawStages1;
   constexpr int kRB = PHASE == 0 ? kQ4Raw0 : kQ4Raw1;
   constexpr int kBS = PHASE == 0 ? kQ4BStages0 : kQ4BStages1;
   constexpr int kBB = PHASE == 0 ? kQ4B0 : kQ4B1;
-  constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared), one per raw stage
+  constexpr int kTS = PHASE == 0 ? kQ4AStages0 : kQ4TileStages1;  // A stages (tensor memory / shared)
+  constexpr int kAPer = PHASE == 0 ? 2 : 1;                         // A stages per raw stage
   constexpr int kSubs = PHASE == 0 ? 4 : 1;                         // 64-wide K sub-chunks of B per raw stage
   constexpr uint32_t kCols = PHASE == 0 ? kQ4TmemCols0 : kQ4TmemCols1;
-  // one accumulator buffer (two buffers); down: two parity accumulators of
-  // two 64-column halves each, one per MMA issuer
-  constexpr uint32_t kAccCols = PHASE == 0 ? kGemmNC : 4 * kGemmNC;
+  // one accumulator buffer (of two): one accumulator per MMA issuer (gate /
+  // up: 64 columns; down: two 64-column halves of the output tile)
+  constexpr uint32_t kParCols = PHASE == 0 ? kGemmNC : 2 * kGemmNC;
+  constexpr uint32_t kAccCols = 2 * kParCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* tiles = sm;                                             // down: kTS x kQ4Tile1
@@ -191,14 +193,14 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
     }
     for (int i = 0; i < kBS; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_empty[i], PHASE == 0 ? 2 : 1);  // gate / up: both issuers read every B stage
     }
     for (int i = 0; i < kTS; ++i) {
       mbar_init(&a_full[i], kQ4Dequant);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], PHASE == 0 ? 1 : 2);
+      mbar_init(&acc_full[i], 2);
       mbar_init(&acc_empty[i], 128);
     }
     s_abort = 0;
@@ -340,10 +342,11 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
     }
   } else if (warp == 1 || warp == 14) {
     // ---------------------------------------------------------- MMA issuers
-    // gate / up: warp 1 issues everything.  down: warp 1 the even K stages
-    // of a unit, warp 14 the odd ones, each into its own accumulator (the
-    // epilogue adds the two in a fixed order), so that one issuer's waits
-    // and commits overlap the other's MMAs
+    // Two issuers, each into its own accumulator (the epilogue adds the two
+    // in a fixed order), so that one issuer's waits and commits overlap the
+    // other's MMAs.  gate / up: warp 1 the first 128 K of every raw stage,
+    // warp 14 the second; down: warp 1 the even raw stages of a unit, warp
+    // 14 the odd ones.
     const int par = warp == 14 ? 1 : 0;
     if (lane == 0) {
       int bs = 0, ts = 0, nu = 0;
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
         const uint32_t idesc = instr_desc(128, npad, 0, true);  // A and B K-major
         const int ab = nu & 1;
         const uint32_t acc_ph = (uint32_t)(nu >> 1) & 1u;
-        const uint32_t dacc = tmem + (uint32_t)ab * kAccCols + (uint32_t)par * (2 * kGemmNC);
+        const uint32_t dacc = tmem + (uint32_t)ab * kAccCols + (uint32_t)par * kParCols;
         if (!mbar_wait(&acc_empty[ab], acc_ph ^ 1u)) {
           set_abort(&s_abort);
           break;
@@ -376,18 +379,19 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
             }
             continue;
           }
-          ok = mbar_wait(&b_full[bs], bph) && mbar_wait(&a_full[ts], tph);
+          const int ta = PHASE == 0 ? ts + par : ts;  // gate / up: this issuer's A stage of the pair
+          ok = mbar_wait(&b_full[bs], bph) && mbar_wait(&a_full[ta], tph);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sb = smem_u32(bst + (size_t)bs * kBB);
           if (PHASE == 0) {
-            // 256 K: A columns kQ4ACol0 + 128 ts + 8 ks, B sub-chunk ks / 4
+            // 128 K: A columns kQ4ACol0 + 64 ta + 8 ks, B sub-chunks 2 par, 2 par + 1
+            const uint64_t bdsc = smem_desc(sb + par * (2 * kGemmNC * 128), 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-              const uint64_t bdsc = smem_desc(sb + (ks >> 2) * (kGemmNC * 128) + (ks & 3) * 32, 16, 1024);
-              umma_ts(dacc, tmem + (uint32_t)(kQ4ACol0 + 128 * ts + 8 * ks), bdsc, idesc,
+            for (int ks = 0; ks < 8; ++ks)
+              umma_ts(dacc, tmem + (uint32_t)(kQ4ACol0 + 64 * ta + 8 * ks),
+                      bdsc + (uint64_t)((ks >> 2) * (kGemmNC * 128 / 16) + (ks & 3) * 2), idesc,
                       (rc > 0 || ks > 0) ? 1u : 0u);
-            }
           } else {
             const uint64_t adsc = smem_desc(smem_u32(tiles + (size_t)ts * kQ4Tile1), 16, 1024);
             const uint64_t bdsc = smem_desc(sb, 16, 1024);
@@ -398,10 +402,10 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
               umma(dacc + kGemmNC, adsc + 1024 + 2 * ks, bdsc + 2 * ks, idesc, acc);  // +16 KB: second half
             }
           }
-          umma_commit(&a_empty[ts]);
+          umma_commit(&a_empty[ta]);
           umma_commit(&b_empty[bs]);
           pending = true;
-          if (++ts == kTS) {
+          if ((ts += kAPer) == kTS) {
             ts = 0;
             tph ^= 1u;
           }
@@ -442,13 +446,14 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
       for (int rc = 0; rc < nrc; ++rc, ++cc) {
         if ((cc & 1) == grp) {
           ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[rs], rph) && mbar_wait(&a_empty[ts], tph ^ 1u) &&
+                                           (kAPer == 1 || mbar_wait(&a_empty[ts + kAPer - 1], tph ^ 1u)) &&
                                            !aborted(&s_abort));
           if (!ok) break;
           const uint8_t* raw = raws + (size_t)rs * kRB;
           if (PHASE == 0) {
             // this thread: A row m (tensor-memory lane; 64 gate rows over 64
             // up rows), the stage's 256 K: 16-byte units 0..7 of the row,
-            // one scale block each
+            // one scale block each; units 0-3 go to A stage ts, 4-7 to ts + 1
             const int q = warp & 3;
             const int m = 32 * q + lane, rr = m & 63;
             const uint8_t* nib = raw + (m >> 6) * 8192 + rr * 128;
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
               dd[j] = scale2(scl + j * 2);
             }
             mbar_arrive(&raw_empty[rs]);  // this thread's reads of the raw stage are done
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 128 * ts);
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kQ4ACol0 + 64 * ts);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               uint32_t v[16];
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
               dequant8(wq[j].y, dd[j], v + 4);
               dequant8(wq[j].z, dd[j], v + 8);
               dequant8(wq[j].w, dd[j], v + 12);
-              tmem_st16(ta + 16 * j, v);
+              tmem_st16(ta + 16 * j, v);  // columns 64 ts + 16 j: stage ts + j / 4
             }
             tmem_wait_st();
             tc_fence_before();
@@ -517,8 +522,9 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
             fence_async_smem();  // the tile's generic writes, visible to the tensor cores
           }
           mbar_arrive(&a_full[ts]);
+          if (kAPer == 2) mbar_arrive(&a_full[ts + 1]);
         }
-        if (++ts == kTS) {
+        if ((ts += kAPer) == kTS) {
           ts = 0;
           tph ^= 1u;
         }
@@ -553,10 +559,11 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
         if (q < 2) {
           if (r < w.n) s_sw[r] = P.slot_w[w.slot0 + r];
           for (int j0 = 0; j0 < w.n; j0 += 16) {
-            uint32_t v[16];
+            uint32_t v[16], v2[16];
             tmem_ld16(acc + (uint32_t)j0, v);
+            tmem_ld16(acc + kParCols + (uint32_t)j0, v2);  // the second K half
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) exch[(j0 + jj) * 64 + r] = __uint_as_float(v[jj]);
+            for (int jj = 0; jj < 16; ++jj) exch[(j0 + jj) * 64 + r] = __uint_as_float(v[jj]) + __uint_as_float(v2[jj]);
           }
         }
         epilogue_sync();
@@ -568,14 +575,15 @@ __global__ void __launch_bounds__(PHASE == 0 ? kQ4Threads : kQ4Threads1, 1) k_ge
           const int xr = ((i & 7) - (i >> 3)) & 7;
           const int ip = (i & ~7) + 2 * (xr & 3) + (xr >> 2);
           for (int j0 = 0; j0 < w.n; j0 += 16) {
-            uint32_t v[16];
+            uint32_t v[16], v2[16];
             tmem_ld16(acc + (uint32_t)j0, v);
+            tmem_ld16(acc + kParCols + (uint32_t)j0, v2);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int j = j0 + jj;
               if (j < w.n) {
                 const int slot = w.slot0 + j;
-                const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
+                const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]) + __uint_as_float(v2[jj]);
                 const float h = __fdividef(g, 1.0f + __expf(-g)) * up * s_sw[j];
                 h_ws[(size_t)slot * (size_t)P.hw + ip] = __half_as_ushort(__float2half_rn(h));
               }
@@ -627,7 +635,7 @@ static cudaError_t launch_q4(const BatchParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(PHASE == 0 ? kQ4Threads : kQ4Threads1);
+  cfg.blockDim = dim3(kQ4Threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -153,23 +153,23 @@ constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;
 // rows, from TMA) and A stages (dequantised weights).
 // gate / up: raw stage = 64 gate + 64 up rows x 256 K (codes 2 x 8 KB,
 // scales 2 x 1 KB); B stage = four 64-wide K sub-chunks (4 x NC x 128
-// bytes); A stages in tensor memory (256 K, 128 columns each) behind two
-// 64-column accumulators.  down: raw stage = 64 downT rows x 256 columns
+// bytes); A stages in tensor memory (128 K, 64 columns each, two per raw
+// stage) behind the accumulators: 2 buffers x 2 K-half parities x 64 columns.  down: raw stage = 64 downT rows x 256 columns
 // (8 KB + 1 KB); B stage = NC x 128 bytes; A stages in shared memory (64 K x
 // 256 M fp16, K-major); accumulators: 2 buffers x 2 K-stage parities x 128
 // columns.
-constexpr int kQ4Threads = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
-constexpr int kQ4Threads1 = 480; // down: a second MMA-issuing warp (warp 14)
+constexpr int kQ4Threads = 480;  // producer, 2 MMA issuers (warps 1, 14), 8 dequant warps, 4 epilogue warps
 constexpr int kQ4Dequant = 128;  // dequant threads per stage (two groups of four warps take alternate stages)
 constexpr int kQ4Raw0 = 2 * 64 * 128 + 2 * 64 * 16, kQ4RawStages0 = 6;  // 18432
 constexpr int kQ4B0 = 4 * kGemmNC * 128, kQ4BStages0 = 3;
-constexpr int kQ4AStages0 = 3, kQ4ACol0 = 128, kQ4TmemCols0 = 512;
+constexpr int kQ4AStages0 = 4, kQ4ACol0 = 256, kQ4TmemCols0 = 512;
 constexpr int kQ4Raw1 = 64 * 128 + 64 * 16, kQ4RawStages1 = 8;  // 9216
 constexpr int kQ4B1 = kGemmNC * 128, kQ4BStages1 = 6;
 constexpr int kQ4Tile1 = 64 * 256 * 2, kQ4TileStages1 = 3, kQ4TmemCols1 = 512;
 constexpr int kQ4Smem0 = kQ4BStages0 * kQ4B0 + kQ4RawStages0 * kQ4Raw0 + kGemmExch + 1024 + 512;
 constexpr int kQ4Smem1 = kQ4TileStages1 * kQ4Tile1 + kQ4BStages1 * kQ4B1 + kQ4RawStages1 * kQ4Raw1 + 1024 + 512;
-static_assert(kQ4ACol0 + 128 * kQ4AStages0 <= kQ4TmemCols0 && 2 * kGemmNC <= kQ4ACol0, "tensor memory, gate / up");
+static_assert(kQ4ACol0 + 64 * kQ4AStages0 <= kQ4TmemCols0 && 4 * kGemmNC <= kQ4ACol0 && kQ4AStages0 % 2 == 0,
+              "tensor memory, gate / up");
 static_assert(kQ4Smem0 + 4608 <= 232448 && kQ4Smem1 + 4608 <= 232448, "shared memory of the 4-bit GEMMs");
 static_assert(kQ4Raw0 % 1024 == 0 && kQ4B0 % 1024 == 0 && kQ4Raw1 % 1024 == 0 && kQ4B1 % 1024 == 0,
               "swizzled stage alignment");
