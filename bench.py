@@ -12,7 +12,7 @@ the host cores instead (the reference arm).
 
 With ``--config batched_bf16 --T 64`` (or 256) the same layer runs on the
 batched path (routing, expert-sorted gather, grouped GEMMs on the tensor
-cores, combine).  ``--config stack_q4`` runs the 48-layer 4-bit decode stack
+cores, combine); ``--config batched_q4`` does the same with 4-bit weights.  ``--config stack_q4`` runs the 48-layer 4-bit decode stack
 (pre-norm RMSNorm and residual add per layer, independent seeded layers);
 a step is one token through all 48 layers, and each token's output feeds the
 next token's input (128 sequential tokens by default).

@@ -102,9 +102,13 @@ typedef struct moe_ffn_plan* moe_ffn_plan_t;
  *     H <= 4096 and a multiple of 8 (bf16 weights) or of 256 (4-bit
  *     weights), I, Is >= 1; x fp32 or bf16;
  *   batched path, 9 <= T <= 1024 (routing, expert-sorted gather, grouped
- *     GEMMs on the tcgen05 tensor cores, fixed-order combine): bf16 weights
- *     and bf16 x, E <= 256, top_k <= 32, H a multiple of 256, I and Is
- *     multiples of 128.
+ *     GEMMs on the tcgen05 tensor cores, fixed-order combine): bf16 or 4-bit
+ *     weights and bf16 x, E <= 256, top_k <= 32, H a multiple of 256, I and
+ *     Is multiples of 128.  With 4-bit weights the GEMM operands are fp16:
+ *     each weight is d (code - 8) rounded once to fp16, x and the SwiGLU
+ *     output h are carried in fp16 (accumulation fp32), so x and h must lie
+ *     within fp16's range (|v| < 65504); the decode path keeps the exact
+ *     weights.
  * moe_ffn_query(MOE_FFN_QUERY_PATH) reports the path taken.
  * Returns MOE_FFN_ERR_UNSUPPORTED otherwise, MOE_FFN_ERR_INVALID_ARG for null
  * pointers.  On success *plan is owned by the caller (moe_ffn_destroy).
