@@ -63,6 +63,32 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def init_ranks():
+    """(dist or None, world, rank, local rank): one process per GPU under torchrun (NCCL), else one process."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    return dist, world, rank, local
+
+
+def whole_job(ms_local: float, units_per_rank: int, world: int, dist=None, device="cpu"):
+    """The job's timed-region duration (the slowest rank's, ms) and its throughput: every rank processed
+    units_per_rank units (replicas, weak scaling), so the whole job did units_per_rank * world of them."""
+    ms = ms_local
+    if dist is not None:
+        import torch
+
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, units_per_rank * world / (ms / 1000.0)
+
+
 def workload(cfg: str, T: int):
     wfmt = datagen.WFMT_Q4B32 if cfg in ("decode_q4", "batched_q4", "stack_q4") else datagen.WFMT_BF16
     shapes = datagen.Shapes(T=T, H=H, E=E, top_k=K_TOP, I=I, Is=IS)
@@ -201,9 +227,7 @@ def run_stack(args, shapes, wfmt, name):
 
     import fusion_backend_gb300 as fb
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist, world, rank, local = init_ranks()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     s1 = datagen.Shapes(1, H, E, K_TOP, I, IS)
@@ -241,6 +265,9 @@ def run_stack(args, shapes, wfmt, name):
     clocks = ClockSampler(local)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.2)
     with torch.cuda.stream(stream):
@@ -249,14 +276,15 @@ def run_stack(args, shapes, wfmt, name):
             g.replay()
         ev1.record(stream)
     torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
+    ms, value = whole_job(ev0.elapsed_time(ev1), steps, world, dist, dev)
     if fb.moe_ffn_read_status(plan, ws, stream) != 0:
         raise RuntimeError("device status after the timed region")
     final = x_res.cpu().numpy()
     if not np.all(np.isfinite(final)):
         raise RuntimeError("non-finite stack output")
-    value = steps * world / (ms / 1000.0)
     ms_per_step = ms / steps
     bytes_per_step = STACK_LAYERS * algorithmic_bytes(s1, wfmt, float(K_TOP))
     peak, peak_kind = peaks()
@@ -297,6 +325,8 @@ def run_stack(args, shapes, wfmt, name):
         }
         print(json.dumps(line), flush=True)
     fb.moe_ffn_destroy(plan)
+    if dist is not None:
+        dist.destroy_process_group()
     return 0
 
 
@@ -331,15 +361,8 @@ def main():
 
     import fusion_backend_gb300 as fb
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist, world, rank, local = init_ranks()
     torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl")
 
     def barrier():
         if dist is not None:
@@ -423,17 +446,11 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    steps = args.steps
+    ms, value = whole_job(ev0.elapsed_time(ev1), steps * T, world, dist, dev)
     status = fb.moe_ffn_read_status(plan, ws, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    steps = args.steps
-    tokens = steps * T * world
-    value = tokens / (ms / 1000.0)
     ms_per_step = ms / steps
     peak, peak_kind = peaks()
     achieved_gbs = bytes_per_step / (ms_per_step / 1000.0) / 1e9

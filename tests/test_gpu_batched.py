@@ -58,6 +58,22 @@ def test_batched_small_q4(shapes):
 
 
 @pytest.mark.parametrize("wfmt", [WFMT_BF16, WFMT_Q4B32])
+@pytest.mark.parametrize("T", [3, 150])
+def test_router_ties_take_lower_index(T, wfmt):
+    """Zero router weights: every logit is exactly 0, so each token takes experts 0 .. k-1 (ties to the lower
+    index) with p = 1/k.  At T = 150 (batched path) experts 0 .. 3 each hold 150 slots (three 64-slot chunks) and
+    the other twelve are idle; at T = 3 the decode path takes the same decision."""
+    from tests.test_gpu_parity import check_case
+
+    shapes = Shapes(T=T, H=256, E=16, top_k=4, I=128, Is=128)
+    layer = _layer(4021, shapes, wfmt)
+    layer.router_w[...] = 0
+    x, _ = draw_tokens(4021, layer, T, ACT_BF16, gap=-1.0)
+    got, ref = check_case(layer, x, ACT_BF16, f"ties T={T} wfmt={wfmt}")
+    np.testing.assert_array_equal(ref["ids"], np.tile(np.arange(4, dtype=ref["ids"].dtype), (T, 1)))
+
+
+@pytest.mark.parametrize("wfmt", [WFMT_BF16, WFMT_Q4B32])
 def test_batched_repeat_bitwise(wfmt):
     from tests.devlayer import DevLayer
 
