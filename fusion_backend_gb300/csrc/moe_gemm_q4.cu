@@ -12,10 +12,11 @@
 // e0 e4 e1 e5 e2 e6 e3 e7.  gate / up take that order along K, so x_perm
 // holds x in the same order (k_bucket_b).
 //
-// gate / up (PHASE 0): one TMA transaction per raw stage (64 gate + 64 up
-// rows x 256 K of codes and scales, and the B rows); the dequant warps write
-// A straight into tensor memory (tcgen05.st, one row per lane), and the MMA
-// reads A from there (the .ts form) and B from the raw stage.
+// gate / up (PHASE 0): a raw stage is 64 gate + 64 up rows x 256 K of codes
+// and scales (one TMA transaction); the slots' B rows come in a ring of their
+// own.  The dequant warps write A straight into tensor memory (tcgen05.st,
+// one row per lane), and the MMA reads A from there (the [a] operand form)
+// and B from shared memory.
 // down (PHASE 1): the raw stage is 64 downT rows (K) x 256 columns (M); the
 // codes run along M, so each dequant thread transposes an 8 x 8 block of
 // codes in registers and writes K-major fp16 tiles (128-byte swizzle) to
@@ -24,12 +25,16 @@
 // group index and interleaved as above, and the gate / up epilogue writes h
 // in that order.
 //
-// Block roles (14 warps): warp 0 lane 0 streams raw stages; warp 1 owns the
-// tensor memory and lane 0 issues the MMAs; warps 2..9 dequantise in two
-// groups that take alternate raw stages (a whole stage between two
-// synchronisations); warps 10..13 are the epilogue.  A warp reaches tensor-memory lanes 32 (w % 4) .. + 31.
-// Every wait is bounded; on a timeout the roles leave their loops and the
-// status word records it.
+// Block roles (15 warps): warp 0 lane 0 streams the raw and B stages; lane 0
+// of warps 1 and 14 issue the MMAs, each into its own accumulator (gate / up:
+// the two 128-K halves of every raw stage; down: alternate raw stages), and
+// the epilogue adds the two in a fixed order (one thread issues a
+// tcgen05.mma every ~85 cycles and spends ~500 more per stage on waits and
+// commits; two overlap); warp 1 also owns the tensor memory; warps 2..9
+// dequantise in two groups that take alternate raw stages; warps 10..13 are
+// the epilogue, on two accumulator buffers.  A warp reaches tensor-memory
+// lanes 32 (w % 4) .. + 31.  Every wait is bounded; on a timeout the roles
+// leave their loops and the status word records it.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
