@@ -45,11 +45,12 @@ __device__ __forceinline__ uint4 x8_f16_order(uint4 v) {
 }
 
 // Router logits in two passes.  Pass 1 (this kernel): plain fp32 sums of
-// the exact bf16 x bf16 products, with a bound on their error from the sum of
-// |w||x| -- each lane adds n = H/32 products and the warp tree adds 5
-// levels, so |l - exact| <= ((n + 5) u / (1 - (n + 5) u)) sum|w x| (u =
-// 2^-24); the bound kept is (n + 8) 2^-22 sum|w x| + 2^-20 |l|, about 4x
-// that (and it covers the final rounding of the exact value to fp32).  Pass 2 (the top-k kernel)
+// the exact bf16 x bf16 products -- each lane adds n = H/32 products and the
+// warp tree adds 5 levels, so |l - exact| <= ((n + 5) u / (1 - (n + 5) u))
+// sum|w x| (u = 2^-24) -- and the norms |w_r|_2, |x_t|_2, which bound
+// sum|w x| from above (Cauchy-Schwarz).  The top-k kernel takes the bound
+// (n + 8) 2^-22 |w|_2 |x|_2 + 2^-20 |l|, about 4x the above (and it covers
+// the final rounding of the exact value to fp32).  Pass 2 (the top-k kernel)
 // recomputes exactly every logit whose interval can reach the top-k.  Block
 // (token group, row group): 4 warps x 1 row x 8 tokens, small blocks so that
 // the whole grid is resident at once.  The first block also clears the
@@ -74,9 +75,9 @@ __global__ void __launch_bounds__(128, 7) k_route_b(const __grid_constant__ Batc
   }
   const int r = blockIdx.y * kRouteRows + warp;
   const uint16_t* w = r < P.E ? P.router_w + (size_t)r * P.H : P.gate_w;
-  float s[kRouteTokens], a[kRouteTokens];
+  float s[kRouteTokens], wsq = 0.f;
 #pragma unroll
-  for (int t = 0; t < kRouteTokens; ++t) s[t] = a[t] = 0.f;
+  for (int t = 0; t < kRouteTokens; ++t) s[t] = 0.f;
   __syncthreads();  // the barrier is initialised before any thread waits on it
   const bool ok = mbar_wait(&s_bar, 0);
   if (!ok && lane == 0) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
@@ -98,27 +99,45 @@ __global__ void __launch_bounds__(128, 7) k_route_b(const __grid_constant__ Batc
         const float wf[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
+        for (int e = 0; e < 8; ++e) wsq = fmaf(wf[e], wf[e], wsq);
+#pragma unroll
         for (int t = 0; t < kRouteTokens; ++t) {
           if (t >= nt) break;
           const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * P.H + c0);
           const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                                bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            s[t] = fmaf(wf[e], xf[e], s[t]);
-            a[t] = fmaf(fabsf(wf[e]), fabsf(xf[e]), a[t]);
-          }
+          for (int e = 0; e < 8; ++e) s[t] = fmaf(wf[e], xf[e], s[t]);
         }
       }
     }
 #pragma unroll
     for (int t = 0; t < kRouteTokens; ++t) {
-      const float st = warp_sum(s[t]), at = warp_sum(a[t]);
-      if (lane == 0 && t < nt) {
-        P.logits[(size_t)(t0 + t) * P.ls + r] = st;
-        P.lbound[(size_t)(t0 + t) * P.ls + r] = at * ((float)(P.H / 32 + 8) * 0x1p-22f) + fabsf(st) * 0x1p-20f;
+      const float st = warp_sum(s[t]);
+      if (lane == 0 && t < nt) P.logits[(size_t)(t0 + t) * P.ls + r] = st;
+    }
+    // |w_r|_2 (the first token group's blocks write it), rounded up by 2^-8:
+    // the fp32 sum of squares and the square root are off by far less
+    const float wn = sqrtf(warp_sum(wsq)) * (1.0f + 0x1p-8f);
+    if (lane == 0 && blockIdx.x == 0) P.lbound[r] = wn;
+  }
+  if (blockIdx.y == 0 && ok) {
+    // |x_t|_2 of this block's tokens (16 threads a token), rounded up likewise
+    const int t = tid >> 4, l16 = tid & 15;
+    float q = 0.f;
+    if (t < nt) {
+      const uint16_t* xt = reinterpret_cast<const uint16_t*>(route_smem) + (size_t)t * P.H;
+      for (int c0 = l16 * 8; c0 < P.H; c0 += 128) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xt + c0);
+        const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                             bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q = fmaf(xf[e], xf[e], q);
       }
     }
+#pragma unroll
+    for (int o = 8; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    if (l16 == 0 && t < nt) P.lbound[P.ls + t0 + t] = sqrtf(q) * (1.0f + 0x1p-8f);
   }
 }
 
@@ -184,13 +203,15 @@ __global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchPar
   uint32_t cmask[EPL];
   {
     const float* lg = P.logits + (size_t)t * P.ls;
-    const float* bd = P.lbound + (size_t)t * P.ls;
+    const float* wn = P.lbound;                                                   // |w_e|_2
+    const float xb = __fmul_ru(__ldcg(P.lbound + P.ls + t), (float)(P.H / 32 + 8) * 0x1p-22f);  // (n + 8) 2^-22 |x_t|_2
     float hi[EPL];
     uint32_t key[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      const float l = e < E ? __ldcg(lg + e) : 0.f, b = e < E ? __ldcg(bd + e) : 0.f;
+      const float l = e < E ? __ldcg(lg + e) : 0.f;
+      const float b = e < E ? __fadd_ru(__fmul_ru(__ldcg(wn + e), xb), __fmul_ru(fabsf(l), 0x1p-20f)) : 0.f;
       const float lo = __fsub_rd(l, b);
       hi[i] = __fadd_ru(l, b);
       key[i] = e < E ? float_order_key(lo != lo ? -INFINITY : lo) : 0u;

@@ -97,7 +97,7 @@ struct BatchParams {
   // workspace
   uint32_t* ctrl;
   float* logits;  // [T][ls] fp32 logits (plain sums)
-  float* lbound;  // [T][ls] bound on |logit - exact logit|
+  float* lbound;  // norms for the logit error bound: [0, ls) router rows' |w|_2, [ls, ls + T) tokens' |x|_2 (rounded up)
   int ls;
   int32_t* ids;       // [T][K] chosen experts, rank order
   float* p;           // [T][K] their weights
