@@ -63,6 +63,10 @@ def lib():
         _lib.or_bf16_to_double.argtypes = [ctypes.c_uint16]
         _lib.or_expert_bytes.restype = i64
         _lib.or_expert_bytes.argtypes = [ctypes.c_int, i64, i64]
+        _lib.or_threads_used.restype = ctypes.c_int
+        _lib.or_threads_used.argtypes = [ctypes.POINTER(_Shapes), ctypes.c_int]
+        _lib.or_float_to_bf16.restype = ctypes.c_uint16
+        _lib.or_float_to_bf16.argtypes = [ctypes.c_float]
     return _lib
 
 
@@ -72,10 +76,22 @@ def _c(a, dtype):
 
 
 def nthreads() -> int:
+    """Host cores this process may run on (sched_getaffinity)."""
     try:
         return max(1, len(os.sched_getaffinity(0)))
     except AttributeError:  # pragma: no cover
         return os.cpu_count() or 1
+
+
+def threads_used(shapes, threads=None) -> int:
+    """Threads a layer call of these shapes starts when offered ``threads`` (default: all cores)."""
+    s = _Shapes(shapes.T, shapes.H, shapes.E, shapes.top_k, shapes.I, shapes.Is)
+    return int(lib().or_threads_used(ctypes.byref(s), threads or nthreads()))
+
+
+def float_to_bf16(v: float) -> int:
+    """The oracle's fp32 -> bf16 conversion (round to nearest even) of one value."""
+    return int(lib().or_float_to_bf16(ctypes.c_float(v)))
 
 
 def moe_ffn(shapes, act, wfmt, x, router_w, expert_w, shexp_w, shexp_gate_w, threads=None):

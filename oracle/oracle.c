@@ -205,30 +205,66 @@ int32_t or_bucketing(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_
 /* ---------------------------------------------------------------- */
 /* The layer                                                         */
 
+/* The FFNs of a layer call (one per routed (token, slot) and one per token for
+ * the shared expert) are evaluated in two phases, each split into tasks of
+ * TASK_ROWS rows that any thread may take:
+ *   phase 0: h[i] = silu(gate_i . x) * (up_i . x) for rows i of each FFN;
+ *   phase 1: y[c] = sum_i downT[i,c] h[i], i ascending, for columns c.
+ * Every value is computed by exactly the loops of or_swiglu_ffn (same terms,
+ * same order), so the result is bit-identical to calling or_swiglu_ffn per FFN
+ * and does not depend on the number of threads. */
+#define TASK_ROWS 64
+
 typedef struct {
   const uint8_t* blk;
   int wfmt;
   int64_t H, inter;
   const double* x;
-  double* y;
+  double* h; /* [inter] */
+  double* y; /* [H] */
 } ffn_job;
 
 typedef struct {
   ffn_job* jobs;
   int64_t njobs;
+  int64_t* first; /* [njobs + 1]: first task of each job in the current phase */
+  int phase;
   int64_t next;
   pthread_mutex_t mu;
 } job_queue;
 
+static void run_task(const ffn_job* f, int phase, int64_t r0, int64_t r1) {
+  const int64_t mb = matrix_bytes(f->wfmt, f->inter, f->H);
+  if (phase == 0) {
+    for (int64_t i = r0; i < r1; ++i) {
+      double g = 0.0, u = 0.0;
+      for (int64_t c = 0; c < f->H; ++c) g += weight_at(f->blk, f->wfmt, f->H, i, c) * f->x[c];
+      for (int64_t c = 0; c < f->H; ++c) u += weight_at(f->blk + mb, f->wfmt, f->H, i, c) * f->x[c];
+      f->h[i] = silu(g) * u;
+    }
+  } else {
+    for (int64_t c = r0; c < r1; ++c) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < f->inter; ++i) acc += weight_at(f->blk + 2 * mb, f->wfmt, f->H, i, c) * f->h[i];
+      f->y[c] = acc;
+    }
+  }
+}
+
 static void* ffn_worker(void* arg) {
   job_queue* q = (job_queue*)arg;
+  const int64_t ntasks = q->first[q->njobs];
   for (;;) {
     pthread_mutex_lock(&q->mu);
-    int64_t j = q->next++;
+    int64_t k = q->next++;
     pthread_mutex_unlock(&q->mu);
-    if (j >= q->njobs) break;
-    ffn_job* f = &q->jobs[j];
-    or_swiglu_ffn(f->blk, f->wfmt, f->H, f->inter, f->x, f->y);
+    if (k >= ntasks) break;
+    int64_t j = 0;
+    while (q->first[j + 1] <= k) ++j;
+    const ffn_job* f = &q->jobs[j];
+    const int64_t n = q->phase == 0 ? f->inter : f->H;
+    const int64_t r0 = (k - q->first[j]) * TASK_ROWS;
+    run_task(f, q->phase, r0, r0 + TASK_ROWS < n ? r0 + TASK_ROWS : n);
   }
   return NULL;
 }
@@ -237,18 +273,39 @@ static void run_jobs(ffn_job* jobs, int64_t njobs, int nthreads) {
   job_queue q;
   q.jobs = jobs;
   q.njobs = njobs;
-  q.next = 0;
+  q.first = (int64_t*)malloc(sizeof(int64_t) * (size_t)(njobs + 1));
   pthread_mutex_init(&q.mu, NULL);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
-  if (nthreads > njobs) nthreads = (int)njobs;
-  pthread_t th[256];
-  int created[256];
-  for (int t = 1; t < nthreads; ++t) created[t] = pthread_create(&th[t], NULL, ffn_worker, &q) == 0;
-  ffn_worker(&q);
-  for (int t = 1; t < nthreads; ++t)
-    if (created[t]) pthread_join(th[t], NULL);
+  for (int phase = 0; phase < 2; ++phase) {
+    q.phase = phase;
+    q.next = 0;
+    q.first[0] = 0;
+    for (int64_t j = 0; j < njobs; ++j)
+      q.first[j + 1] = q.first[j] + ((phase == 0 ? jobs[j].inter : jobs[j].H) + TASK_ROWS - 1) / TASK_ROWS;
+    int nt = nthreads;
+    if (nt > q.first[njobs]) nt = (int)q.first[njobs];
+    pthread_t th[256];
+    int created[256];
+    for (int t = 1; t < nt; ++t) created[t] = pthread_create(&th[t], NULL, ffn_worker, &q) == 0;
+    ffn_worker(&q);
+    for (int t = 1; t < nt; ++t)
+      if (created[t]) pthread_join(th[t], NULL);
+  }
   pthread_mutex_destroy(&q.mu);
+  free(q.first);
+}
+
+/* Threads a layer call of these shapes would use when offered nthreads. */
+int or_threads_used(const or_shapes* s, int nthreads) {
+  const int64_t njobs = (int64_t)s->T * s->top_k + s->T;
+  const int64_t t0 = ((int64_t)s->T * s->top_k * ((s->I + TASK_ROWS - 1) / TASK_ROWS) +
+                      (int64_t)s->T * ((s->Is + TASK_ROWS - 1) / TASK_ROWS));
+  const int64_t t1 = njobs * ((s->H + TASK_ROWS - 1) / TASK_ROWS);
+  int64_t m = t0 > t1 ? t0 : t1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  return (int)(m < nthreads ? m : nthreads);
 }
 
 /*
@@ -287,17 +344,20 @@ int or_moe_ffn(const or_shapes* s, int act, int wfmt, const void* x, const uint1
   /* One job per routed (token, slot) and one per token for the shared expert. */
   const int64_t eb = or_expert_bytes(wfmt, H, I);
   const int64_t njobs = T * k + T;
+  const int64_t hmax = I > Is ? I : Is;
   ffn_job* jobs = (ffn_job*)malloc(sizeof(ffn_job) * (size_t)njobs);
   double* y = (double*)malloc(sizeof(double) * (size_t)(njobs * H));
+  double* hbuf = (double*)malloc(sizeof(double) * (size_t)(njobs * hmax));
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t j = 0; j < k; ++j) {
       int64_t n = t * k + j;
-      jobs[n] = (ffn_job){expert_w + (int64_t)ids[n] * eb, wfmt, H, I, xd + t * H, y + n * H};
+      jobs[n] = (ffn_job){expert_w + (int64_t)ids[n] * eb, wfmt, H, I, xd + t * H, hbuf + n * hmax, y + n * H};
     }
     int64_t n = T * k + t;
-    jobs[n] = (ffn_job){shexp_w, wfmt, H, Is, xd + t * H, y + n * H};
+    jobs[n] = (ffn_job){shexp_w, wfmt, H, Is, xd + t * H, hbuf + n * hmax, y + n * H};
   }
   run_jobs(jobs, njobs, nthreads);
+  free(hbuf);
 
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t h = 0; h < H; ++h) {

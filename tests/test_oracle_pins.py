@@ -250,6 +250,35 @@ def test_thread_count_does_not_change_bits(tiny_layer):
     np.testing.assert_array_equal(a["out"], b["out"])
 
 
+@pytest.mark.parametrize("wfmt", [WFMT_BF16, WFMT_Q4B32])
+@pytest.mark.parametrize("threads", [1, 5])
+def test_layer_split_over_rows_equals_whole_ffns(wfmt, threads):
+    """The layer evaluates its FFNs in row and column tasks spread over threads; with top_k = 1 (p = 1) and the
+    shared down projection zeroed (shared term exactly 0) each output row must equal, bit for bit, one whole
+    SwiGLU FFN of the chosen expert (or_swiglu_ffn, pinned against torch above), rounded to fp32.  Sizes that are
+    not multiples of the task size check the ragged last task."""
+    if wfmt == WFMT_BF16:
+        shapes = datagen.Shapes(T=3, H=264, E=5, top_k=1, I=136, Is=72)
+    else:
+        shapes = datagen.Shapes(T=3, H=288, E=5, top_k=1, I=96, Is=160)
+    layer = datagen.make_layer(41, with_T(shapes, 1), wfmt)
+    sh = layer.shexp_w.copy()
+    mb = sh.size // 3
+    if wfmt == WFMT_BF16:
+        sh[2 * mb :] = 0
+    else:
+        # zero every scale of the shared downT rows: its weights decode to exactly 0
+        sh[2 * mb :].reshape(shapes.Is, -1)[:, shapes.H // 2 :] = 0
+    x, _ = draw_tokens(41, layer, shapes.T, ACT_F32)
+    r = oracle.moe_ffn(shapes, ACT_F32, wfmt, x, layer.router_w, layer.expert_w, sh, layer.shexp_gate_w,
+                       threads=threads)
+    eb = layer.expert_w.size // shapes.E
+    for t in range(shapes.T):
+        e = int(r["ids"][t, 0])
+        y = oracle.swiglu_ffn(layer.expert_w[e * eb : (e + 1) * eb], wfmt, shapes.H, shapes.I, x[t].astype(np.float64))
+        np.testing.assert_array_equal(r["out"][t], y.astype(np.float32))
+
+
 def test_expert_permutation_invariance(tiny_layer):
     layer = tiny_layer
     s = layer.shapes
@@ -360,6 +389,43 @@ def test_rmsnorm_matches_numpy():
     y = datagen.bf16_to_f32(oracle.rmsnorm_bf16(x)).astype(np.float64)
     ref = x.astype(np.float64) / np.sqrt(np.mean(x.astype(np.float64) ** 2) + 1e-6)
     assert np.max(np.abs(y - ref) / np.maximum(np.abs(ref), 1e-30)) <= 2.0**-8
+
+
+def test_float_to_bf16_rounds_ties_to_even():
+    """bf16 keeps 8 significant bits.  Values exactly halfway between two bf16 neighbours go to the one with an
+    even last bit: 1 + 3*2^-8 (between 0x3F81 and 0x3F82) rounds up to 0x3F82, 1 + 2^-8 (between 0x3F80 and 0x3F81)
+    rounds down to 0x3F80; truncation would give 0x3F81 for the first, rounding half up 0x3F81 for the second."""
+    assert oracle.float_to_bf16(1.0 + 3 * 2.0**-8) == 0x3F82
+    assert oracle.float_to_bf16(1.0 + 2.0**-8) == 0x3F80
+    assert oracle.float_to_bf16(-(1.0 + 3 * 2.0**-8)) == 0xBF82
+    assert oracle.float_to_bf16(-(1.0 + 2.0**-8)) == 0xBF80
+    # just above a tie rounds up, just below rounds down
+    assert oracle.float_to_bf16(1.0 + 2.0**-8 + 2.0**-20) == 0x3F81
+    assert oracle.float_to_bf16(1.0 + 3 * 2.0**-8 - 2.0**-20) == 0x3F81
+    # exact values and the largest finite bf16
+    assert oracle.float_to_bf16(1.0 + 2.0**-7) == 0x3F81
+    assert oracle.float_to_bf16(3.4375) == 0x405C
+    assert oracle.float_to_bf16(float(np.float32(3.3895313892515355e38))) == 0x7F7F
+
+
+def test_rmsnorm_exact_ties_with_unit_factor():
+    """H = 16 values n/256 whose squares sum to exactly 16, so mean(x^2) = 1 and with eps = 0 the factor is exactly
+    1: the output is bf16(x), and the tie values must round to even (see the test above)."""
+    n = [259, 257, -259, 258, 1, 2, 86, 880] + [0] * 8
+    assert sum(v * v for v in n) == 16 * 256 * 256
+    y = oracle.rmsnorm_bf16((np.array(n, np.float64) / 256).astype(np.float32), eps=0.0)
+    assert list(y[:8]) == [0x3F82, 0x3F80, 0xBF82, 0x3F81, 0x3B80, 0x3C00, 0x3EAC, 0x405C]
+    assert np.all(y[8:] == 0)
+
+
+def test_rmsnorm_eps_inside_the_root():
+    """x = 1e-3 everywhere: y = c / sqrt(c^2 + eps).  eps = 1e-6 gives 1/sqrt(2) = 0.7071 -> bf16 0x3F35;
+    eps = 1e-5 gives 0.3015 -> 0x3E9A; eps = 0 gives 1 -> 0x3F80.  eps added outside the root (c / (c + eps))
+    would give 0.999 -> 0x3F80, and eps scaled by H would give a value near 0.022."""
+    c = np.full(64, 1e-3, np.float32)
+    assert np.all(oracle.rmsnorm_bf16(c, eps=1e-6) == 0x3F35)
+    assert np.all(oracle.rmsnorm_bf16(c, eps=1e-5) == 0x3E9A)
+    assert np.all(oracle.rmsnorm_bf16(c, eps=0.0) == 0x3F80)
 
 
 def test_block_step_is_norm_then_layer_then_residual():
