@@ -153,14 +153,36 @@ typedef struct {
   int kind; /* 0: f32, 1: bf16 */
 } fill_job;
 
+static void store_at(const fill_job* j, int64_t i, double z) {
+  float v = (float)(z * j->std);
+  if (j->kind == 0)
+    ((float*)j->out)[i] = v;
+  else
+    ((uint16_t*)j->out)[i] = f32_to_bf16(v);
+}
+
+/* Elements of one Box-Muller pair share u1, u2 and the radius: both are
+ * formed from one evaluation of them (the same expressions as normal_at,
+ * so the same bits). */
 static void* fill_worker(void* arg) {
+  const double two_pi = 6.283185307179586476925286766559;
   fill_job* j = (fill_job*)arg;
-  for (int64_t i = j->begin; i < j->end; ++i) {
-    float v = (float)(normal_at(j->key, j->offset + (uint64_t)i) * j->std);
-    if (j->kind == 0)
-      ((float*)j->out)[i] = v;
-    else
-      ((uint16_t*)j->out)[i] = f32_to_bf16(v);
+  int64_t i = j->begin;
+  while (i < j->end) {
+    const uint64_t c = j->offset + (uint64_t)i;
+    if ((c & 1) || i + 1 == j->end) {
+      store_at(j, i, normal_at(j->key, c));
+      ++i;
+      continue;
+    }
+    const uint64_t a = mix64(j->key + c * DG_GAMMA);
+    const uint64_t b = mix64(j->key + (c + 1) * DG_GAMMA);
+    const double u1 = (double)((a >> 11) + 1) * (1.0 / 9007199254740992.0);
+    const double u2 = (double)(b >> 11) * (1.0 / 9007199254740992.0);
+    const double rad = sqrt(-2.0 * log(u1));
+    store_at(j, i, rad * cos(two_pi * u2));
+    store_at(j, i + 1, rad * sin(two_pi * u2));
+    i += 2;
   }
   return NULL;
 }
