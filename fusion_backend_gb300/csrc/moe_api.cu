@@ -387,22 +387,27 @@ namespace {
 // Every GPU that loads this library holds these bytes until the process exits.
 __device__ __align__(256) uint8_t g_static_scratch[MOE_FFN_STATIC_SCRATCH_BYTES];
 
-void* g_static_scratch_addr[kMaxDevices];
+std::atomic<void*> g_static_scratch_addr[kMaxDevices];
 std::mutex g_static_scratch_mu;
 
 // Device address of g_static_scratch on the current device, looked up once per
-// device (the host-side symbol is only a stand-in for it).
+// device with that device current (the host-side symbol is only a stand-in for
+// it).  Later calls read the cached address without taking the lock.
 int static_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_FFN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_FFN_ERR_DEVICE;
-  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (!g_static_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_FFN_ERR_CUDA;
-    g_static_scratch_addr[dev] = p;
+  void* p = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    p = g_static_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      cudaError_t err = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (err != cudaSuccess || !p) return cuda_status(err != cudaSuccess ? err : cudaErrorInvalidSymbol);
+      g_static_scratch_addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_static_scratch_addr[dev];
+  *out = p;
   return MOE_FFN_OK;
 }
 

@@ -44,13 +44,22 @@ __device__ __forceinline__ uint4 x8_f16_order(uint4 v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// sqrt(H) 2^-75 rounded up: the most a norm can lose to squares that round
+// in the subnormal range (see k_route_b).
+__device__ __forceinline__ float norm_underflow_pad(int H) { return __fmul_ru(sqrtf((float)H) * 1.0001f, 0x1p-75f); }
+
 // Router logits in two passes.  Pass 1 (this kernel): plain fp32 sums of
-// the exact bf16 x bf16 products -- each lane adds n = H/32 products and the
-// warp tree adds 5 levels, so |l - exact| <= ((n + 5) u / (1 - (n + 5) u))
-// sum|w x| (u = 2^-24) -- and the norms |w_r|_2, |x_t|_2, which bound
-// sum|w x| from above (Cauchy-Schwarz).  The top-k kernel takes the bound
-// (n + 8) 2^-22 |w|_2 |x|_2 + 2^-20 |l|, about 4x the above (and it covers
-// the final rounding of the exact value to fp32).  Pass 2 (the top-k kernel)
+// the bf16 x bf16 products (fused multiply-adds: the product is exact inside
+// each, only the sum rounds) -- each lane adds n = H/32 products and the warp
+// tree adds 5 levels, so |l - exact| <= ((n + 5) u / (1 - (n + 5) u))
+// sum|w x| + H 2^-150 (u = 2^-24; the second term is the rounding of partial
+// sums in the subnormal range, at most 2^-150 per fused multiply-add, and the
+// warp tree's additions there are exact) -- and the norms |w_r|_2, |x_t|_2,
+// which bound sum|w x| from above (Cauchy-Schwarz).  The top-k kernel takes
+// the bound (n + 8) 2^-22 |w|_2 |x|_2 + 2^-20 |l| + H 2^-149, about 4x the
+// above (and it covers the final rounding of the exact value to fp32); the
+// norms carry their own margin for squares lost to underflow, so the bound
+// holds for every finite input.  Pass 2 (the top-k kernel)
 // recomputes exactly every logit whose interval can reach the top-k.  Block
 // (token group, row group): 4 warps x 1 row x 8 tokens, small blocks so that
 // the whole grid is resident at once.  The first block also clears the
@@ -117,8 +126,11 @@ __global__ void __launch_bounds__(128, 7) k_route_b(const __grid_constant__ Batc
       if (lane == 0 && t < nt) P.logits[(size_t)(t0 + t) * P.ls + r] = st;
     }
     // |w_r|_2 (the first token group's blocks write it), rounded up by 2^-8:
-    // the fp32 sum of squares and the square root are off by far less
-    const float wn = sqrtf(warp_sum(wsq)) * (1.0f + 0x1p-8f);
+    // the fp32 sum of squares and the square root are off by far less.  Squares
+    // in the subnormal range lose at most 2^-150 each to rounding, so the exact
+    // norm is below sqrt(sum + H 2^-150) <= sqrt(sum) + sqrt(H) 2^-75: that
+    // term is added too.
+    const float wn = __fadd_ru(__fmul_ru(sqrtf(warp_sum(wsq)), 1.0f + 0x1p-8f), norm_underflow_pad(P.H));
     if (lane == 0 && blockIdx.x == 0) P.lbound[r] = wn;
   }
   if (blockIdx.y == 0 && ok) {
@@ -137,7 +149,8 @@ __global__ void __launch_bounds__(128, 7) k_route_b(const __grid_constant__ Batc
     }
 #pragma unroll
     for (int o = 8; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-    if (l16 == 0 && t < nt) P.lbound[P.ls + t0 + t] = sqrtf(q) * (1.0f + 0x1p-8f);
+    if (l16 == 0 && t < nt)
+      P.lbound[P.ls + t0 + t] = __fadd_ru(__fmul_ru(sqrtf(q), 1.0f + 0x1p-8f), norm_underflow_pad(P.H));
   }
 }
 
@@ -205,13 +218,17 @@ __global__ void __launch_bounds__(256) k_topk_b(const __grid_constant__ BatchPar
     const float* lg = P.logits + (size_t)t * P.ls;
     const float* wn = P.lbound;                                                   // |w_e|_2
     const float xb = __fmul_ru(__ldcg(P.lbound + P.ls + t), (float)(P.H / 32 + 8) * 0x1p-22f);  // (n + 8) 2^-22 |x_t|_2
+    // rounding of partial sums in the subnormal range: at most 2^-150 per
+    // fused multiply-add, H of them over the warp's lanes
+    const float sub_floor = __fmul_ru((float)P.H, 0x1p-149f);
     float hi[EPL];
     uint32_t key[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
       const float l = e < E ? __ldcg(lg + e) : 0.f;
-      const float b = e < E ? __fadd_ru(__fmul_ru(__ldcg(wn + e), xb), __fmul_ru(fabsf(l), 0x1p-20f)) : 0.f;
+      const float b =
+          e < E ? __fadd_ru(__fadd_ru(__fmul_ru(__ldcg(wn + e), xb), __fmul_ru(fabsf(l), 0x1p-20f)), sub_floor) : 0.f;
       const float lo = __fsub_rd(l, b);
       hi[i] = __fadd_ru(l, b);
       key[i] = e < E ? float_order_key(lo != lo ? -INFINITY : lo) : 0u;

@@ -31,16 +31,20 @@
 // of its own output columns in block order and writes out (adding x_res in
 // the block form).  All orders are fixed, so results are bitwise repeatable.
 //
-// 4-bit weights, fast instance: codes are decoded with the fp16 exponent
-// trick (a nibble n OR-ed into the mantissa of fp16 1024 reads 1024 + n, so
-// (1024 + n) - 1032 = n - 8 exactly); products with the fp16 activation and
-// their 16-element sums are formed with packed half2 FMAs and scaled by the
-// block's d in fp32.  The general instance decodes to fp32.
+// Tensor-core instances (H = 2048, bf16-exact activation): the stage loops
+// run on mma.m16n8k16 / m16n8k8 over the swizzled tensor-copy boxes.  With
+// 4-bit weights each code becomes the exact bf16 (code - 8) in registers (the
+// nibble OR-ed into the mantissa of bf16 128 reads 128 + n, minus 136), the
+// products of a 32-element block are summed on the tensor cores and scaled by
+// the block's fp16 scale in fp32, so no weight is rounded.  The general
+// instance decodes every weight to fp32 and uses CUDA-core FMAs.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "moe_layer_common.cuh"
@@ -100,47 +104,10 @@ MOE_DEV uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t c) {
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(m), "r"(c));
   return r;
 }
-MOE_DEV uint32_t h2_sub(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-MOE_DEV uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-MOE_DEV float h2_sum(uint32_t a) {
-  const __half2 h = *reinterpret_cast<const __half2*>(&a);
-  const float2 f = __half22float2(h);
-  return f.x + f.y;
-}
-MOE_DEV uint32_t pack_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// The 8 codes of one 32-bit word (elements 2j in the low nibble of byte j)
-// -> 4 half2 of (n - 8): (e0,e4) (e1,e5) (e2,e6) (e3,e7), the order of
-// pack_quarter.
-MOE_DEV void dequant_quarter(uint32_t w, uint32_t* o) {
-  constexpr uint32_t kMagic = 0x64006400u, kSub = 0x64086408u, kSixteenth = 0x2C002C00u, kMinus72 = 0xD480D480u;
-  const uint32_t w8 = w >> 8;
-  o[0] = h2_sub(lop3_and_or(w, 0x000F000Fu, kMagic), kSub);
-  o[1] = h2_fma(lop3_and_or(w, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
-  o[2] = h2_sub(lop3_and_or(w8, 0x000F000Fu, kMagic), kSub);
-  o[3] = h2_fma(lop3_and_or(w8, 0x00F000F0u, kMagic), kSixteenth, kMinus72);
-}
-
 // Code n of nibble j of a 32-bit word, as the float n - 8 (exact: the
 // nibble OR-ed into the mantissa of 2^23 reads 2^23 + n).
 MOE_DEV float nib_f32(uint32_t w, int j) {
   return __fsub_rn(__uint_as_float(0x4B000000u | ((w >> (4 * j)) & 0xFu)), 8388616.0f);
-}
-
-// Eight consecutive values c = 8q .. 8q+7 of a row -> the uint4 of quarter q%4.
-MOE_DEV uint4 pack_quarter(const float* v) {
-  return make_uint4(pack_h2(v[0], v[4]), pack_h2(v[1], v[5]), pack_h2(v[2], v[6]), pack_h2(v[3], v[7]));
 }
 
 // v[0..7] per lane -> the warp sum of v[(lane >> 2) & 7], in every lane of the
@@ -335,7 +302,6 @@ MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int n
 // E <= 256 and a bf16-exact activation (the tensor-core loops).
 template <int TMAX, bool Q4, bool FAST, int NCH>
 __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
-  constexpr bool H16 = false;                // (generic instances only)
   constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;                  // 4-bit tensor-core loop
   constexpr bool Q4MC = Q4C && TMAX >= 4;           // 4-bit: tensor-core down projection
@@ -570,8 +536,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // tid = (8w + kp) * 4 + q, the fragments of steps 2kp and 2kp + 1.
   // Other shapes: fp32 rows.  All reads of the source precede the barrier,
   // all writes follow it.
-  uint32_t xb[1][4];  // (generic instances only)
-  uint32_t xh[1][4];
   if constexpr (FAST) {
     uint32_t fr[TMAX][4];
     const int w = tid >> 5, kp = (tid >> 2) & 7, q = tid & 3;
@@ -1123,20 +1087,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
                   if (!(mrow[r] >> t & 1u)) continue;
-                  float xv[8];
-                  if (FAST) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                      xv[2 * e] = bf16_lo(xb[FAST && !Q4 ? t : 0][e]);
-                      xv[2 * e + 1] = bf16_hi(xb[FAST && !Q4 ? t : 0][e]);
-                    }
-                  } else {
-                    const float4* xp =
-                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
-                    const float4 a = xp[0], b = xp[1];
-                    xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-                    xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
-                  }
+                  const float4* xp =
+                      reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
+                  const float4 a = xp[0], b = xp[1];
+                  const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                   float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
@@ -1152,38 +1106,21 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
                 const uint32_t qg = wgq[Q4 ? r : 0][k], qu = wuq[Q4 ? r : 0][k];
                 const float dg = __half2float(__ushort_as_half(sgq[Q4 ? r : 0][k]));
                 const float du = __half2float(__ushort_as_half(suq[Q4 ? r : 0][k]));
-                if (H16) {
-                  uint32_t hg[4], hu[4];
-                  dequant_quarter(qg, hg);
-                  dequant_quarter(qu, hu);
 #pragma unroll
-                  for (int t = 0; t < TMAX; ++t) {
-                    if (!(mrow[r] >> t & 1u)) continue;
-                    const uint32_t* xv = xh[FAST && Q4 ? t : 0];
-                    const uint32_t sg = h2_fma(hg[1], xv[1], h2_fma(hg[0], xv[0], 0u));
-                    const uint32_t tg = h2_fma(hg[3], xv[3], h2_fma(hg[2], xv[2], 0u));
-                    const uint32_t su = h2_fma(hu[1], xv[1], h2_fma(hu[0], xv[0], 0u));
-                    const uint32_t tu = h2_fma(hu[3], xv[3], h2_fma(hu[2], xv[2], 0u));
-                    ga[t] = fmaf(dg, h2_sum(sg) + h2_sum(tg), ga[t]);
-                    ua[t] = fmaf(du, h2_sum(su) + h2_sum(tu), ua[t]);
+                for (int t = 0; t < TMAX; ++t) {
+                  if (!(mrow[r] >> t & 1u)) continue;
+                  const float4* xp =
+                      reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
+                  const float4 a = xp[0], b = xp[1];
+                  const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                  float sg = 0.f, su = 0.f;
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    sg = fmaf(nib_f32(qg, e), xv[e], sg);
+                    su = fmaf(nib_f32(qu, e), xv[e], su);
                   }
-                } else {
-#pragma unroll
-                  for (int t = 0; t < TMAX; ++t) {
-                    if (!(mrow[r] >> t & 1u)) continue;
-                    const float4* xp =
-                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + (size_t)t * H + 8 * ch);
-                    const float4 a = xp[0], b = xp[1];
-                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    float sg = 0.f, su = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                      sg = fmaf(nib_f32(qg, e), xv[e], sg);
-                      su = fmaf(nib_f32(qu, e), xv[e], su);
-                    }
-                    ga[t] = fmaf(dg, sg, ga[t]);
-                    ua[t] = fmaf(du, su, ua[t]);
-                  }
+                  ga[t] = fmaf(dg, sg, ga[t]);
+                  ua[t] = fmaf(du, su, ua[t]);
                 }
               }
             }
@@ -1374,9 +1311,39 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   }
 }
 
+// Per device, once per instance and shared-memory size: the kernel's dynamic
+// shared-memory limit, and a check that one block fits on an SM next to
+// nothing else of this kernel -- the combine's grid barrier needs all G
+// blocks (G <= the SM count) resident at once.  A launch whose blocks could
+// not all be resident is refused (cudaErrorCooperativeLaunchTooLarge) instead
+// of ending in a timed-out barrier.
+template <typename Kern>
+inline cudaError_t rows_configure(Kern kern, int smem, int G) {
+  constexpr int kDevs = 64;
+  static std::atomic<int> done_smem[kDevs];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
+  if (done_smem[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done_smem[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0, sms = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, smem);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  if ((long long)per_sm * sms < G) return cudaErrorCooperativeLaunchTooLarge;
+  done_smem[dev].store(smem, std::memory_order_release);
+  return cudaSuccess;
+}
+
 template <int TMAX, bool Q4, bool FAST, int NCH = 1>
 inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(k_rows<TMAX, Q4, FAST, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+  cudaError_t err = rows_configure(k_rows<TMAX, Q4, FAST, NCH>, p.smem, p.G);
   if (err != cudaSuccess) return err;
   err = launch_route(p, stream);
   if (err != cudaSuccess) return err;

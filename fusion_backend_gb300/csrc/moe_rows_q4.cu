@@ -1,4 +1,5 @@
-// Row kernel instances: 4-bit weights with fp16 products, H = 2048
+// Row kernel instances: 4-bit weights on the tensor cores (codes decoded to
+// exact bf16 fragments, block scales applied in fp32), H = 2048
 // (T <= 1, 2, 4, 8).
 #include "moe_rows.cuh"
 

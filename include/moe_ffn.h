@@ -127,6 +127,9 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
  *                 H-element rows: gate and up are [out,in]; downT is the down
  *                 projection stored transposed (row i holds the weights from
  *                 intermediate unit i to all H outputs)
+ *                 A caller holding the usual down[H,I] matrix passes its
+ *                 transpose; with 4-bit weights it quantises that transpose
+ *                 row by row, so down's blocks of 32 run along H.
  *   shexp_w       gate[Is,H] | up[Is,H] | downT[Is,H]
  *   shexp_gate_w  bf16 [H]
  *   out           fp32 [T,H]; may alias x exactly (the layer reads all of x

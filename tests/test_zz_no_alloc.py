@@ -4,8 +4,12 @@ It exists for callers that cannot allocate device memory (a library embedded
 in a runtime that already owns all free device memory, or a plugin given no
 allocator): instead of a caller workspace it uses one device array inside the
 library.  Here it is called through the C ABI and its output is compared with
-moe_ffn_execute's on the same inputs, for two calls in a row, with the
-tolerance of the other parity tests (max|d| <= 1e-2 rms + 1e-5).
+moe_ffn_execute's on the same inputs, for two calls in a row on different
+tokens.  Both run the same deterministic kernels, so the outputs must be equal
+bit for bit (a stale or misplaced scratch region would show up there); the
+parity tests' tolerance (max|d| <= 1e-2 rms + 1e-5) is checked as well.  The
+cases cover the decode path and the batched path (grouped GEMMs whose tensor
+maps then point into the library's array), with bf16 and 4-bit weights.
 
 This file is collected last on purpose, and passes both alone in a fresh
 process and after the rest of the suite.
@@ -34,7 +38,8 @@ def _tol_ok(got, ref):
 
 @pytest.mark.parametrize(
     "base,T,act,wfmt",
-    [(TINY, 2, ACT_F32, WFMT_BF16), (DECODE, 1, ACT_BF16, WFMT_BF16), (DECODE, 8, ACT_BF16, WFMT_Q4B32)],
+    [(TINY, 2, ACT_F32, WFMT_BF16), (DECODE, 1, ACT_BF16, WFMT_BF16), (DECODE, 8, ACT_BF16, WFMT_Q4B32),
+     (DECODE, 64, ACT_BF16, WFMT_BF16), (DECODE, 64, ACT_BF16, WFMT_Q4B32)],
 )
 def test_static_scratch_matches_workspace_entry_point(base, T, act, wfmt):
     import fusion_backend_gb300 as fb
@@ -54,7 +59,9 @@ def test_static_scratch_matches_workspace_entry_point(base, T, act, wfmt):
         fb.moe_ffn_execute(plan, ws, xd, dl.router_w, dl.expert_w, dl.shexp_w, dl.gate_w, ref)
         fb.moe_ffn_execute_static_scratch(plan, xd, dl.router_w, dl.expert_w, dl.shexp_w, dl.gate_w, got)
         torch.cuda.synchronize()
-        ok, err, rms = _tol_ok(got.cpu().numpy(), ref.cpu().numpy())
+        g, r = got.cpu().numpy(), ref.cpu().numpy()
+        assert g.tobytes() == r.tobytes(), f"call {call}: outputs differ bitwise"
+        ok, err, rms = _tol_ok(g, r)
         assert ok, f"call {call}: max|d| {err:.3e} vs rms {rms:.3e}"
     fb.moe_ffn_destroy(plan)
 
