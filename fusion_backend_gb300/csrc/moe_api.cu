@@ -255,7 +255,7 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
     L.x_perm = off;
     off = align256(off + (dtype.wfmt == MOE_FFN_W_Q4B32 ? TK + T : TK) * H * 2);
     L.h_ws = off;
-    off = align256(off + (TK + T) * hw * 2);
+    off = align256(off + (TK + T) * hw * 2 * (dtype.wfmt == MOE_FFN_W_Q4B32 ? 1 : 2));
     L.y_ws = off;
     off = align256(off + (TK + T) * H * 4);
   }

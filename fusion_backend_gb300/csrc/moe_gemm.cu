@@ -9,11 +9,14 @@
 //   gate / up (PHASE 0):  [G; U] = [W_g; W_u] X^T over K = H: 64 rows of I
 //     of the gate matrix over the same 64 rows of the up matrix form one
 //     128-row A tile, so one accumulator holds both; h = silu(G) * U *
-//     w(slot), stored as bf16 rows h_ws[slot][hw].
-//   down (PHASE 1):  Y^T = downT^T H^T over K = I (Is for the shared expert),
-//     256 output columns per unit (two 128-column accumulators); the downT
-//     tile is the MN-major A operand, straight from its [I][H] rows;
-//     y_ws[slot][H] in fp32.
+//     w(slot), stored as two bf16 parts, hi = bf16(h) and lo = bf16(h - hi),
+//     in the rows h_ws[slot][2 hw] (hi in [0, hw), lo in [hw, 2 hw)).
+//   down (PHASE 1):  Y^T = downT^T (H_hi + H_lo)^T over K = I (Is for the
+//     shared expert), 256 output columns per unit (two 128-column
+//     accumulators); the downT tile is the MN-major A operand, straight from
+//     its [I][H] rows, and every K step runs once with each part of h, so h
+//     enters the products with about 16 significant bits instead of bf16's
+//     8; y_ws[slot][H] in fp32.
 //
 // Block roles: warp 0 lane 0 moves tiles with TMA into a ring of stages
 // (one or two 128 x 64 A tiles + an NC x 64 B tile, 128-byte swizzled);
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
         unit_of(u, w);
         const int nk = w.shared ? nk_s : nk_r;
         const int npad = (w.n + 15) & ~15;
-        const uint32_t bytes = kKSub * (kA + (uint32_t)npad * 128);
+        const uint32_t bytes = kKSub * (kA + (PHASE == 0 ? 1u : 2u) * (uint32_t)npad * 128);
         const CUtensorMap* m = w.shared ? &P.tm_w64_s : &P.tm_w64_e;
         const int I = w.shared ? P.Is : P.I;
         for (int kc = 0; kc < nk; ++kc) {
@@ -202,8 +205,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
             const int r = (w.e * 3 + 2) * I + kc * 64;
 #pragma unroll
             for (int q = 0; q < 4; ++q) tma_load_2d(slot + q * 8192, m, w.tile * 256 + 64 * q, r, &full[stage], pol_w);
-            for (int j = 0; j < npad; j += 16)
+            for (int j = 0; j < npad; j += 16) {
               tma_load_2d(slot + kA + j * 128, &P.tm_h, kc * 64, w.brow0 + j, &full[stage], pol_x);
+              tma_load_2d(slot + kA + kGemmNC * 128 + j * 128, &P.tm_h, P.hw + kc * 64, w.brow0 + j, &full[stage],
+                          pol_x);
+            }
           }
           if (++stage == kS) {
             stage = 0;
@@ -250,8 +256,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
             if (PHASE == 0) {
               umma(tmem, smem_desc(sub + (ks & 3) * 32, 16, 1024), bd, idesc, acc);
             } else {
-              umma(tmem, smem_desc(sa + ks * 2048, 8192, 1024), bd, idesc, acc);
-              umma(tmem + kGemmNC, smem_desc(sa + 16384 + ks * 2048, 8192, 1024), bd, idesc, acc);
+              // h hi, then h lo, into each of the two column halves
+              const uint64_t bl = smem_desc(sub + kA + kGemmNC * 128 + (ks & 3) * 32, 16, 1024);
+              const uint64_t a0 = smem_desc(sa + ks * 2048, 8192, 1024), a1 = smem_desc(sa + 16384 + ks * 2048, 8192, 1024);
+              umma(tmem, a0, bd, idesc, acc);
+              umma(tmem, a0, bl, idesc, 1u);
+              umma(tmem + kGemmNC, a1, bd, idesc, acc);
+              umma(tmem + kGemmNC, a1, bl, idesc, 1u);
             }
           }
           umma_commit(&empty[stage]);
@@ -313,7 +324,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_gemm(const __grid_constant_
                 const int slot = w.slot0 + j;
                 const float g = exch[j * 64 + r], up = __uint_as_float(v[jj]);
                 const float h = g / (1.0f + expf(-g)) * up * P.slot_w[slot];
-                P.h_ws[(size_t)slot * (size_t)P.hw + i] = float_to_bf16_rne(h);
+                const uint16_t hi = float_to_bf16_rne(h);
+                uint16_t* row = P.h_ws + (size_t)slot * (size_t)(2 * P.hw);
+                row[i] = hi;
+                row[P.hw + i] = float_to_bf16_rne(h - bf16_to_float(hi));
               }
             }
           }
@@ -412,7 +426,7 @@ cudaError_t batch_tensor_maps(BatchParams& p) {
   if (!encode_2d(fn, &p.tm_w64_e, p.expert_w, er, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_w64_s, p.shexp_w, sr, p.H, 64, 64) ||
       !encode_2d(fn, &p.tm_xp, p.x_perm, TK, p.H, 64, 16) || !encode_2d(fn, &p.tm_x, p.x, p.T, p.H, 64, 16) ||
-      !encode_2d(fn, &p.tm_h, p.h_ws, TK + p.T, p.hw, 64, 16))
+      !encode_2d(fn, &p.tm_h, p.h_ws, TK + p.T, 2 * p.hw, 64, 16))
     return cudaErrorInvalidValue;
   return cudaSuccess;
 }

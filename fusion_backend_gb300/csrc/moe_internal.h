@@ -106,8 +106,9 @@ struct BatchParams {
   int32_t* slot_of;   // [T][K] slot (row of the expert-sorted order) of each choice
   float* slot_w;      // [T K + T] weight of each slot (routed p, then the shared gate per token)
   uint16_t* x_perm;   // [T K][H] bf16, x of each routed slot (4-bit weights: [T K + T][H] fp16)
-  uint16_t* h_ws;     // [T K + T][hw] bf16, h of each slot (weight applied)
-  int hw;             // h_ws row length: max(I, Is)
+  uint16_t* h_ws;     // h of each slot (weight applied): bf16 weights [T K + T][2 hw], the bf16 hi part in
+                      // columns [0, hw) and the bf16 lo part (h - hi) in [hw, 2 hw); 4-bit [T K + T][hw] fp16
+  int hw;             // h values per slot: max(I, Is)
   float* y_ws;        // [T K + T][H] fp32, expert output of each slot
   int32_t* r_counts;  // [E]
   int32_t* r_offsets; // [E + 1]
@@ -141,10 +142,11 @@ constexpr int kBatchLaunches = 6;
 // Ring depth and stage bytes of the GEMM kernels: gate / up stages hold
 // kGemmKSub0 pairs of a 128 x 64 A tile (64 gate rows over 64 up rows) and
 // an NC x 64 B tile;
-// down stages two 128 x 64 A tiles (MN-major) and an NC x 64 B tile.
+// down stages two 128 x 64 A tiles (MN-major) and two NC x 64 B tiles (the
+// bf16 hi and lo parts of h).
 constexpr int kGemmKSub0 = 2;  // gate / up: 64-wide K sub-chunks per stage (256 bytes of each weight row)
 constexpr int kGemmStages0 = 4, kGemmStageBytes0 = kGemmKSub0 * (128 * 128 + kGemmNC * 128);
-constexpr int kGemmStages1 = 5, kGemmStageBytes1 = 2 * 128 * 128 + kGemmNC * 128;
+constexpr int kGemmStages1 = 4, kGemmStageBytes1 = 2 * 128 * 128 + 2 * kGemmNC * 128;
 constexpr int kGemmExch = 64 * kGemmNC * 4;  // gate / up epilogue: the gate half of the accumulator
 constexpr int kGemmSmem0 = kGemmStages0 * kGemmStageBytes0 + kGemmExch + 1024 + 256;
 constexpr int kGemmSmem1 = kGemmStages1 * kGemmStageBytes1 + 1024 + 256;

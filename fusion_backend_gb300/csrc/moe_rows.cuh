@@ -1317,8 +1317,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 // blocks (G <= the SM count) resident at once.  A launch whose blocks could
 // not all be resident is refused (cudaErrorCooperativeLaunchTooLarge) instead
 // of ending in a timed-out barrier.
-template <typename Kern>
-inline cudaError_t rows_configure(Kern kern, int smem, int G) {
+template <int TMAX, bool Q4, bool FAST, int NCH>
+inline cudaError_t rows_configure(int smem, int G) {
+  // one record per instance (the statics of each template instantiation)
+  auto* const kern = k_rows<TMAX, Q4, FAST, NCH>;
   constexpr int kDevs = 64;
   static std::atomic<int> done_smem[kDevs];
   static std::mutex mu;
@@ -1343,7 +1345,7 @@ inline cudaError_t rows_configure(Kern kern, int smem, int G) {
 
 template <int TMAX, bool Q4, bool FAST, int NCH = 1>
 inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
-  cudaError_t err = rows_configure(k_rows<TMAX, Q4, FAST, NCH>, p.smem, p.G);
+  cudaError_t err = rows_configure<TMAX, Q4, FAST, NCH>(p.smem, p.G);
   if (err != cudaSuccess) return err;
   err = launch_route(p, stream);
   if (err != cudaSuccess) return err;
