@@ -128,11 +128,11 @@ def token_batch(step_token: int, T: int) -> np.ndarray:
 
 def kernel_names(cfg: str, T: int) -> str:
     if cfg == "stack_q4":
-        return "k_rows (+ k_route) per layer, block form; duration = step time / layers"
+        return "k_rows per layer, block form; duration = step time / layers"
     if T > 8:
         return (("k_gemm_q4<0>, k_gemm_q4<1>" if cfg == "batched_q4" else "k_gemm<0>, k_gemm<1>")
                 + " (+ routing, gather, combine); duration = step time")
-    return "k_rows (+ k_route, programmatic dependent launch); duration = step time"
+    return "k_rows (one kernel per layer call, programmatic dependent launch); duration = step time"
 
 
 def roofline(bytes_per_step: float, ms_per_step: float, cfg: str, T: int):

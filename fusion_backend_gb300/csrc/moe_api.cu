@@ -1,6 +1,7 @@
 // C ABI of the fused MoE FFN layer: plan, validation, workspace layout and
 // launches.  See include/moe_ffn.h for the contract.
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -22,7 +23,7 @@ constexpr int kMaxDevices = 64;
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t ctrl, logits, partial, counts, offsets, perm, active, nactive, total;
+  size_t ctrl, sync, logits, partial, counts, offsets, perm, active, nactive, total;
   // batched path
   size_t ids, p, bitmap, slot_of, slot_w, x_perm, h_ws, y_ws, lbound;
 };
@@ -98,6 +99,7 @@ void fill_params(const moe_ffn_plan* plan, LayerParams& P, void* ws) {
   P.wfmt = plan->wfmt;
   uint8_t* w = static_cast<uint8_t*>(ws);
   P.ctrl = reinterpret_cast<uint32_t*>(w + plan->ws.ctrl);
+  P.sync = reinterpret_cast<RowSync*>(w + plan->ws.sync);
   P.logits = reinterpret_cast<float*>(w + plan->ws.logits);
   P.ls = (s.E + 1 + 3) / 4 * 4;
   P.partial = reinterpret_cast<float*>(w + plan->ws.partial);
@@ -234,6 +236,8 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   const size_t T = s.T, E = s.E, K = s.top_k;
   L.ctrl = off;
   off = align256(off + kCtrlWords * 4);
+  L.sync = off;
+  if (path == 0) off = align256(off + sizeof(RowSync));
   L.logits = off;
   off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
   L.partial = off;
@@ -303,8 +307,18 @@ int moe_ffn_read_status(moe_ffn_plan_t plan, const void* workspace, moe_ffn_stre
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_FFN_ERR_CUDA;
   const uint8_t* w = static_cast<const uint8_t*>(workspace);
-  if (cudaMemcpy(device_status, w + plan->ws.ctrl + kCtrlStatus * 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+  int32_t status = 0;
+  if (cudaMemcpy(&status, w + plan->ws.ctrl + kCtrlStatus * 4, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_FFN_ERR_CUDA;
+  if (status == 0 && plan->path == 0) {
+    // decode path: each block of the row kernel writes its own status slot
+    int32_t slots[kMaxGrid];
+    if (cudaMemcpy(slots, w + plan->ws.sync + offsetof(RowSync, status), sizeof(slots), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+      return MOE_FFN_ERR_CUDA;
+    for (int i = 0; i < kMaxGrid && status == 0; ++i) status = slots[i];
+  }
+  *device_status = status;
   return MOE_FFN_OK;
 }
 
@@ -421,9 +435,9 @@ extern "C" int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_strea
   void* scratch = nullptr;
   const int rc = static_scratch_address(&scratch);
   if (rc != MOE_FFN_OK) return rc;
-  // The router kernel of each call zeroes the control words before the row
-  // kernel of that call counts on them, so no part of the (shared, reused)
-  // array has to be cleared here.
+  // The kernels initialise on each call every word of the workspace that they
+  // count on (see RowSync and the batched path's router kernel), so no part
+  // of the (shared, reused) array has to be cleared here.
   return run(plan, stream, scratch, MOE_FFN_STATIC_SCRATCH_BYTES, x, router_w, expert_w, shexp_w, shexp_gate_w, out,
              nullptr, nullptr, 0, 0.f);
 }

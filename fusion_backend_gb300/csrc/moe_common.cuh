@@ -124,6 +124,18 @@ MOE_DEV uint32_t ld_acquire_gpu(const uint32_t* p) {
 MOE_DEV void red_release_gpu_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+MOE_DEV unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// With relaxed loads that observed other threads' release stores before it,
+// this fence makes the loads an acquire: later accesses see what those
+// threads wrote before their releases.
+MOE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ------------------------------------------------------- named barriers
 MOE_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {

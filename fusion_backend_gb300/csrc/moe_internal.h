@@ -21,9 +21,28 @@ constexpr int kMaxGrid = 192;            // row kernel blocks (one per SM, at mo
 constexpr int kStatusTimeout = -6;       // device status word: a bounded wait gave up
 constexpr int kXPitch = 4160;            // tensor-core loops: bytes per token row of x fragments (4 KB + 64)
 
-// Control words at the start of the workspace.  The router kernel of each
-// call zeroes them before the row kernel of that call reads them.
-enum : int { kCtrlStatus = 0, kCtrlDone = 1, kCtrlProbe = 2, kCtrlWords = 64 };
+// Control words at the start of the workspace.  The batched path's router
+// kernel zeroes them on each call before its later kernels use them; the
+// decode row kernel clears the status word on each call.
+enum : int { kCtrlStatus = 0, kCtrlProbe = 2, kCtrlWords = 64 };
+
+// Decode row kernel: its grid-wide synchronisation words (in the workspace,
+// after the control words).  The call's epoch e is one more than the value in
+// `epoch`, which every block reads after the wait on the previous kernel;
+// block c announces a barrier by storing e into its own slot of a flag array
+// (release), and a barrier is complete when every slot holds e.  Nothing has
+// to be reset between calls: each call overwrites every slot it waits on with
+// a value no earlier call stored (the previous call stored e - 1).  Block 0
+// advances `epoch` once all blocks have read it (after the first barrier).
+// Each block also writes its own status slot (0 or the timeout status) on
+// every call.
+struct RowSync {
+  unsigned long long epoch;
+  unsigned long long pad[15];
+  unsigned long long logits_ready[kMaxGrid];   // first barrier: the block's router logits are written
+  unsigned long long partial_ready[kMaxGrid];  // second barrier: the block's partial output is written
+  int32_t status[kMaxGrid];
+};
 
 struct LayerParams {
   // shapes
@@ -46,6 +65,7 @@ struct LayerParams {
 
   // workspace
   uint32_t* ctrl;
+  RowSync* sync;
   float* logits;   // [T][ls]: columns 0..E-1 router logits, column E the shared-gate logit
   int ls;          // logits row stride in floats: E + 1 rounded up to a multiple of 4
   float* partial;  // [G][T][H] per-block partial outputs
@@ -176,14 +196,9 @@ static_assert(kQ4Smem0 + 4608 <= 232448 && kQ4Smem1 + 4608 <= 232448, "shared me
 static_assert(kQ4Raw0 % 1024 == 0 && kQ4B0 % 1024 == 0 && kQ4Raw1 % 1024 == 0 && kQ4B1 % 1024 == 0,
               "swizzled stage alignment");
 
-// Router kernel (moe_route.cu): logits of all tokens, control words zeroed.
-// Launched behind the previous kernel of the stream with programmatic
-// stream serialisation.
-cudaError_t launch_route(const LayerParams& p, cudaStream_t stream);
-
-// The failure-path probe (moe_route.cu): one thread waits, bounded, on an
-// mbarrier phase that never completes (which = 0) or on a control word that
-// never reaches its target (which = 1), then records the timeout.
+// The failure-path probe (moe_probe.cu): one warp waits, bounded, on an
+// mbarrier phase that never completes (which = 0) or on a grid-barrier flag
+// slot that never receives its epoch (which = 1), then records the timeout.
 cudaError_t launch_probe_timeout(uint32_t* ctrl, int which, cudaStream_t stream);
 
 // Row kernel (moe_rows_*.cu).  rows_layout fills the layout fields and
@@ -193,6 +208,6 @@ int rows_layout(LayerParams& p);
 // cudaSuccess or an error.
 cudaError_t rows_tensor_maps(LayerParams& p);
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream);
-constexpr int kLaunchesPerExecute = 2;
+constexpr int kLaunchesPerExecute = 1;
 
 }  // namespace moe

@@ -14,6 +14,40 @@ namespace moe {
 
 static inline int tmax_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 
+// Bounded wait of one warp until every slot flags[0 .. G) holds `epoch`
+// (the grid-wide barriers of the decode row kernel; see RowSync).  The
+// lane's slots are polled with relaxed loads, all in flight together, and an
+// acquire fence follows.  Gives up after about a second (the global timer,
+// and an iteration cap in case it does not advance); returns false on every
+// lane then.
+MOE_DEV bool grid_flags_wait(const unsigned long long* flags, int G, unsigned long long epoch) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = (kMaxGrid + 31) / 32;
+  uint32_t pending = 0u;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < G) pending |= 1u << i;
+  bool ok = true;
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0; pending; ++it) {
+    unsigned long long v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) v[i] = (pending >> i & 1u) ? ld_relaxed_gpu_u64(flags + lane + 32 * i) : epoch;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (v[i] == epoch) pending &= ~(1u << i);
+    if (!pending) break;
+    if (it == 32) t0 = global_ns();
+    if (it >= kSpinLimit || (it > 32 && (it & 15) == 0 && global_ns() - t0 > kWaitLimitNs)) {
+      ok = false;
+      break;
+    }
+    if (it > 32) __nanosleep(64);
+  }
+  fence_acq_rel_gpu();
+  return __all_sync(0xffffffffu, ok);
+}
+
 // -------------------------------------------------------------- reductions
 MOE_DEV float warp_sum(float v) {
 #pragma unroll

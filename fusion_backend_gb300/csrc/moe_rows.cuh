@@ -1,6 +1,7 @@
 #pragma once
-// Row kernel of the fused MoE FFN layer (decode path, T <= 8), sm_103a.
-// Instantiated by the moe_rows_*.cu units.
+// Row kernel of the fused MoE FFN layer (decode path, T <= 8), sm_103a: the
+// whole layer in one kernel per call.  Instantiated by the moe_rows_*.cu
+// units.
 //
 // Work unit: one intermediate index i of one expert group (the shared expert,
 // or a routed expert selected by some token).  Its weights are three
@@ -9,27 +10,33 @@
 //     y_t += w_t * silu(gate_i . x_t) * (up_i . x_t) * downT_i
 // to every token t the group serves (w_t = the routing weight p, or the
 // shared-expert gate s).  A block owns a contiguous run of units, so it needs
-// nothing from other blocks until its partial y is complete: the only
-// grid-wide step is the final fixed-order sum of the G partials.
+// nothing from other blocks but the routing until its partial y is complete.
 //
-// One persistent block of 8 warps per SM.  Weights stream through a ring of
-// `ns` stages of `rs` units, each stage three bulk copies (TMA engine) issued
-// by thread 0 on one mbarrier.  Per stage:
-//   A  warp r (< rows in the stage) forms the two dot products of unit r for
-//      its tokens and writes h_t = w_t silu(g_t) u_t to shared memory;
-//   -- one block barrier (after it, thread 0 refills the slot of the
-//      previous stage) --
-//   C  every thread owns 8 (or 16) columns of y for all tokens and adds
-//      h_t * downT_r over the stage's rows, in row order.
-// The shared expert's stages are issued at kernel start, before the wait for
-// the router (weights do not depend on the previous kernel); the routed
-// stages follow once this block has computed the routing itself from the
-// router's logits.
-//
-// End: each block stores its partial y[T][H] (fp32), counts itself done on a
-// release counter, waits (bounded) for all G blocks, then sums the G partials
-// of its own output columns in block order and writes out (adding x_res in
-// the block form).  All orders are fixed, so results are bitwise repeatable.
+// One persistent block of 8 warps per SM (G blocks).  Before the wait on the
+// previous kernel (programmatic dependent launch; nothing produced by it is
+// read), each block loads its router row and issues the shared expert's
+// first stages -- weights are never written by a kernel that lets this one
+// start early.  After the wait:
+//   1. x (block form: x_res, and its RMSNorm factors) into shared memory;
+//   2. router: block c computes the logits of router row c (row E: the
+//      shared-gate vector) for all tokens with error-free sums, writes them
+//      and announces them (first grid-wide barrier);
+//   3. every block reads all logits, takes the top-k of each token (ties to
+//      the lower index) and the softmax weights, builds the active-expert
+//      tables, and issues its routed stages;
+//   4. stages: weights stream through a ring of `ns` stages of `rs` units
+//      (tensor copies issued by one thread on one mbarrier).  Per stage:
+//        A  the gate and up dot products of the stage's rows for all tokens
+//           (warp partials), then one block barrier;
+//        A2 h_t = w_t silu(g_t) u_t of each row from the warp partials;
+//        C  y[cols][tokens] += downT_r^T h over the stage's rows;
+//   5. end: each block stores its partial y[T][H] (fp32) and announces it
+//      (second grid-wide barrier); then each block sums the G partials of
+//      its own output columns in block order and writes out (adding x_res in
+//      the block form).  All orders are fixed, so results are bitwise
+//      repeatable.
+// The grid-wide barriers use per-block flag slots tagged with the call's
+// epoch (RowSync), so no workspace word has to be reset between calls.
 //
 // Tensor-core instances (H = 2048, bf16-exact activation): the stage loops
 // run on mma.m16n8k16 / m16n8k8 over the swizzled tensor-copy boxes.  With
@@ -344,7 +351,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   uint8_t* dring = sm + P.off_dring + ring_pad;  // tensor-core path: downT boxes
   const uint64_t pol = policy_evict_first();
 
-  // The next call's router blocks may become resident beside this block.
+  // The next kernel of the stream (the next call's row kernel) may start its
+  // blocks as soon as this kernel's blocks leave an SM.
   pdl_launch_dependents();
 
   // Units of this block: groups of RS consecutive rows of one expert (the
@@ -466,8 +474,30 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       if (tid == 0) issue_d(cd);
     }
 
-  // ---- the router's logits, the activation and (block form) x_res are ready
+  // Router row of this block (row cta of router_w; row E is the shared-gate
+  // vector), read before the wait: the weights are never written by a kernel
+  // that lets this one start early (only this kernel does, and it writes no
+  // weights; any other predecessor has completed before this kernel starts).
+  constexpr int kRC = kMaxH / (kRowThreads * 8);  // 8-element chunks of a row per thread
+  uint4 wr[kRC];
+  {
+    const uint16_t* w = cta < P.E ? P.router_w + (size_t)cta * H : P.gate_w;
+#pragma unroll
+    for (int q = 0; q < kRC; ++q) {
+      const int c0 = 8 * tid + kRowThreads * 8 * q;
+      wr[q] = (cta <= P.E && c0 < H) ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  // ---- the activation (block form: x_res) and the workspace belong to this
+  // kernel from here on
   pdl_wait();
+  RowSync* const sync = P.sync;
+  const unsigned long long epoch = __ldcg(&sync->epoch) + 1ull;
+  if (cta == 0) {
+    if (tid == 0) P.ctrl[kCtrlStatus] = 0u;  // a status left by the failure-path probe
+    for (int c = P.G + tid; c < kMaxGrid; c += kRowThreads) sync->status[c] = 0;
+  }
   // The activation (or x_res) of all tokens: one bulk copy per block into
   // shared memory -- every block needs all of it, and one read per block
   // keeps the L2 lines of x from being hammered by every warp of the grid.
@@ -477,65 +507,91 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     mbar_arrive_expect_tx(xbar, bytes);
     bulk_g2s(xs, P.x, bytes, xbar, policy_evict_last());
   }
-  // routing, every block from the router's logits: top-k of token t on warp
-  // 7 - t (the chosen experts, their softmax weights and their bits in the
-  // selection bitmap) and the shared gate sigmoid(logit_E)
-  {
-    const int t = kRowWarps - 1 - warp;
-    if (t < T) {
-      float sl = 0.f;
-      if (lane == 0) sl = __ldcg(P.logits + (size_t)t * P.ls + P.E);
-      warp_topk<EPL>(P.logits + (size_t)t * P.ls, P.E, K, tb.ids + t * K, tb.p + t * K);
-      if (lane < K) {
-        const int e = tb.ids[t * K + lane];
-        atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
-      }
-      if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-sl));
-    }
-  }
-  if (!mbar_wait(xbar, 0)) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  bool timed_out = false;
+  if (!mbar_wait(xbar, 0)) timed_out = true;
   // block form: RMSNorm factors of the fp32 rows, all warps (scratch: the
-  // partials region, unused before the stage loop)
+  // partials region, unused before the stage loop; ends with a barrier)
   if (P.block_mode)
     block_norm_factors(reinterpret_cast<const float*>(xs), T, H, P.eps, reinterpret_cast<float*>(sm + P.off_part),
                        tb.inv, kRowWarps);
-  __syncthreads();
-  if (warp == 0) {
-    // active experts in ascending order (active index u): bitmap word l on
-    // lane l, an exclusive scan of the word counts
-    const int nw = (P.E + 31) / 32;
-    const uint32_t w = lane < nw ? tb.bitmap[lane] : 0u;
-    const int c = __popc(w);
-    int incl = c;
+  // ---- router logits of this block's rows r = cta, cta + G, ... (<= E):
+  // logit[t][r] = sum_h W[r,h] x_t[h], accumulated error-free (TwoSum of the
+  // exact bf16 x bf16 products, TwoProduct for fp32 x) so that the fp32 logit
+  // is the exact dot product rounded once (up to a residual far below fp32
+  // resolution) and the top-k decision does not depend on any summation
+  // order.  The block's 8 warps reduce in warp order.
+  {
+    float* red = reinterpret_cast<float*>(sm + P.off_part);  // [kRowWarps][TMAX][2]
+    const bool exact_products = P.block_mode || P.act == 1;   // bf16 x bf16 is exact in fp32
+    for (int r = cta, j = 0; r <= P.E; r += P.G, ++j) {
+      if (j > 0) {
+        const uint16_t* w = r < P.E ? P.router_w + (size_t)r * H : P.gate_w;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int U = __shfl_sync(0xffffffffu, incl, 31);
-    int u = incl - c;
-    for (uint32_t m = w; m; m &= m - 1u, ++u) {
-      const int e = 32 * lane + __ffs((int)m) - 1;
-      tb.active[u] = e;
-      tb.inv_u[e] = static_cast<int16_t>(u);
-    }
-    __syncwarp();
-    // tokens of every active expert and their weights
-    for (int t = 0; t < T; ++t)
-      for (int k = lane; k < K; k += 32) {
-        const int ts = t * K + k;
-        const int ua = tb.inv_u[tb.ids[ts]];
-        atomicOr(&tb.mask[ua], 1u << t);
-        tb.wt[ua * T + t] = tb.p[ts];
+        for (int q = 0; q < kRC; ++q) {
+          const int c0 = 8 * tid + kRowThreads * 8 * q;
+          wr[q] = c0 < H ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
+        }
       }
-    if (lane == 0) tb.misc[0] = U;
+      float sa[TMAX], ca[TMAX];
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) sa[t] = ca[t] = 0.f;
+#pragma unroll
+      for (int q = 0; q < kRC; ++q) {
+        const int c0 = 8 * tid + kRowThreads * 8 * q;
+        if (c0 >= H) break;
+        const uint4 wv = wr[q];
+        const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t >= T) break;
+          float xf[8];
+          x8_from_smem(xs + (size_t)t * H * (src4 ? 4 : 2), src4, P.block_mode, P.block_mode ? tb.inv[2 * t] : 0.f,
+                       P.block_mode ? tb.inv[2 * t + 1] : 0.f, c0, xf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float pr, e1 = 0.f, tt, e2;
+            if (exact_products)
+              pr = __fmul_rn(wf[e], xf[e]);
+            else
+              two_prod(wf[e], xf[e], pr, e1);
+            two_sum(sa[t], pr, tt, e2);
+            sa[t] = tt;
+            ca[t] = __fadd_rn(ca[t], __fadd_rn(e1, e2));
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        warp_sum2(sa[t], ca[t]);
+        if (lane == 0) {
+          red[(warp * TMAX + t) * 2] = sa[t];
+          red[(warp * TMAX + t) * 2 + 1] = ca[t];
+        }
+      }
+      __syncthreads();
+      if (tid < T) {
+        float S = red[tid * 2], C = red[tid * 2 + 1];
+        for (int w = 1; w < kRowWarps; ++w) {
+          float tt, e;
+          two_sum(S, red[(w * TMAX + tid) * 2], tt, e);
+          S = tt;
+          C = __fadd_rn(__fadd_rn(C, red[(w * TMAX + tid) * 2 + 1]), e);
+        }
+        __stcg(P.logits + (size_t)tid * P.ls + r, __fadd_rn(S, C));
+      }
+      __syncthreads();
+    }
   }
-  // activation in its compute form, in place.  Fast shapes: the bf16 A
-  // fragments of the tensor-core loops, token t's row at t * kXPitch, 16
-  // bytes per (warp slice w, 32-column block kp, lane quad q) -- unit
-  // tid = (8w + kp) * 4 + q, the fragments of steps 2kp and 2kp + 1.
-  // Other shapes: fp32 rows.  All reads of the source precede the barrier,
-  // all writes follow it.
+  // this block's logits are written: announce it (the barrier before orders
+  // every thread's stores before thread 0's release)
+  if (tid == 0) st_release_gpu_u64(&sync->logits_ready[cta], epoch);
+  // activation in its compute form, in place, while the other blocks finish
+  // their logits.  Fast shapes: the bf16 A fragments of the tensor-core
+  // loops, token t's row at t * kXPitch, 16 bytes per (warp slice w, 32-column
+  // block kp, lane quad q) -- unit tid = (8w + kp) * 4 + q, the fragments of
+  // steps 2kp and 2kp + 1.  Other shapes: fp32 rows.  All reads of the source
+  // precede the barrier, all writes follow it.
   if constexpr (FAST) {
     uint32_t fr[TMAX][4];
     const int w = tid >> 5, kp = (tid >> 2) & 7, q = tid & 3;
@@ -590,6 +646,59 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         dst[1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
       }
     }
+  }
+  // ---- every block's logits: warp 0 waits (bounded) until each block's
+  // slot holds this call's epoch
+  if (warp == 0 && !grid_flags_wait(sync->logits_ready, P.G, epoch)) timed_out = true;
+  __syncthreads();
+  // every block has read the epoch (before its announcement): advance it
+  if (cta == 0 && tid == 0) sync->epoch = epoch;
+  // routing, every block from all logits: top-k of token t on warp 7 - t
+  // (the chosen experts, their softmax weights and their bits in the
+  // selection bitmap) and the shared gate sigmoid(logit_E)
+  {
+    const int t = kRowWarps - 1 - warp;
+    if (t < T) {
+      float sl = 0.f;
+      if (lane == 0) sl = __ldcg(P.logits + (size_t)t * P.ls + P.E);
+      warp_topk<EPL>(P.logits + (size_t)t * P.ls, P.E, K, tb.ids + t * K, tb.p + t * K);
+      if (lane < K) {
+        const int e = tb.ids[t * K + lane];
+        atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
+      }
+      if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-sl));
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // active experts in ascending order (active index u): bitmap word l on
+    // lane l, an exclusive scan of the word counts
+    const int nw = (P.E + 31) / 32;
+    const uint32_t w = lane < nw ? tb.bitmap[lane] : 0u;
+    const int c = __popc(w);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int U = __shfl_sync(0xffffffffu, incl, 31);
+    int u = incl - c;
+    for (uint32_t m = w; m; m &= m - 1u, ++u) {
+      const int e = 32 * lane + __ffs((int)m) - 1;
+      tb.active[u] = e;
+      tb.inv_u[e] = static_cast<int16_t>(u);
+    }
+    __syncwarp();
+    // tokens of every active expert and their weights
+    for (int t = 0; t < T; ++t)
+      for (int k = lane; k < K; k += 32) {
+        const int ts = t * K + k;
+        const int ua = tb.inv_u[tb.ids[ts]];
+        atomicOr(&tb.mask[ua], 1u << t);
+        tb.wt[ua * T + t] = tb.p[ts];
+      }
+    if (lane == 0) tb.misc[0] = U;
   }
   __syncthreads();
   const int U = tb.misc[0];
@@ -661,7 +770,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr int NV = 2 * RSM * TMAX;  // dot values per warp per stage: (row, gate|up, token)
   float* part = reinterpret_cast<float*>(sm + P.off_part);  // [2][kRowWarps][NV]
   float* hb = reinterpret_cast<float*>(sm + P.off_h);       // [2][RSM][TMAX]
-  bool timed_out = false;
   float y[TMAX][NCH][8];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t)
@@ -1206,10 +1314,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       if (s + 1 <= n_stages) step(std::integral_constant<int, 1>(), s + 1);
     }
   }
-  if (__syncthreads_or(timed_out) && tid == 0) {
+  const bool block_timed_out = __syncthreads_or(timed_out);
+  if (block_timed_out && tid == 0) {
     // leave no copy in flight into this block's shared memory: wait (bounded)
     // once more for the last stages issued
-    atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
     for (int s = max(0, n_stages - NS); s < n_stages; ++s) mbar_wait(&full[s % NS], (uint32_t)(s / NS) & 1u);
     for (int s = max(0, n_stages - P.nsd); s < n_stages; ++s) mbar_wait(&fulld[s % P.nsd], (uint32_t)(s / P.nsd) & 1u);
   }
@@ -1258,22 +1366,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   }
   // every block's partial, then the sum of this block's columns: the block
   // barrier orders all threads' stores before thread 0's release (a
-  // cumulative release at GPU scope), and its acquire orders every other
-  // block's stores before this block's reads
+  // cumulative release at GPU scope), and warp 0's acquire orders every
+  // other block's stores before this block's reads
   __syncthreads();
-  if (tid == 0) {
-    red_release_gpu_add(&P.ctrl[kCtrlDone], 1u);
-    bool ok = false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-      if (ld_acquire_gpu(&P.ctrl[kCtrlDone]) >= (uint32_t)P.G) {
-        ok = true;
-        break;
-      }
-      if (i > 256) __nanosleep(32);
-    }
-    if (!ok) atomicExch(reinterpret_cast<int*>(&P.ctrl[kCtrlStatus]), kStatusTimeout);
+  if (tid == 0) st_release_gpu_u64(&sync->partial_ready[cta], epoch);
+  bool tail_timed_out = false;
+  if (warp == 0 && !grid_flags_wait(sync->partial_ready, P.G, epoch)) tail_timed_out = true;
+  if (__syncthreads_or(tail_timed_out) || block_timed_out) {
+    if (tid == 0) sync->status[cta] = kStatusTimeout;
+  } else if (tid == 0) {
+    sync->status[cta] = 0;
   }
-  __syncthreads();
   // This block's output columns [da, db) for all tokens: O sums of G
   // partials.  Thread (sp, o) adds partials sp, sp + S, ... in order, all
   // loads in flight together; the S part sums are then added in order.
@@ -1346,8 +1449,6 @@ inline cudaError_t rows_configure(int smem, int G) {
 template <int TMAX, bool Q4, bool FAST, int NCH = 1>
 inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
   cudaError_t err = rows_configure<TMAX, Q4, FAST, NCH>(p.smem, p.G);
-  if (err != cudaSuccess) return err;
-  err = launch_route(p, stream);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

@@ -14,8 +14,12 @@ near-tie positions (k-th and (k+1)-th oracle logits closer than 1e-3), which
 are counted and reported; there the GPU's choice must still be a valid top-k
 of the oracle's logits up to that gap.  Every layer's output (the residual
 increment) must be within max|d| <= 1e-2 rms(oracle) + 1e-5.  Finally the
-GPU's free-running output is compared with the oracle's own free-running
-stack, token by token, and the relative rms drift is reported.
+GPU's free-running stack is compared with the oracle's own free-running
+stack: the two must agree closely up to the first layer where their routing
+differs, that layer must be a near-tie on the oracle's side, and the relative
+rms drift of every token's output is reported (after a routing difference the
+two trajectories part: bf16 rounding of the normalised input and the discrete
+top-k make the stack chaotic).
 """
 
 from __future__ import annotations
@@ -77,58 +81,83 @@ def test_stack_teacher_forced_and_drift(stack):
 
     layers, dev = stack
     s1 = with_T(DECODE, 1)
+    k = DECODE.top_k
     m = fb.MoeFFN(s1, ACT_BF16, WFMT_Q4B32)
     x0 = datagen.normal_f32(SEED, 7, DECODE.H).reshape(1, DECODE.H)
     xd = torch.from_numpy(x0.copy()).cuda()
-    ids = torch.full((1, DECODE.top_k), -1, dtype=torch.int32, device="cuda")
+    # the GPU's free-running trajectory: x_res and ids after every layer of every token
+    g_x = torch.empty((DRIFT_TOKENS, N_LAYERS, DECODE.H), dtype=torch.float32, device="cuda")
+    g_ids = torch.full((DRIFT_TOKENS, N_LAYERS, k), -1, dtype=torch.int32, device="cuda")
     near_ties, exact = 0, 0
     worst = 0.0
-    gpu_tokens = []
     for n in range(DRIFT_TOKENS):
         for l in range(N_LAYERS):
             L, D = layers[l], dev[l]
             if n < TF_TOKENS:
                 x_in = xd.cpu().numpy()
-            m.block(xd, D.router_w, D.expert_w, D.shexp_w, D.gate_w, eps=EPS, topk_ids=ids)
+            m.block(xd, D.router_w, D.expert_w, D.shexp_w, D.gate_w, eps=EPS, topk_ids=g_ids[n, l].view(1, k))
+            g_x[n, l].copy_(xd[0])
             if n >= TF_TOKENS:
                 continue
+            # teacher-forced: the oracle's block step on the GPU's layer input
             torch.cuda.synchronize()
             assert m.status() == 0, f"token {n} layer {l}: device status"
             new_ref, ids_ref, xn_ref = oracle.block_step(s1, WFMT_Q4B32, x_in, L.router_w, L.expert_w, L.shexp_w,
                                                          L.shexp_gate_w, eps=EPS)
-            g_ids = ids.cpu().numpy()
+            gi = g_ids[n, l].view(1, k).cpu().numpy()
             lg = oracle.router_logits(L.router_w, DECODE.E, DECODE.H, _bf16_row_f64(xn_ref[0]))
-            if kth_gap(lg, DECODE.top_k) >= NEAR_TIE_GAP:
-                np.testing.assert_array_equal(g_ids, ids_ref, err_msg=f"token {n} layer {l}")
+            if kth_gap(lg, k) >= NEAR_TIE_GAP:
+                np.testing.assert_array_equal(gi, ids_ref, err_msg=f"token {n} layer {l}")
                 exact += 1
             else:
                 near_ties += 1
-                assert _valid_topk_within_gap(g_ids[0], lg, DECODE.top_k, NEAR_TIE_GAP), f"token {n} layer {l}"
+                assert _valid_topk_within_gap(gi[0], lg, k, NEAR_TIE_GAP), f"token {n} layer {l}"
             ok, err, rms = tolerance_ok(xd.cpu().numpy() - x_in, new_ref - x_in)
             worst = max(worst, err / rms)
             assert ok, f"token {n} layer {l}: max|d| {err:.3e} > 1e-2 * rms({rms:.3e}) + 1e-5"
-        torch.cuda.synchronize()
-        assert m.status() == 0
-        gpu_tokens.append(xd.cpu().numpy().copy())
+    torch.cuda.synchronize()
+    assert m.status() == 0
     m.close()
+    g_x = g_x.cpu().numpy().astype(np.float64)
+    g_ids = g_ids.cpu().numpy()
 
-    # the oracle's own free-running stack from the same first input
+    # The oracle's own free-running stack from the same first input.  The two trajectories agree closely until
+    # the routing first differs; that can only happen where the oracle's k-th and (k+1)-th logits are nearly
+    # tied (inputs that differ by rounding move logits by far less than the 1e-3 gap), and from there the
+    # trajectories part (a different expert changes the layer's output by a large fraction).
     x_ref = x0.copy()
+    first = None  # (token, layer, oracle gap) of the first routing difference
+    close = 0.0  # largest relative rms difference of x_res before it
     drift = []
+    ties_free = 0
     for n in range(DRIFT_TOKENS):
         for l in range(N_LAYERS):
             L = layers[l]
-            x_ref, _, _ = oracle.block_step(s1, WFMT_Q4B32, x_ref, L.router_w, L.expert_w, L.shexp_w,
-                                            L.shexp_gate_w, eps=EPS)
-        d = gpu_tokens[n].astype(np.float64) - x_ref.astype(np.float64)
+            x_ref, ids_ref, xn_ref = oracle.block_step(s1, WFMT_Q4B32, x_ref, L.router_w, L.expert_w, L.shexp_w,
+                                                       L.shexp_gate_w, eps=EPS)
+            lg = oracle.router_logits(L.router_w, DECODE.E, DECODE.H, _bf16_row_f64(xn_ref[0]))
+            gap = kth_gap(lg, k)
+            ties_free += gap < NEAR_TIE_GAP
+            if first is None:
+                if not np.array_equal(g_ids[n, l], ids_ref[0]):
+                    first = (n, l, gap)
+                else:
+                    d = g_x[n, l] - x_ref[0].astype(np.float64)
+                    close = max(close, float(np.sqrt(np.mean(d * d) / np.mean(x_ref.astype(np.float64) ** 2))))
+        d = g_x[n, N_LAYERS - 1] - x_ref[0].astype(np.float64)
         drift.append(float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(x_ref.astype(np.float64) ** 2))))
     print(f"\nstack: {TF_TOKENS} tokens x {N_LAYERS} layers teacher-forced: {exact} positions with ids equal bit for "
           f"bit, {near_ties} near-tie positions (gap < {NEAR_TIE_GAP}); worst layer max|d|/rms {worst:.2e}")
+    print(f"stack: free-running, {DRIFT_TOKENS} tokens: first routing difference "
+          f"{'none' if first is None else f'at token {first[0]} layer {first[1]} (oracle gap {first[2]:.2e})'}; "
+          f"largest relative rms difference of x_res before it {close:.2e}; {ties_free} near-tie positions on the "
+          f"oracle's trajectory")
     print("stack: free-running relative rms drift per token: " + " ".join(f"{v:.2e}" for v in drift))
     assert exact + near_ties == TF_TOKENS * N_LAYERS
     assert all(np.isfinite(drift))
-    # the first token's output went through the same 48 layers on both sides from the same input
-    assert drift[0] <= 1e-2, f"first-token drift {drift[0]:.3e}"
+    assert close <= 1e-4, f"trajectories differ by {close:.2e} before any routing difference"
+    if first is not None:
+        assert first[2] < NEAR_TIE_GAP, f"routing first differs at a clear decision: {first}"
 
 
 def test_block_form_bf16_weights_full_size():
