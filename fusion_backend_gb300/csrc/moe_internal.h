@@ -28,17 +28,31 @@ enum : int { kCtrlStatus = 0, kCtrlProbe = 2, kCtrlWords = 64 };
 
 // Decode row kernel: its grid-wide synchronisation words (in the workspace,
 // after the control words).  The call's epoch e is one more than the value in
-// `epoch`, which every block reads after the wait on the previous kernel;
-// block c announces a barrier by storing e into its own slot of a flag array
-// (release), and a barrier is complete when every slot holds e.  Nothing has
-// to be reset between calls: each call overwrites every slot it waits on with
-// a value no earlier call stored (the previous call stored e - 1).  Block 0
-// advances `epoch` once all blocks have read it (after the first barrier).
-// Each block also writes its own status slot (0 or the timeout status) on
-// every call.
+// `epoch`, which every block reads after the wait on the previous kernel.  A
+// barrier: block c stores e into its own slot of a flag array (release);
+// block 0 waits until every slot holds e, then stores e into the barrier's
+// `go` word (release); every block waits until `go` holds e.  Nothing has to
+// be reset between calls: each call overwrites every word it waits on with a
+// value no earlier call stored (the previous call stored e - 1).  Block 0
+// advances `epoch` once all blocks have read it (in the first barrier, after
+// it has seen every slot).  Each block also writes its own status slot (0 or
+// the timeout status) on every call.
+//
+// Fast path: once a call has run to its first barrier on this workspace, the
+// two arrival counters of the next call (count[e + 1 parity]) are zero --
+// block 0 clears them after that barrier, when no block of this call can
+// touch them -- and `sig` holds ~e.  A call that finds sig == ~epoch uses the
+// counters (each block adds one; a barrier is complete at G), one hop through
+// L2 instead of two; any other state (a workspace that another user
+// overwrote, or never initialised) takes the flag barrier, which needs no
+// prior state.  Both decisions are the same in every block: they read
+// `epoch` and `sig` before any block can change them.
 struct RowSync {
   unsigned long long epoch;
-  unsigned long long pad[15];
+  unsigned long long sig;
+  unsigned long long go[2];  // the two barriers' release words
+  uint32_t count[2][2];      // [call parity][barrier] arrival counters of the fast path
+  unsigned long long pad[10];
   unsigned long long logits_ready[kMaxGrid];   // first barrier: the block's router logits are written
   unsigned long long partial_ready[kMaxGrid];  // second barrier: the block's partial output is written
   int32_t status[kMaxGrid];

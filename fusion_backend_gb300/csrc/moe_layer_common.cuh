@@ -14,6 +14,20 @@ namespace moe {
 
 static inline int tmax_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 
+// Bounded wait of one thread until *word holds `epoch` (relaxed polls, then
+// an acquire fence); false when the bound (about a second) ran out.
+MOE_DEV bool word_wait(const unsigned long long* word, unsigned long long epoch) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (ld_relaxed_gpu_u64(word) == epoch) break;
+    if (it == 16) t0 = global_ns();
+    if (it >= kSpinLimit || (it > 16 && (it & 15) == 0 && global_ns() - t0 > kWaitLimitNs)) return false;
+    if (it > 16) __nanosleep(64);
+  }
+  fence_acq_rel_gpu();
+  return true;
+}
+
 // Bounded wait of one warp until every slot flags[0 .. G) holds `epoch`
 // (the grid-wide barriers of the decode row kernel; see RowSync).  The
 // lane's slots are polled with relaxed loads, all in flight together, and an
@@ -46,6 +60,56 @@ MOE_DEV bool grid_flags_wait(const unsigned long long* flags, int G, unsigned lo
   }
   fence_acq_rel_gpu();
   return __all_sync(0xffffffffu, ok);
+}
+
+// A grid-wide barrier of the decode row kernel (see RowSync), called by
+// every thread of every block after the block's writes that the barrier
+// publishes.  fast: each block adds one to *count (release) and waits until
+// it reaches G.  Otherwise block c stores `epoch` into flags[c] (release);
+// block 0's warp 0 waits for every slot and releases *go; every block waits
+// for *go.  first: the call's first barrier -- block 0 then (after every
+// block has arrived, hence has read RowSync's epoch and sig) clears the next
+// call's counters and advances epoch and sig.  Returns false in every thread
+// of the block when a wait gave up (bounded, about a second).
+MOE_DEV bool grid_barrier(RowSync* sy, int which, bool fast, int G, unsigned long long epoch, int cta, bool first) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  __syncthreads();
+  bool ok = true;
+  uint32_t* count = &sy->count[epoch & 1][which];
+  if (tid == 0) {
+    if (fast) {
+      red_release_gpu_add(count, 1u);
+      unsigned long long t0 = 0;
+      for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(count) >= (uint32_t)G) break;
+        if (it == 16) t0 = global_ns();
+        if (it >= kSpinLimit || (it > 16 && (it & 15) == 0 && global_ns() - t0 > kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        if (it > 16) __nanosleep(32);
+      }
+    } else {
+      st_release_gpu_u64((which ? sy->partial_ready : sy->logits_ready) + cta, epoch);
+    }
+  }
+  if (!fast && tid < 32) {
+    if (cta == 0) {
+      ok = grid_flags_wait(which ? sy->partial_ready : sy->logits_ready, G, epoch);
+      if (ok && lane == 0) st_release_gpu_u64(&sy->go[which], epoch);
+    }
+    if (ok && lane == 0) ok = word_wait(&sy->go[which], epoch);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  }
+  if (first && cta == 0 && tid == 0 && ok) {
+    // every block has read epoch and sig: prepare the next call's fast path
+    sy->count[(epoch + 1) & 1][0] = 0u;
+    sy->count[(epoch + 1) & 1][1] = 0u;
+    sy->epoch = epoch;
+    __threadfence();
+    sy->sig = ~epoch;
+  }
+  return !__syncthreads_or(!ok);
 }
 
 // -------------------------------------------------------------- reductions

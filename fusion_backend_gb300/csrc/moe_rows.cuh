@@ -51,6 +51,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstddef>
 #include <mutex>
 #include <type_traits>
 
@@ -315,23 +316,13 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
   extern __shared__ __align__(128) uint8_t sm[];
-  // The parameter block is read once into shared memory, before the wait on
-  // the router: later reads then never miss in the constant cache on the
-  // critical path.
-  __shared__ LayerParams sP;
+  // The parameter block is read in place (parameter space).  The set-up work
+  // before the wait on the previous kernel is split over the warps so that
+  // its pieces -- each short, and each first executed cold on every call --
+  // run side by side rather than one after the other.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x;
-  if (tid == 0) sP = Pk;
-  if constexpr (FAST) {
-    // descriptors of the routed maps are first used after the routing, under
-    // load: fetch all four now
-    if (tid == 32) prefetch_tensormap(&Pk.tm_gu_e);
-    if (tid == 64) prefetch_tensormap(&Pk.tm_d_e);
-    if (tid == 96) prefetch_tensormap(&Pk.tm_gu_s);
-    if (tid == 128) prefetch_tensormap(&Pk.tm_d_s);
-  }
-  __syncthreads();
-  const LayerParams& P = sP;
+  const LayerParams& P = Pk;
   const int T = P.T, K = P.K, TK = T * K;
   const int H = FAST ? 2048 : P.H;
   const int RS = P.rs, NS = P.ns;
@@ -429,41 +420,58 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   cursor_init(ci, NS);
   cursor_init(cd, P.nsd > 0 ? P.nsd : 1);
 
-  // ---- barriers, a cleared routing table, and the shared-expert stages
-  // issued before the wait (their weights do not depend on the previous
-  // kernel)
-  for (int i = tid; i < (P.E + 31) / 32; i += kRowThreads) tb.bitmap[i] = 0u;
-  for (int i = tid; i < TK; i += kRowThreads) tb.mask[i] = 0u;
-  for (int i = tid; i < TK * T; i += kRowThreads) tb.wt[i] = 0.f;
-  // the routed run of this block for every possible count U of active
-  // experts (K <= U <= min(E, T K)): groups [q0, q1) of the flattened
-  // (active expert, group) order, so that shared + routed groups are
-  // balanced over the blocks
-  for (int j = tid; j <= min(P.E, TK) - K; j += kRowThreads) {
-    const uint32_t R = (uint32_t)(K + j) * (uint32_t)gI, G = P.G, cc = cta;
-    uint32_t q0, q1;
-    if (R >= G) {
-      q0 = muldiv(R + gS, cc, G) - gs0;
-      q1 = muldiv(R + gS, cc + 1, G) - gs1;
-    } else {
-      q0 = muldiv(R, cc, G);
-      q1 = muldiv(R, cc + 1, G);
+  // ---- before the wait (nothing the previous kernel writes is read), side
+  // by side: warp 0 initialises the barriers and issues the shared expert's
+  // first stages (their weights do not depend on the previous kernel), warp 1
+  // clears the routing tables, warp 2 fills the per-U stage table, warp 3
+  // fetches the tensor-map descriptors; every thread loads its part of the
+  // block's router row.
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < NS; ++i) {
+        mbar_init(&full[i], 1);
+        scnt[i] = 0;
+      }
+      for (int i = 0; i < P.nsd; ++i) mbar_init(&fulld[i], 1);
+      mbar_init(xbar, 1);
+      mbar_fence_init();
     }
-    const uint32_t u0 = q0 / (uint32_t)gI;
-    tb.qtab[4 * j] = (int)(q1 - q0);
-    tb.qtab[4 * j + 1] = (int)u0;
-    tb.qtab[4 * j + 2] = (int)(q0 - u0 * (uint32_t)gI);
-  }
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&full[i], 1);
-      scnt[i] = 0;
+  } else if (warp == 1) {
+    for (int i = lane; i < (P.E + 31) / 32; i += 32) tb.bitmap[i] = 0u;
+    for (int i = lane; i < TK; i += 32) tb.mask[i] = 0u;
+    for (int i = lane; i < TK * T; i += 32) tb.wt[i] = 0.f;
+  } else if (warp == 2) {
+    // the routed run of this block for every possible count U of active
+    // experts (K <= U <= min(E, T K)): groups [q0, q1) of the flattened
+    // (active expert, group) order, so that shared + routed groups are
+    // balanced over the blocks
+    for (int j = lane; j <= min(P.E, TK) - K; j += 32) {
+      const uint32_t R = (uint32_t)(K + j) * (uint32_t)gI, G = P.G, cc = cta;
+      uint32_t q0, q1;
+      if (R >= G) {
+        q0 = muldiv(R + gS, cc, G) - gs0;
+        q1 = muldiv(R + gS, cc + 1, G) - gs1;
+      } else {
+        q0 = muldiv(R, cc, G);
+        q1 = muldiv(R, cc + 1, G);
+      }
+      const uint32_t u0 = q0 / (uint32_t)gI;
+      tb.qtab[4 * j] = (int)(q1 - q0);
+      tb.qtab[4 * j + 1] = (int)u0;
+      tb.qtab[4 * j + 2] = (int)(q0 - u0 * (uint32_t)gI);
     }
-    for (int i = 0; i < P.nsd; ++i) mbar_init(&fulld[i], 1);
-    mbar_init(xbar, 1);
-    mbar_fence_init();
+  } else if (warp == 3) {
+    if constexpr (FAST) {
+      // descriptors of the routed maps are first used after the routing,
+      // under load: fetch all four now
+      if (lane == 0) prefetch_tensormap(&Pk.tm_gu_e);
+      if (lane == 1) prefetch_tensormap(&Pk.tm_d_e);
+      if (lane == 2) prefetch_tensormap(&Pk.tm_gu_s);
+      if (lane == 3) prefetch_tensormap(&Pk.tm_d_s);
+    }
   }
-  __syncthreads();
+  // the shared stages (every thread advances the issue cursors in step; the
+  // thread that initialised the barriers issues)
   for (int k = 0; k < min(n_sh, NS); ++k) {
     advance(ci, NS);
     if (tid == 0) issue(ci);
@@ -488,12 +496,15 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       wr[q] = (cta <= P.E && c0 < H) ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  __syncthreads();  // barriers initialised, tables cleared
 
   // ---- the activation (block form: x_res) and the workspace belong to this
   // kernel from here on
   pdl_wait();
   RowSync* const sync = P.sync;
-  const unsigned long long epoch = __ldcg(&sync->epoch) + 1ull;
+  const unsigned long long prev_epoch = __ldcg(&sync->epoch);
+  const unsigned long long epoch = prev_epoch + 1ull;
+  const bool fast_sync = __ldcg(&sync->sig) == ~prev_epoch;
   if (cta == 0) {
     if (tid == 0) P.ctrl[kCtrlStatus] = 0u;  // a status left by the failure-path probe
     for (int c = P.G + tid; c < kMaxGrid; c += kRowThreads) sync->status[c] = 0;
@@ -583,9 +594,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       __syncthreads();
     }
   }
-  // this block's logits are written: announce it (the barrier before orders
-  // every thread's stores before thread 0's release)
-  if (tid == 0) st_release_gpu_u64(&sync->logits_ready[cta], epoch);
   // activation in its compute form, in place, while the other blocks finish
   // their logits.  Fast shapes: the bf16 A fragments of the tensor-core
   // loops, token t's row at t * kXPitch, 16 bytes per (warp slice w, 32-column
@@ -647,12 +655,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     }
   }
-  // ---- every block's logits: warp 0 waits (bounded) until each block's
-  // slot holds this call's epoch
-  if (warp == 0 && !grid_flags_wait(sync->logits_ready, P.G, epoch)) timed_out = true;
-  __syncthreads();
-  // every block has read the epoch (before its announcement): advance it
-  if (cta == 0 && tid == 0) sync->epoch = epoch;
+  // ---- every block's logits (first barrier; see RowSync)
+  if (!grid_barrier(sync, 0, fast_sync, P.G, epoch, cta, true)) timed_out = true;
   // routing, every block from all logits: top-k of token t on warp 7 - t
   // (the chosen experts, their softmax weights and their bits in the
   // selection bitmap) and the shared gate sigmoid(logit_E)
@@ -667,10 +671,25 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         atomicOr(&tb.bitmap[e >> 5], 1u << (e & 31));
       }
       if (lane == 0) tb.s[t] = 1.0f / (1.0f + expf(-sl));
+      if constexpr (TMAX == 1) {
+        // one token: its k distinct experts are the active list; expert j's
+        // active index is its rank among them (ascending)
+        __syncwarp();
+        const int e = lane < K ? tb.ids[lane] : 0x7FFFFFFF;
+        int rank = 0;
+        for (int j = 0; j < K; ++j) rank += __shfl_sync(0xffffffffu, e, j) < e;
+        if (lane < K) {
+          tb.active[rank] = e;
+          tb.inv_u[e] = static_cast<int16_t>(rank);
+          tb.mask[rank] = 1u;
+          tb.wt[rank] = tb.p[lane];
+        }
+        if (lane == 0) tb.misc[0] = K;
+      }
     }
   }
   __syncthreads();
-  if (warp == 0) {
+  if (TMAX > 1 && warp == 0) {
     // active experts in ascending order (active index u): bitmap word l on
     // lane l, an exclusive scan of the word counts
     const int nw = (P.E + 31) / 32;
@@ -700,7 +719,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     if (lane == 0) tb.misc[0] = U;
   }
-  __syncthreads();
+  if (TMAX > 1) __syncthreads();
   const int U = tb.misc[0];
   {
     const int32_t* q = tb.qtab + 4 * (U - K);
@@ -1368,11 +1387,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // barrier orders all threads' stores before thread 0's release (a
   // cumulative release at GPU scope), and warp 0's acquire orders every
   // other block's stores before this block's reads
-  __syncthreads();
-  if (tid == 0) st_release_gpu_u64(&sync->partial_ready[cta], epoch);
-  bool tail_timed_out = false;
-  if (warp == 0 && !grid_flags_wait(sync->partial_ready, P.G, epoch)) tail_timed_out = true;
-  if (__syncthreads_or(tail_timed_out) || block_timed_out) {
+  const bool tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
+  if (tail_timed_out || block_timed_out) {
     if (tid == 0) sync->status[cta] = kStatusTimeout;
   } else if (tid == 0) {
     sync->status[cta] = 0;
