@@ -54,7 +54,8 @@ PREROLL_S = 0.15  # GPU work enqueued right before each timed region (clock samp
 # captures (profiles/), per (config, T); None until captured for the current kernel.
 NCU_TRAFFIC_BYTES = {("batched_bf16", 256): 823_113_984, ("batched_q4", 256): 238_398_464}
 # Extra workloads measured in the default N=1 run: (config, T, steps, warm-up steps, oracle budget in s)
-EXTRAS = [("decode_bf16", 8, 400, 20, 3.0), ("decode_q4", 1, 400, 20, 3.0), ("decode_q4", 2, 400, 20, 3.0),
+EXTRAS = [("decode_bf16", 8, 400, 20, 3.0), ("two_stream_bf16", 1, 400, 20, 0.0), ("two_stream_bf16", 8, 400, 20, 0.0),
+          ("decode_q4", 1, 400, 20, 3.0), ("decode_q4", 2, 400, 20, 3.0),
           ("decode_q4", 4, 400, 20, 3.0), ("decode_q4", 8, 400, 20, 3.0), ("batched_bf16", 64, 64, 5, 3.0),
           ("batched_bf16", 256, 64, 5, 4.0), ("batched_q4", 64, 64, 5, 3.0), ("batched_q4", 256, 64, 5, 4.0),
           ("stack_q4", 1, 32, 3, 6.0)]
@@ -105,6 +106,9 @@ def workload(cfg: str, T: int):
     shapes = datagen.Shapes(T=T, H=H, E=E, top_k=K_TOP, I=I, Is=IS)
     name = {
         "decode_bf16": f"decode bf16 MoE FFN layer: T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
+        "two_stream_bf16": f"decode bf16 MoE FFN layer as two branches on two CUDA streams (routed on the main stream, "
+                           f"gated shared expert on a forked stream, event join, join add): T={T}, H={H}, E={E}, "
+                           f"top_k={K_TOP}, I={I}, Is={IS}",
         "decode_q4": f"decode 4-bit MoE FFN layer (blocks of 32, fp16 scale): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_bf16": f"batched bf16 MoE FFN layer (grouped GEMMs): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_q4": f"batched 4-bit MoE FFN layer (grouped GEMMs, fp16 operands): T={T}, H={H}, E={E}, top_k={K_TOP}, "
@@ -129,6 +133,8 @@ def token_batch(step_token: int, T: int) -> np.ndarray:
 def kernel_names(cfg: str, T: int) -> str:
     if cfg == "stack_q4":
         return "k_rows per layer, block form; duration = step time / layers"
+    if cfg == "two_stream_bf16":
+        return "k_rows routed part (main stream) + k_rows shared part (aux stream) + join add; duration = step time"
     if T > 8:
         return (("k_gemm_q4<0>, k_gemm_q4<1>" if cfg == "batched_q4" else "k_gemm<0>, k_gemm<1>")
                 + " (+ routing, gather, combine); duration = step time")
@@ -343,8 +349,21 @@ def time_layer(fb, res: Resident, cfg: str, T: int, steps: int, warmup: int, str
     xs = torch.from_numpy(xs_host.view(np.int16)).to(dev)
     plan, ws_bytes = fb.moe_ffn_prepare(shapes, fb.ACT_BF16, wfmt)
     launches_per_step = fb.moe_ffn_query(plan, fb.QUERY_LAUNCHES_PER_EXECUTE)
+    two = cfg == "two_stream_bf16"
+    if two:
+        launches_per_step = 3  # routed part, shared part, join add
+        ws_two = torch.empty(fb.moe_ffn_query(plan, fb.QUERY_TWO_STREAM_WORKSPACE), dtype=torch.uint8, device=dev)
+        aux = torch.cuda.Stream(device=dev)
+        ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+    def run_step(x, r, ew, sw, gv):
+        if two:
+            fb.moe_ffn_execute_two_stream(plan, ws_two, x, r, ew, sw, gv, out, aux_stream=aux, fork_event=ev_fork,
+                                          join_event=ev_join, stream=stream)
+        else:
+            fb.moe_ffn_execute(plan, ws, x, r, ew, sw, gv, out, stream=stream)
 
     def step_args(s):
         r, ew, sw, gv = res.copies[s % n_copies]
@@ -370,14 +389,12 @@ def time_layer(fb, res: Resident, cfg: str, T: int, steps: int, warmup: int, str
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for s in range(n):
-                x, r, ew, sw, gv = step_args(s)
-                fb.moe_ffn_execute(plan, ws, x, r, ew, sw, gv, out, stream=stream)
+                run_step(*step_args(s))
         return g
 
     with torch.cuda.stream(stream):
         for s in range(max(3, warmup)):
-            x, r, ew, sw, gv = step_args(s)
-            fb.moe_ffn_execute(plan, ws, x, r, ew, sw, gv, out, stream=stream)
+            run_step(*step_args(s))
     torch.cuda.synchronize()
     g_main = capture(graph_steps)
     reps, rem = divmod(steps, graph_steps)
@@ -596,7 +613,7 @@ def main():
                 else:
                     r = time_layer(fb, res_for(w), cfg, T, steps, warm, stream, dev, ClockSampler(local))
                     fb.moe_ffn_destroy(r["_plan"])
-                    if want_cpu:
+                    if want_cpu and budget > 0:
                         rate, n, dt, used, offered = oracle_rate(sh, w, budget, 100000, res_for(w).host)
                         r["cpu_baseline"] = cpu_entry(rate, n, dt, used, offered, f"{n} layer calls of T={T}")
                 extras.append(public(r))

@@ -34,6 +34,7 @@ W_Q4B32 = 1
 
 QUERY_PATH = 0
 QUERY_LAUNCHES_PER_EXECUTE = 1
+QUERY_TWO_STREAM_WORKSPACE = 2
 
 EXPORTS = (
     "moe_ffn_prepare",
@@ -48,6 +49,7 @@ EXPORTS = (
     "moe_ffn_strerror",
     "moe_ffn_execute_static_scratch",
     "moe_ffn_last_cuda_error",
+    "moe_ffn_execute_two_stream",
 )
 
 STATIC_SCRATCH_BYTES = 1 << 24
@@ -106,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.moe_ffn_probe_timeout.argtypes = [vp, vp, vp, sz, i32]
         L.moe_ffn_last_cuda_error.restype = ctypes.c_char_p
         L.moe_ffn_last_cuda_error.argtypes = []
+        L.moe_ffn_execute_two_stream.restype = ctypes.c_int
+        L.moe_ffn_execute_two_stream.argtypes = [vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -221,6 +225,19 @@ def moe_ffn_execute_static_scratch(plan, x, router_w, expert_w, shexp_w, shexp_g
     _check(lib().moe_ffn_execute_static_scratch(plan, _stream(stream), _ptr(x), _ptr(router_w), _ptr(expert_w),
                                                 _ptr(shexp_w), _ptr(shexp_gate_w), _ptr(out)),
            "moe_ffn_execute_static_scratch")
+
+
+def moe_ffn_execute_two_stream(plan, workspace, x, router_w, expert_w, shexp_w, shexp_gate_w, out, aux_stream=None,
+                               fork_event=None, join_event=None, stream=None, workspace_bytes=None):
+    """The layer as two branches on two streams joined by an add (routed on ``stream``, the gated shared expert
+    on ``aux_stream``, torch.cuda.Event objects or raw handles as the fork and join events); with no aux stream the
+    same kernels run one after the other on ``stream``."""
+    nbytes = workspace_bytes if workspace_bytes is not None else workspace.numel() * workspace.element_size()
+    ev = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
+    _check(lib().moe_ffn_execute_two_stream(plan, _stream(stream), None if aux_stream is None else _stream(aux_stream),
+                                            ev(fork_event), ev(join_event), _ptr(workspace), nbytes, _ptr(x),
+                                            _ptr(router_w), _ptr(expert_w), _ptr(shexp_w), _ptr(shexp_gate_w),
+                                            _ptr(out)), "moe_ffn_execute_two_stream")
 
 
 def moe_ffn_strerror(status: int) -> str:

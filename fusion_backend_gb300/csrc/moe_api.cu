@@ -195,6 +195,75 @@ int run(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t wo
   return cuda_status(err);
 }
 
+// Workspace of the two-stream form: the routed part's and the shared part's
+// own workspaces, then their outputs y_r and y_s ([T][H] fp32 each).
+size_t two_stream_bytes(const moe_ffn_plan* plan) {
+  const size_t y = align256((size_t)plan->s.T * plan->s.H * 4);
+  return 2 * plan->ws.total + 2 * y;
+}
+
+int run_two_stream(moe_ffn_plan_t plan, cudaStream_t stream, cudaStream_t aux, cudaEvent_t fork, cudaEvent_t join,
+                   void* workspace, size_t workspace_bytes, const void* x, const void* router_w,
+                   const void* expert_w, const void* shexp_w, const void* shexp_gate_w, float* out) {
+  if (!valid_plan(plan)) return MOE_FFN_ERR_INVALID_ARG;
+  if (plan->path != 0) return MOE_FFN_ERR_UNSUPPORTED;
+  if (!workspace || !x || !router_w || !expert_w || !shexp_w || !shexp_gate_w || !out) return MOE_FFN_ERR_INVALID_ARG;
+  if (workspace_bytes < two_stream_bytes(plan)) return MOE_FFN_ERR_WORKSPACE;
+  if (!aligned(workspace, 256) || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(expert_w, 16) ||
+      !aligned(shexp_w, 16) || !aligned(shexp_gate_w, 16) || !aligned(out, 16))
+    return MOE_FFN_ERR_MISALIGNED;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != MOE_FFN_OK) return rc;
+  const moe_ffn_shapes& s = plan->s;
+  const int G = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
+  if (G < 2) return MOE_FFN_ERR_UNSUPPORTED;
+  // SMs split by the bytes each branch streams (the routed branch at its
+  // largest number of distinct experts), so that both grids are resident at
+  // once: every grid waits at grid-wide barriers for all of its blocks.
+  const double eb = (plan->wfmt == MOE_FFN_W_Q4B32 ? 9.0 / 16.0 : 2.0) * 3.0 * s.H;
+  const double b_sh = eb * s.Is, b_r = eb * s.I * (double)(s.E < s.T * s.top_k ? s.E : s.T * s.top_k);
+  int Gs = (int)(G * b_sh / (b_sh + b_r) + 0.5);
+  Gs = Gs < 1 ? 1 : (Gs > G - 1 ? G - 1 : Gs);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const size_t y = align256((size_t)s.T * s.H * 4);
+  float* y_r = reinterpret_cast<float*>(w + 2 * plan->ws.total);
+  float* y_s = reinterpret_cast<float*>(w + 2 * plan->ws.total + y);
+  LayerParams P[2];
+  for (int part = 1; part <= 2; ++part) {
+    LayerParams& L = P[part - 1];
+    fill_params(plan, L, w + (part - 1) * plan->ws.total);
+    L.x = x;
+    L.router_w = static_cast<const uint16_t*>(router_w);
+    L.gate_w = static_cast<const uint16_t*>(shexp_gate_w);
+    L.expert_w = static_cast<const uint8_t*>(expert_w);
+    L.shexp_w = static_cast<const uint8_t*>(shexp_w);
+    L.out = part == 1 ? y_r : y_s;
+    L.part = part;
+    L.G = part == 1 ? G - Gs : Gs;
+    if (rows_layout(L) < 0 || L.smem > dev->smem_optin) return MOE_FFN_ERR_UNSUPPORTED;
+    cudaError_t err = rows_tensor_maps(L);
+    if (err != cudaSuccess) return cuda_status(err);
+  }
+  const bool two = aux && fork && join && aux != stream;
+  cudaError_t err = cudaSuccess;
+  if (two) {
+    // fork: the shared branch on the aux stream after everything before
+    // this call on the main stream; join: the add after both branches
+    err = cudaEventRecord(fork, stream);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(aux, fork, 0);
+    if (err == cudaSuccess) err = launch_rows(P[0], stream);
+    if (err == cudaSuccess) err = launch_rows(P[1], aux);
+    if (err == cudaSuccess) err = cudaEventRecord(join, aux);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, join, 0);
+  } else {
+    err = launch_rows(P[0], stream);
+    if (err == cudaSuccess) err = launch_rows(P[1], stream);
+  }
+  if (err == cudaSuccess) err = launch_join_add(y_r, y_s, out, s.T * s.H, stream);
+  return cuda_status(err);
+}
+
 }  // namespace
 
 extern "C" {
@@ -363,9 +432,22 @@ int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value) {
     case MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE:
       *value = plan->path == 1 ? kBatchLaunches : kLaunchesPerExecute;
       return MOE_FFN_OK;
+    case MOE_FFN_QUERY_TWO_STREAM_WORKSPACE:
+      if (plan->path != 0) return MOE_FFN_ERR_UNSUPPORTED;
+      *value = (int64_t)two_stream_bytes(plan);
+      return MOE_FFN_OK;
     default:
       return MOE_FFN_ERR_INVALID_ARG;
   }
+}
+
+int moe_ffn_execute_two_stream(moe_ffn_plan_t plan, moe_ffn_stream_t stream, moe_ffn_stream_t aux_stream,
+                               moe_ffn_event_t fork_event, moe_ffn_event_t join_event, void* workspace,
+                               size_t workspace_bytes, const void* x, const void* router_w, const void* expert_w,
+                               const void* shexp_w, const void* shexp_gate_w, float* out) {
+  return run_two_stream(plan, reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<cudaStream_t>(aux_stream),
+                        reinterpret_cast<cudaEvent_t>(fork_event), reinterpret_cast<cudaEvent_t>(join_event),
+                        workspace, workspace_bytes, x, router_w, expert_w, shexp_w, shexp_gate_w, out);
 }
 
 void moe_ffn_destroy(moe_ffn_plan_t plan) {

@@ -66,6 +66,10 @@ struct LayerParams {
   int block_mode;
   float eps;
   int G;  // grid of the row kernel
+  // 0: the whole layer; 1: the routed experts only, out = sum_j p_j FFN_j(x)
+  // (ffn_moe_out); 2: the gated shared expert only, out = s FFN_shared(x)
+  // (ffn_shexp).  Parts 1 and 2 are the two branches of the two-stream form.
+  int part;
 
   // caller tensors
   const void* x;  // [T,H] (block mode: fp32 x_res)
@@ -223,5 +227,8 @@ int rows_layout(LayerParams& p);
 cudaError_t rows_tensor_maps(LayerParams& p);
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream);
 constexpr int kLaunchesPerExecute = 1;
+// out[i] = a[i] + b[i], i < n: the join add(ffn_moe_out, ffn_shexp) of the
+// two-stream form (moe_rows.cu).
+cudaError_t launch_join_add(const float* a, const float* b, float* out, int n, cudaStream_t stream);
 
 }  // namespace moe

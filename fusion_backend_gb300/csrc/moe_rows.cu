@@ -143,6 +143,21 @@ cudaError_t rows_tensor_maps(LayerParams& p) {
   return cudaSuccess;
 }
 
+namespace {
+
+__global__ void __launch_bounds__(256) k_join_add(const float* __restrict__ a, const float* __restrict__ b,
+                                                  float* __restrict__ out, int n) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < n) out[i] = __fadd_rn(a[i], b[i]);
+}
+
+}  // namespace
+
+cudaError_t launch_join_add(const float* a, const float* b, float* out, int n, cudaStream_t stream) {
+  k_join_add<<<(n + 255) / 256, 256, 0, stream>>>(a, b, out, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream) {
   if (!rows_fast(p)) return launch_rows_generic(p, stream);
   return p.wfmt == 1 ? launch_rows_q4_fast(p, stream) : launch_rows_bf16_fast(p, stream);

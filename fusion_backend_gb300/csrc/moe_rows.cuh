@@ -351,7 +351,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // known now; the routed groups are the run [q0, q1) of the flattened
   // (active expert u, group) order, known after the routing and sized so
   // that shared + routed groups (stages) are balanced over the blocks.
-  const int gS = (P.Is + RS - 1) / RS, gI = (P.I + RS - 1) / RS;
+  const int gS = P.part == 1 ? 0 : (P.Is + RS - 1) / RS, gI = (P.I + RS - 1) / RS;
   const int gs0 = (int)muldiv(gS, cta, P.G), gs1 = (int)muldiv(gS, cta + 1, P.G);
   const int n_sh = gs1 - gs0;
   int n_stages = n_sh;
@@ -488,12 +488,15 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // weights; any other predecessor has completed before this kernel starts).
   constexpr int kRC = kMaxH / (kRowThreads * 8);  // 8-element chunks of a row per thread
   uint4 wr[kRC];
+  // the shared-expert part needs only the shared-gate row (block 0)
+  const int r_first = P.part == 2 ? (cta == 0 ? P.E : P.E + 1) : cta;
+  const int r_step = P.part == 2 ? P.E + 1 : P.G;
   {
-    const uint16_t* w = cta < P.E ? P.router_w + (size_t)cta * H : P.gate_w;
+    const uint16_t* w = r_first < P.E ? P.router_w + (size_t)r_first * H : P.gate_w;
 #pragma unroll
     for (int q = 0; q < kRC; ++q) {
       const int c0 = 8 * tid + kRowThreads * 8 * q;
-      wr[q] = (cta <= P.E && c0 < H) ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
+      wr[q] = (r_first <= P.E && c0 < H) ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
   __syncthreads();  // barriers initialised, tables cleared
@@ -534,7 +537,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   {
     float* red = reinterpret_cast<float*>(sm + P.off_part);  // [kRowWarps][TMAX][2]
     const bool exact_products = P.block_mode || P.act == 1;   // bf16 x bf16 is exact in fp32
-    for (int r = cta, j = 0; r <= P.E; r += P.G, ++j) {
+    for (int r = r_first, j = 0; r <= P.E; r += r_step, ++j) {
       if (j > 0) {
         const uint16_t* w = r < P.E ? P.router_w + (size_t)r * H : P.gate_w;
 #pragma unroll
@@ -660,7 +663,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // routing, every block from all logits: top-k of token t on warp 7 - t
   // (the chosen experts, their softmax weights and their bits in the
   // selection bitmap) and the shared gate sigmoid(logit_E)
-  {
+  if (P.part == 2) {
+    // shared-expert part: only the gate s of every token
+    if (tid < T) tb.s[tid] = 1.0f / (1.0f + expf(-__ldcg(P.logits + (size_t)tid * P.ls + P.E)));
+  } else {
     const int t = kRowWarps - 1 - warp;
     if (t < T) {
       float sl = 0.f;
@@ -689,7 +695,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   }
   __syncthreads();
-  if (TMAX > 1 && warp == 0) {
+  if (TMAX > 1 && warp == 0 && P.part != 2) {
     // active experts in ascending order (active index u): bitmap word l on
     // lane l, an exclusive scan of the word counts
     const int nw = (P.E + 31) / 32;
@@ -719,9 +725,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     if (lane == 0) tb.misc[0] = U;
   }
-  if (TMAX > 1) __syncthreads();
-  const int U = tb.misc[0];
-  {
+  if (TMAX > 1 && P.part != 2) __syncthreads();
+  const int U = P.part == 2 ? 0 : tb.misc[0];
+  if (P.part != 2) {
     const int32_t* q = tb.qtab + 4 * (U - K);
     n_stages = n_sh + q[0];
     ur0 = q[1];
@@ -740,7 +746,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         if (tid == 32 * (j++ & (kRowWarps - 1))) issue_d(cd);
       }
   }
-  if (cta == 0 && warp == kRowWarps - 1) {
+  if (cta == 0 && warp == kRowWarps - 1 && P.part != 2) {
     // routing outputs for the caller and the test readers: counts, offsets
     // (a scan over the experts) and the stable token-major permutation
     int base = 0;
@@ -1387,17 +1393,23 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // barrier orders all threads' stores before thread 0's release (a
   // cumulative release at GPU scope), and warp 0's acquire orders every
   // other block's stores before this block's reads
+  // This block's output columns [da, db) for all tokens (O values).  In the
+  // block form the residual x_res of those columns is read now, before the
+  // barrier: no other block writes them, and every block read all of x at
+  // its start.
+  const int da = (int)muldiv(H, cta, P.G), db = (int)muldiv(H, cta + 1, P.G);
+  const int nD = db - da, O = T * nD;
+  float resid = 0.f;
+  if (P.block_mode && tid < O) resid = __ldcg(P.out + (size_t)(tid / nD) * H + da + tid % nD);
   const bool tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
   if (tail_timed_out || block_timed_out) {
     if (tid == 0) sync->status[cta] = kStatusTimeout;
   } else if (tid == 0) {
     sync->status[cta] = 0;
   }
-  // This block's output columns [da, db) for all tokens: O sums of G
-  // partials.  Thread (sp, o) adds partials sp, sp + S, ... in order, all
-  // loads in flight together; the S part sums are then added in order.
-  const int da = (int)muldiv(H, cta, P.G), db = (int)muldiv(H, cta + 1, P.G);
-  const int nD = db - da, O = T * nD;
+  // The O sums of G partials.  Thread (sp, o) adds partials sp, sp + S, ...
+  // in order, up to 16 loads in flight together; the S part sums are then
+  // added in order.
   if (O > 0) {
     const int S = O >= kRowThreads ? 1 : kRowThreads / O;
     // The ring is idle now (every issued stage was waited on); reuse it.
@@ -1408,15 +1420,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       const float* src = P.partial + (size_t)t * H + col;
       const size_t stride = (size_t)T * H;
       float acc = 0.f;
-      int c = sp;
-      for (; c + 7 * S < P.G; c += 8 * S) {
-        float v[8];
+      for (int c0 = sp; c0 < P.G; c0 += 16 * S) {
+        float v[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = __ldcg(src + (size_t)(c + q * S) * stride);
+        for (int q = 0; q < 16; ++q) {
+          const int c = c0 + q * S;
+          v[q] = c < P.G ? __ldcg(src + (size_t)c * stride) : 0.f;
+        }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc += v[q];
+        for (int q = 0; q < 16; ++q)
+          if (c0 + q * S < P.G) acc += v[q];
       }
-      for (; c < P.G; c += S) acc += __ldcg(src + (size_t)c * stride);
       red[sp * O + o] = acc;
     }
     __syncthreads();
@@ -1425,7 +1439,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       for (int q = 1; q < S; ++q) acc += red[q * O + oo];
       const int t = oo / nD, col = da + oo % nD;
       float* dst = P.out + (size_t)t * H + col;
-      *dst = P.block_mode ? __fadd_rn(*dst, acc) : acc;
+      *dst = P.block_mode ? __fadd_rn(oo < kRowThreads ? resid : *dst, acc) : acc;
     }
   }
 }

@@ -54,6 +54,8 @@ extern "C" {
 
 /* Same type as cudaStream_t; 0 is the legacy default stream. */
 typedef struct CUstream_st* moe_ffn_stream_t;
+/* Same type as cudaEvent_t. */
+typedef struct CUevent_st* moe_ffn_event_t;
 
 typedef enum {
   MOE_FFN_OK = 0,
@@ -225,10 +227,37 @@ int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream,
 int moe_ffn_probe_timeout(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
                           int32_t which);
 
+/*
+ * The layer in the form of "ggml-cuda: overlap the MoE shared expert on a
+ * separate stream" (ROCm/llama.cpp PR #36, "What this changes"): the routed
+ * branch (router, top-k, routed experts: ffn_moe_out) runs on `stream`, the
+ * gated shared expert (ffn_shexp) on `aux_stream`, forked after everything
+ * enqueued on `stream` before this call (fork_event recorded on `stream`,
+ * waited by `aux_stream`) and joined back (join_event recorded on
+ * `aux_stream`, waited by `stream`); then out = ffn_moe_out + ffn_shexp on
+ * `stream`, the add of the page's diamond.  Decode plans (T <= 8) only, like
+ * the page's batch gate; MOE_FFN_ERR_UNSUPPORTED otherwise.  The two
+ * branches split the SMs in proportion to the bytes they stream.  When
+ * aux_stream equals `stream` or an event is NULL, the same kernels run one
+ * after the other on `stream` (the sequential form); both forms give
+ * bit-identical results.  The fused moe_ffn_execute overlaps the shared
+ * expert inside one kernel instead; its results agree with these within
+ * the layer's tolerance (the sums are formed in another order).
+ * Arguments as moe_ffn_execute, except that the workspace must hold
+ * moe_ffn_query(MOE_FFN_QUERY_TWO_STREAM_WORKSPACE) bytes.  The events are
+ * caller-owned (cudaEventCreateWithFlags with cudaEventDisableTiming is
+ * enough); the call records and waits on them and keeps no reference.
+ */
+int moe_ffn_execute_two_stream(moe_ffn_plan_t plan, moe_ffn_stream_t stream, moe_ffn_stream_t aux_stream,
+                               moe_ffn_event_t fork_event, moe_ffn_event_t join_event, void* workspace,
+                               size_t workspace_bytes, const void* x, const void* router_w, const void* expert_w,
+                               const void* shexp_w, const void* shexp_gate_w, float* out);
+
 /* Queries on a plan. */
 typedef enum {
-  MOE_FFN_QUERY_PATH = 0,                /* 0 = decode, 1 = grouped GEMM */
-  MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE = 1 /* kernels one execute launches */
+  MOE_FFN_QUERY_PATH = 0,                 /* 0 = decode, 1 = grouped GEMM */
+  MOE_FFN_QUERY_LAUNCHES_PER_EXECUTE = 1, /* kernels one execute launches */
+  MOE_FFN_QUERY_TWO_STREAM_WORKSPACE = 2  /* workspace bytes of moe_ffn_execute_two_stream (decode plans) */
 } moe_ffn_query_t;
 int moe_ffn_query(moe_ffn_plan_t plan, int32_t what, int64_t* value);
 

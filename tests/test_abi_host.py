@@ -122,3 +122,16 @@ def test_strerror_covers_codes(lib):
     for code in range(0, -8, -1):
         assert fb.strerror(code) != "unknown status"
     assert fb.strerror(-99) == "unknown status"
+
+
+def test_two_stream_workspace_query(lib):
+    plan, ws = fb.moe_ffn_prepare(datagen.Shapes(1, 2048, 128, 8, 768, 512), fb.ACT_BF16, fb.W_BF16)
+    two = fb.moe_ffn_query(plan, fb.QUERY_TWO_STREAM_WORKSPACE)
+    # both branches' own workspaces, then their two [T][H] fp32 outputs
+    assert two == 2 * ws + 2 * 2048 * 4
+    fb.moe_ffn_destroy(plan)
+    plan, _ = fb.moe_ffn_prepare(datagen.Shapes(64, 2048, 128, 8, 768, 512), fb.ACT_BF16, fb.W_BF16)
+    with pytest.raises(fb.MoeFFNError) as e:
+        fb.moe_ffn_query(plan, fb.QUERY_TWO_STREAM_WORKSPACE)
+    assert e.value.status == fb.ERR_UNSUPPORTED
+    fb.moe_ffn_destroy(plan)
