@@ -30,6 +30,11 @@
  * Encoding the weights is input preparation (the layer only ever reads the
  * encoded form); decoding belongs to the layer and is not here.
  *
+ * The int8 encoder writes one fp32 scale per row, s = fp32(max|w|) / 127 in
+ * fp32, and q = clamp(round(w / s), -127, 127) (division in fp32, rounding
+ * half away from zero; an all-zero row gets s = 0 and q = 0); a row is its C
+ * signed bytes, then s (little endian), then 12 zero bytes, C + 16 bytes.
+ *
  * Portable C11, no intrinsics: identical integer streams on x86-64 and
  * aarch64.  Built with -ffp-contract=off so the double arithmetic is not
  * fused differently on the two machines.
@@ -304,6 +309,38 @@ int dg_encode_q4b32(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* out,
       pthread_join(th[t], NULL);
     else
       enc_worker(&jobs[t]);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* int8 row encoder (input preparation for the int8 weight format)     */
+
+/* Encode a row-major [rows, cols] bf16 matrix into rows of cols int8 values
+ * followed by the row's fp32 scale and 12 bytes of padding.  Returns 0, or -1
+ * when cols % 16 != 0. */
+int dg_encode_i8(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* out) {
+  if (cols % 16 != 0 || rows < 0) return -1;
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* src = w + r * cols;
+    uint8_t* dst = out + r * (cols + 16);
+    float amax = 0.0f;
+    for (int64_t c = 0; c < cols; ++c) {
+      float v = fabsf(bf16_to_f32(src[c]));
+      if (v > amax) amax = v;
+    }
+    float s = amax / 127.0f;
+    for (int64_t c = 0; c < cols; ++c) {
+      int q = 0;
+      if (s != 0.0f) {
+        q = (int)roundf(bf16_to_f32(src[c]) / s);
+        if (q > 127) q = 127;
+        if (q < -127) q = -127;
+      }
+      dst[c] = (uint8_t)(int8_t)q;
+    }
+    memcpy(dst + cols, &s, 4);
+    memset(dst + cols + 4, 0, 12);
   }
   return 0;
 }

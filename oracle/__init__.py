@@ -67,6 +67,8 @@ def lib():
         _lib.or_threads_used.argtypes = [ctypes.POINTER(_Shapes), ctypes.c_int]
         _lib.or_float_to_bf16.restype = ctypes.c_uint16
         _lib.or_float_to_bf16.argtypes = [ctypes.c_float]
+        _lib.or_quantize_i8.restype = None
+        _lib.or_quantize_i8.argtypes = [vp, i64, vp, vp]
     return _lib
 
 
@@ -87,6 +89,15 @@ def threads_used(shapes, threads=None) -> int:
     """Threads a layer call of these shapes starts when offered ``threads`` (default: all cores)."""
     s = _Shapes(shapes.T, shapes.H, shapes.E, shapes.top_k, shapes.I, shapes.Is)
     return int(lib().or_threads_used(ctypes.byref(s), threads or nthreads()))
+
+
+def quantize_i8(x_f64):
+    """The int8 activation of one row (values must be fp32-representable): (q int8 [n], scale fp32)."""
+    x, xp = _c(x_f64, np.float64)
+    q = np.empty(x.size, np.int8)
+    sc = np.empty(1, np.float32)
+    lib().or_quantize_i8(xp, x.size, q.ctypes.data, sc.ctypes.data)
+    return q, float(sc[0])
 
 
 def float_to_bf16(v: float) -> int:

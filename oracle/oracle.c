@@ -30,6 +30,16 @@
  *   4-bit: each row = cols/2 bytes of nibbles (element 2j in the low nibble of
  *          byte j, element 2j+1 in the high nibble) followed by cols/32 fp16
  *          scales; element value = d * (nibble - 8) for its 32-block.
+ *   int8:  each row = cols signed bytes q, then one fp32 scale s (little
+ *          endian) and 12 bytes of padding; element value = s * q.  With this
+ *          format the gate and up projections take an int8 activation, as the
+ *          int8 linear of "ggml operator extensions" (sd.cpp integration,
+ *          sd.linear_i8.v1) defines it: x is quantised per token,
+ *          xs = max|x| / 127 and qx = clamp(round(x / xs), -127, 127) in fp32
+ *          (round half away from zero; xs = 0 gives qx = 0), and the
+ *          projection is float(int32_dot(W, qx)) * xs * s, the products in
+ *          that order in fp32; SwiGLU follows.  The down projection uses the
+ *          weights s * q with the fp32 h (in double, like the other formats).
  * Layer layout: router [E,H]; expert e = gate [I,H] | up [I,H] | downT [I,H];
  * shared = gate [Is,H] | up [Is,H] | downT [Is,H]; shared-gate vector [H] bf16.
  * downT is the down projection stored transposed (row i = column i of the
@@ -84,11 +94,22 @@ uint16_t or_float_to_bf16(float f) {
   return (uint16_t)((u + rounding) >> 16);
 }
 
+/* fp32 scale of an int8 row (the 4 bytes after its cols values). */
+static float i8_row_scale(const uint8_t* row, int64_t cols) {
+  float s;
+  memcpy(&s, row + cols, 4);
+  return s;
+}
+
 /* Value of element c of row r of a weight matrix with `cols` columns. */
 static double weight_at(const uint8_t* base, int wfmt, int64_t cols, int64_t r, int64_t c) {
   if (wfmt == 0) {
     const uint16_t* w = (const uint16_t*)base;
     return or_bf16_to_double(w[r * cols + c]);
+  }
+  if (wfmt == 2) {
+    const uint8_t* row = base + r * (cols + 16);
+    return (double)i8_row_scale(row, cols) * (double)(int8_t)row[c];
   }
   const uint8_t* row = base + r * (cols * 9 / 16);
   uint8_t byte = row[c / 2];
@@ -104,7 +125,42 @@ void or_decode_row(const uint8_t* base, int wfmt, int64_t cols, int64_t r, doubl
 }
 
 static int64_t matrix_bytes(int wfmt, int64_t rows, int64_t cols) {
-  return wfmt == 0 ? rows * cols * 2 : rows * (cols * 9 / 16);
+  return wfmt == 0 ? rows * cols * 2 : wfmt == 1 ? rows * (cols * 9 / 16) : rows * (cols + 16);
+}
+
+/* The int8 activation of one row of n values (each an fp32 value): scale
+ * xs = fp32(max|x|) / 127 in fp32, q = clamp(roundf(x / xs), -127, 127) with
+ * the division in fp32 and rounding half away from zero; xs = 0 gives q = 0. */
+void or_quantize_i8(const double* x, int64_t n, int8_t* q, float* scale) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf((float)x[i]);
+    if (a > amax) amax = a;
+  }
+  float xs = amax / 127.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    int v = 0;
+    if (xs != 0.0f) {
+      float r = roundf((float)x[i] / xs);
+      v = (int)r;
+      if (v > 127) v = 127;
+      if (v < -127) v = -127;
+    }
+    q[i] = (int8_t)v;
+  }
+  *scale = xs;
+}
+
+/* float(int32_dot(W_r, q)) * xs * s_r for row r of an int8 matrix, in fp32,
+ * the products in that order; returned as double. */
+static double i8_projection(const uint8_t* W, int64_t cols, int64_t r, const int8_t* q, float xs) {
+  const uint8_t* row = W + r * (cols + 16);
+  int64_t dot = 0;
+  for (int64_t c = 0; c < cols; ++c) dot += (int64_t)(int8_t)row[c] * (int64_t)q[c];
+  float v = (float)dot;
+  v = v * xs;
+  v = v * i8_row_scale(row, cols);
+  return (double)v;
 }
 
 /* Bytes of one expert block (gate | up | downT) with intermediate size `inter`. */
@@ -132,8 +188,19 @@ void or_swiglu_ffn(const uint8_t* blk, int wfmt, int64_t H, int64_t inter, const
   const uint8_t* Wg = blk;
   const uint8_t* Wu = blk + matrix_bytes(wfmt, inter, H);
   const uint8_t* WdT = blk + 2 * matrix_bytes(wfmt, inter, H);
-  matvec(Wg, wfmt, inter, H, x, g);
-  matvec(Wu, wfmt, inter, H, x, u);
+  if (wfmt == 2) {
+    int8_t* q = (int8_t*)malloc((size_t)H);
+    float xs;
+    or_quantize_i8(x, H, q, &xs);
+    for (int64_t i = 0; i < inter; ++i) {
+      g[i] = i8_projection(Wg, H, i, q, xs);
+      u[i] = i8_projection(Wu, H, i, q, xs);
+    }
+    free(q);
+  } else {
+    matvec(Wg, wfmt, inter, H, x, g);
+    matvec(Wu, wfmt, inter, H, x, u);
+  }
   for (int64_t i = 0; i < inter; ++i) g[i] = silu(g[i]) * u[i];
   for (int64_t c = 0; c < H; ++c) {
     double acc = 0.0;
@@ -220,8 +287,10 @@ typedef struct {
   int wfmt;
   int64_t H, inter;
   const double* x;
-  double* h; /* [inter] */
-  double* y; /* [H] */
+  const int8_t* qx; /* int8 format: the token's int8 activation [H] */
+  float xs;         /* and its scale */
+  double* h;        /* [inter] */
+  double* y;        /* [H] */
 } ffn_job;
 
 typedef struct {
@@ -238,8 +307,13 @@ static void run_task(const ffn_job* f, int phase, int64_t r0, int64_t r1) {
   if (phase == 0) {
     for (int64_t i = r0; i < r1; ++i) {
       double g = 0.0, u = 0.0;
-      for (int64_t c = 0; c < f->H; ++c) g += weight_at(f->blk, f->wfmt, f->H, i, c) * f->x[c];
-      for (int64_t c = 0; c < f->H; ++c) u += weight_at(f->blk + mb, f->wfmt, f->H, i, c) * f->x[c];
+      if (f->wfmt == 2) {
+        g = i8_projection(f->blk, f->H, i, f->qx, f->xs);
+        u = i8_projection(f->blk + mb, f->H, i, f->qx, f->xs);
+      } else {
+        for (int64_t c = 0; c < f->H; ++c) g += weight_at(f->blk, f->wfmt, f->H, i, c) * f->x[c];
+        for (int64_t c = 0; c < f->H; ++c) u += weight_at(f->blk + mb, f->wfmt, f->H, i, c) * f->x[c];
+      }
       f->h[i] = silu(g) * u;
     }
   } else {
@@ -310,7 +384,7 @@ int or_threads_used(const or_shapes* s, int nthreads) {
 
 /*
  * Full layer for T tokens.  act: 0 = x is fp32 [T,H], 1 = x is bf16 [T,H].
- * wfmt: 0 = bf16 experts and shared expert, 1 = 4-bit blocks.
+ * wfmt: 0 = bf16 experts and shared expert, 1 = 4-bit blocks, 2 = int8 rows.
  * Outputs: out fp32 [T,H]; optional logits fp32 [T,E], ids int32 [T,k],
  * p fp32 [T,k], s fp32 [T].  The result does not depend on nthreads.
  * Returns 0, or -1 on an invalid argument.
@@ -322,6 +396,8 @@ int or_moe_ffn(const or_shapes* s, int act, int wfmt, const void* x, const uint1
   const int64_t T = s->T, H = s->H, E = s->E, k = s->top_k, I = s->I, Is = s->Is;
   if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || I <= 0 || Is <= 0) return -1;
   if (wfmt == 1 && (H % 32 || I % 32 || Is % 32)) return -1;
+  if (wfmt == 2 && H % 16) return -1;
+  if (wfmt < 0 || wfmt > 2) return -1;
   if (T == 0) return 0;
 
   double* xd = (double*)malloc(sizeof(double) * (size_t)(T * H));
@@ -348,16 +424,26 @@ int or_moe_ffn(const or_shapes* s, int act, int wfmt, const void* x, const uint1
   ffn_job* jobs = (ffn_job*)malloc(sizeof(ffn_job) * (size_t)njobs);
   double* y = (double*)malloc(sizeof(double) * (size_t)(njobs * H));
   double* hbuf = (double*)malloc(sizeof(double) * (size_t)(njobs * hmax));
+  /* int8 format: each token's activation quantised once, shared by its FFNs */
+  int8_t* qx = (int8_t*)malloc((size_t)(T * H));
+  float* xs = (float*)malloc(sizeof(float) * (size_t)T);
+  for (int64_t t = 0; t < T; ++t) {
+    xs[t] = 0.0f;
+    if (wfmt == 2) or_quantize_i8(xd + t * H, H, qx + t * H, &xs[t]);
+  }
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t j = 0; j < k; ++j) {
       int64_t n = t * k + j;
-      jobs[n] = (ffn_job){expert_w + (int64_t)ids[n] * eb, wfmt, H, I, xd + t * H, hbuf + n * hmax, y + n * H};
+      jobs[n] = (ffn_job){expert_w + (int64_t)ids[n] * eb, wfmt, H, I, xd + t * H, qx + t * H, xs[t],
+                          hbuf + n * hmax, y + n * H};
     }
     int64_t n = T * k + t;
-    jobs[n] = (ffn_job){shexp_w, wfmt, H, Is, xd + t * H, hbuf + n * hmax, y + n * H};
+    jobs[n] = (ffn_job){shexp_w, wfmt, H, Is, xd + t * H, qx + t * H, xs[t], hbuf + n * hmax, y + n * H};
   }
   run_jobs(jobs, njobs, nthreads);
   free(hbuf);
+  free(qx);
+  free(xs);
 
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t h = 0; h < H; ++h) {

@@ -60,3 +60,21 @@ def test_layer_block_sizes():
         assert L.expert_w.size == s.E * eb
         assert L.shexp_w.size == datagen.expert_bytes(wfmt, s.H, s.Is)
         assert eb % 16 == 0
+
+
+def test_i8_encoder_scale_rounding_and_layout():
+    """Per row: s = fp32(max|w|) / 127, q = round half away from zero of w / s, then s and 12 zero bytes."""
+    w = datagen.f32_to_bf16(np.array([[1.0, -0.5, 0.25, 0.49609375] + [0.0] * 12], np.float32))
+    e = datagen.encode_i8(w)
+    assert e.shape == (1, 32)
+    assert list(e[0, :4].view(np.int8)) == [127, -64, 32, 63]
+    assert e[0, 16:20].view("<f4")[0] == np.float32(1.0) / np.float32(127.0)
+    assert not e[0, 20:].any()
+    z = datagen.encode_i8(np.zeros((1, 16), np.uint16))
+    assert not z.any()
+    rows = datagen.normal_bf16(9, 9, 64 * 256, 0.02).reshape(64, 256)
+    enc = datagen.encode_i8(rows)
+    q = enc[:, :256].view(np.int8).astype(np.float64)
+    s = enc[:, 256:260].copy().view("<f4").astype(np.float64)
+    wf = datagen.bf16_to_f32(rows).astype(np.float64)
+    assert np.all(np.abs(wf - q * s) <= s / 2 * (1 + 1e-6) + 1e-12)

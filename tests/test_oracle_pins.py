@@ -438,3 +438,101 @@ def test_block_step_is_norm_then_layer_then_residual():
     r = oracle.moe_ffn(s, ACT_BF16, WFMT_Q4B32, xn, layer.router_w, layer.expert_w, layer.shexp_w, layer.shexp_gate_w)
     np.testing.assert_array_equal(ids, r["ids"])
     np.testing.assert_array_equal(new, (x_res + r["out"]).astype(np.float32))
+
+
+# ----------------------------------------------------------------------------
+# int8 weights with an int8 activation (the int8 linear of "ggml operator extensions", sd.cpp integration)
+
+
+def test_i8_activation_quantizer_known_values():
+    """max|x| = 127 gives the scale 127 / 127 = 1 exactly, so q is x rounded half away from zero."""
+    x = np.array([127.0, -63.5, 0.5, -0.5, 1.49, -1.5, 2.5, 0.0] + [3.0] * 8)
+    q, s = oracle.quantize_i8(x)
+    assert s == 1.0
+    assert list(q[:8]) == [127, -64, 1, -1, 1, -2, 3, 0]
+    # a scale that is not a power of two: max 1.0 -> 1/127 in fp32; 0.5 / s = 63.5 -> 64
+    q, s = oracle.quantize_i8(np.array([1.0, 0.5, -0.25, -1.0] + [0.0] * 12))
+    assert s == float(np.float32(1.0) / np.float32(127.0))
+    assert list(q[:4]) == [127, 64, -32, -127]
+    q, s = oracle.quantize_i8(np.zeros(16))
+    assert s == 0.0 and not q.any()
+
+
+def test_i8_weight_rows_decode():
+    """An int8 row is its C signed bytes, then its fp32 scale; the value is scale * q."""
+    cols = 32
+    row = np.zeros(cols + 16, np.uint8)
+    qv = (np.arange(cols) - 16).astype(np.int8)
+    row[:cols] = qv.view(np.uint8)
+    row[cols : cols + 4] = np.array([0.25], "<f4").view(np.uint8)
+    np.testing.assert_array_equal(oracle.decode_row(row, datagen.WFMT_I8, cols, 0), qv.astype(np.float64) * 0.25)
+
+
+def _i8_block_dequant(block, H, inter):
+    rb = H + 16
+    mats = []
+    for m in range(3):
+        rows = block[m * inter * rb : (m + 1) * inter * rb].reshape(inter, rb)
+        q = rows[:, :H].view(np.int8).astype(np.float64)
+        sc = rows[:, H : H + 4].copy().view("<f4").astype(np.float64)
+        mats.append(q * sc)
+    return mats
+
+
+def test_i8_ffn_matches_torch_for_integral_activation():
+    """x integral with max|x| = 127: the scale is 1 and the int8 activation is x itself, so the int8 path must
+    equal the plain SwiGLU FFN of the dequantised weights (torch, fp64) up to the fp32 rounding of
+    float(dot) * xs * s."""
+    H, inter = 256, 96
+    block = datagen.expert_block(51, 0, H, inter, datagen.WFMT_I8)
+    Wg, Wu, WdT = (torch.from_numpy(m) for m in _i8_block_dequant(block, H, inter))
+    x = np.round(datagen.normal_f32(51, 3, H).astype(np.float64) * 40.0)
+    x = np.clip(x, -126, 126)
+    x[7] = 127.0
+    xt = torch.from_numpy(x)
+    g, u = Wg @ xt, Wu @ xt
+    h = torch.nn.functional.silu(g) * u
+    ref = h @ WdT
+    y = oracle.swiglu_ffn(block, datagen.WFMT_I8, H, inter, x)
+    # the projections round twice in fp32 (float(dot) is exact here, then * xs = 1 and * s), so h carries a
+    # relative error of a few 2^-24; each output moves by at most that times sum_i |WdT[i,c] h_i|
+    bound = 4e-7 * (h.abs() @ WdT.abs()).numpy() + 1e-12
+    assert np.all(np.abs(y - ref.numpy()) <= bound)
+
+
+def test_i8_ffn_quantization_error_is_bounded():
+    """For a general x the int8 activation differs from x by at most half a step (xs / 2) per element; the
+    resulting change of the FFN output stays within the bound that half a step per element gives through the
+    gate and up projections (checked against torch on the unquantised x, loosely)."""
+    H, inter = 256, 64
+    block = datagen.expert_block(52, 0, H, inter, datagen.WFMT_I8)
+    Wg, Wu, WdT = (torch.from_numpy(m) for m in _i8_block_dequant(block, H, inter))
+    x = datagen.normal_f32(52, 4, H).astype(np.float64)
+    q, s = oracle.quantize_i8(x)
+    assert np.all(np.abs(x - q.astype(np.float64) * s) <= s / 2 * (1 + 1e-6))
+    xq = torch.from_numpy(q.astype(np.float64) * s)
+    ref_q = (torch.nn.functional.silu(Wg @ xq) * (Wu @ xq)) @ WdT
+    y = oracle.swiglu_ffn(block, datagen.WFMT_I8, H, inter, x)
+    # the oracle is the FFN of the quantised activation (up to fp32 rounding of the projections)
+    np.testing.assert_allclose(y, ref_q.numpy(), rtol=1e-5, atol=1e-6 * float(ref_q.abs().max()))
+    ref = (torch.nn.functional.silu(Wg @ torch.from_numpy(x)) * (Wu @ torch.from_numpy(x))) @ WdT
+    assert float((torch.from_numpy(y) - ref).abs().max()) < 0.05 * float(ref.abs().max())
+
+
+def test_i8_zero_activation_gives_zero_output():
+    H, inter = 128, 64
+    block = datagen.expert_block(53, 0, H, inter, datagen.WFMT_I8)
+    y = oracle.swiglu_ffn(block, datagen.WFMT_I8, H, inter, np.zeros(H))
+    assert np.all(y == 0.0)
+
+
+def test_i8_layer_routing_is_format_independent():
+    """The router and the top-k do not depend on the expert weight format."""
+    s = datagen.Shapes(T=3, H=256, E=8, top_k=2, I=64, Is=64)
+    lb = datagen.make_layer(54, with_T(s, 1), WFMT_BF16)
+    li = datagen.make_layer(54, with_T(s, 1), datagen.WFMT_I8)
+    x, _ = draw_tokens(54, lb, 3, ACT_BF16)
+    rb = oracle.moe_ffn(s, ACT_BF16, WFMT_BF16, x, lb.router_w, lb.expert_w, lb.shexp_w, lb.shexp_gate_w)
+    ri = oracle.moe_ffn(s, ACT_BF16, datagen.WFMT_I8, x, li.router_w, li.expert_w, li.shexp_w, li.shexp_gate_w)
+    np.testing.assert_array_equal(rb["ids"], ri["ids"])
+    np.testing.assert_array_equal(rb["p"], ri["p"])
