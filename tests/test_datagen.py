@@ -77,4 +77,5 @@ def test_i8_encoder_scale_rounding_and_layout():
     q = enc[:, :256].view(np.int8).astype(np.float64)
     s = enc[:, 256:260].copy().view("<f4").astype(np.float64)
     wf = datagen.bf16_to_f32(rows).astype(np.float64)
-    assert np.all(np.abs(wf - q * s) <= s / 2 * (1 + 1e-6) + 1e-12)
+    # w / s is formed in fp32 before the rounding: up to 127 * 2^-24 beyond half a step
+    assert np.all(np.abs(wf - q * s) <= s * (0.5 + 1e-5) + 1e-12)
