@@ -31,6 +31,7 @@ ACT_F32 = 0
 ACT_BF16 = 1
 W_BF16 = 0
 W_Q4B32 = 1
+W_I8 = 2
 
 QUERY_PATH = 0
 QUERY_LAUNCHES_PER_EXECUTE = 1

@@ -221,7 +221,9 @@ int run_two_stream(moe_ffn_plan_t plan, cudaStream_t stream, cudaStream_t aux, c
   // SMs split by the bytes each branch streams (the routed branch at its
   // largest number of distinct experts), so that both grids are resident at
   // once: every grid waits at grid-wide barriers for all of its blocks.
-  const double eb = (plan->wfmt == MOE_FFN_W_Q4B32 ? 9.0 / 16.0 : 2.0) * 3.0 * s.H;
+  const double eb = 3.0 * (plan->wfmt == MOE_FFN_W_Q4B32 ? 9.0 / 16.0 * s.H
+                                : plan->wfmt == MOE_FFN_W_I8  ? s.H + 16.0
+                                                              : 2.0 * s.H);
   const double b_sh = eb * s.Is, b_r = eb * s.I * (double)(s.E < s.T * s.top_k ? s.E : s.T * s.top_k);
   int Gs = (int)(G * b_sh / (b_sh + b_r) + 0.5);
   Gs = Gs < 1 ? 1 : (Gs > G - 1 ? G - 1 : Gs);
@@ -274,7 +276,8 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   *plan = nullptr;
   const moe_ffn_shapes s = *shapes;
   if (dtype.act != MOE_FFN_ACT_F32 && dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_INVALID_ARG;
-  if (dtype.wfmt != MOE_FFN_W_BF16 && dtype.wfmt != MOE_FFN_W_Q4B32) return MOE_FFN_ERR_INVALID_ARG;
+  if (dtype.wfmt != MOE_FFN_W_BF16 && dtype.wfmt != MOE_FFN_W_Q4B32 && dtype.wfmt != MOE_FFN_W_I8)
+    return MOE_FFN_ERR_INVALID_ARG;
   if (s.T < 1 || s.T > kBatchMaxT || s.E < 1 || s.E > kMaxExperts || s.top_k < 1 || s.top_k > s.E ||
       s.top_k > kMaxTopK || s.H < 1 || s.I < 1 || s.Is < 1)
     return MOE_FFN_ERR_UNSUPPORTED;
@@ -282,13 +285,15 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   const int path = s.T > kDecodeMaxT ? 1 : 0;
   if (path == 0) {
     // Decode path: T <= 8; stored rows of H elements (bf16: H a multiple of
-    // 8, 4-bit: of 256, so that rows are 16-byte multiples); H <= 4096.
+    // 8, 4-bit: of 256, int8: of 16, so that rows are 16-byte multiples);
+    // H <= 4096.
     if (s.H > kMaxH) return MOE_FFN_ERR_UNSUPPORTED;
-    if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : 256)) return MOE_FFN_ERR_UNSUPPORTED;
+    if (s.H % (dtype.wfmt == MOE_FFN_W_BF16 ? 8 : dtype.wfmt == MOE_FFN_W_I8 ? 16 : 256))
+      return MOE_FFN_ERR_UNSUPPORTED;
   } else {
     // Batched path (grouped GEMMs): bf16 or 4-bit weights, bf16 activation, E <= 256,
     // tiles of 256 columns of H and 128 rows of I and Is.
-    if (dtype.act != MOE_FFN_ACT_BF16) return MOE_FFN_ERR_UNSUPPORTED;
+    if (dtype.act != MOE_FFN_ACT_BF16 || dtype.wfmt == MOE_FFN_W_I8) return MOE_FFN_ERR_UNSUPPORTED;
     if (s.E > kBatchMaxE || s.H % 256 || s.I % 128 || s.Is % 128) return MOE_FFN_ERR_UNSUPPORTED;
     if ((long long)s.E * 3 * s.I >= (1LL << 31) || 3LL * s.Is >= (1LL << 31)) return MOE_FFN_ERR_UNSUPPORTED;
   }

@@ -62,7 +62,7 @@ struct LayerParams {
   // shapes
   int T, H, E, K, I, Is;
   int act;   // 0 fp32 x, 1 bf16 x
-  int wfmt;  // 0 bf16 weights, 1 4-bit blocks
+  int wfmt;  // 0 bf16 weights, 1 4-bit blocks, 2 int8 rows (int8 activation)
   int block_mode;
   float eps;
   int G;  // grid of the row kernel

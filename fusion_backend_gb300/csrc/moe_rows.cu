@@ -3,9 +3,13 @@
 
 #include <algorithm>
 
+#include "moe_ffn.h"
 #include "moe_rows.cuh"
 
 namespace moe {
+
+static_assert(kWkBf16 == MOE_FFN_W_BF16 && kWkQ4 == MOE_FFN_W_Q4B32 && kWkI8 == MOE_FFN_W_I8,
+              "weight kinds follow the public weight formats");
 
 cudaError_t launch_rows_bf16_fast(const LayerParams& p, cudaStream_t stream);
 cudaError_t launch_rows_q4_fast(const LayerParams& p, cudaStream_t stream);
@@ -13,10 +17,16 @@ cudaError_t launch_rows_generic(const LayerParams& p, cudaStream_t stream);
 
 namespace {
 
-// The fast (tensor-core) instances: H = 2048, E <= 256, and an activation
-// that bf16 holds exactly -- bf16 x, or the block form whose normalised
-// input is bf16 -- so that it enters the bf16 products unchanged.
-bool rows_fast(const LayerParams& p) { return p.H == 2048 && p.E <= 256 && (p.act == 1 || p.block_mode); }
+// The fast (tensor-core) instances: bf16 or 4-bit weights, H = 2048,
+// E <= 256, and an activation that bf16 holds exactly -- bf16 x, or the
+// block form whose normalised input is bf16 -- so that it enters the bf16
+// products unchanged.  Int8 weights run the general instances.
+bool rows_fast(const LayerParams& p) {
+  return p.wfmt != kWkI8 && p.H == 2048 && p.E <= 256 && (p.act == 1 || p.block_mode);
+}
+
+// Rows per stage at most, by weight format.
+int rows_rsm(int wfmt) { return wfmt == kWkBf16 ? kRsMaxB16 : kRsMaxQ4; }
 
 int align128(int v) { return (v + 127) & ~127; }
 
@@ -29,9 +39,10 @@ static bool rows_layout_rs(LayerParams& p, int rs, int xbytes, int tab, int tmax
   p.stage_bytes = 3 * rs * p.rp;
   p.off_bar = 0;
   p.off_tab = 256;
-  const int rsm = p.wfmt == 1 ? kRsMaxQ4 : kRsMaxB16;
+  const int rsm = rows_rsm(p.wfmt);
   p.off_h = align128(p.off_tab + tab);
-  p.off_part = align128(p.off_h + 2 * rsm * tmax * 4);
+  // h by stage parity, then (int8) the stage's row scales by parity
+  p.off_part = align128(p.off_h + 2 * rsm * tmax * 4 + 2 * 3 * kRsMaxQ4 * 4);
   p.off_x = align128(p.off_part + 2 * kRowWarps * 2 * rsm * tmax * 4);
   p.off_ring = (p.off_x + xbytes + 1023) & ~1023;  // 128-byte-swizzled tensor copies want 1024-byte alignment
   if (p.off_ring >= kSmemBudget) return false;
@@ -60,11 +71,11 @@ static bool rows_layout_rs(LayerParams& p, int rs, int xbytes, int tab, int tmax
 
 int rows_layout(LayerParams& p) {
   if (p.T < 1 || p.T > kDecodeMaxT || p.H < 8 || p.H > kMaxH || p.G < 1 || p.G > kMaxGrid) return -1;
-  const bool q4 = p.wfmt == 1;
-  if (q4 ? (p.H % 256) : (p.H % 8)) return -1;
+  if (p.wfmt < kWkBf16 || p.wfmt > kWkI8) return -1;
+  if (p.H % (p.wfmt == kWkQ4 ? 256 : p.wfmt == kWkI8 ? 16 : 8)) return -1;
   const bool fast = rows_fast(p);
   const int tmax = fast ? tmax_for(p.T) : 8;
-  p.rb = q4 ? (long long)p.H * 9 / 16 : (long long)p.H * 2;
+  p.rb = p.wfmt == kWkQ4 ? (long long)p.H * 9 / 16 : p.wfmt == kWkI8 ? (long long)p.H + 16 : (long long)p.H * 2;
   p.expert_bytes = 3LL * p.I * p.rb;
   p.xmode = fast ? kXReg : kXF32;
   // x region: the bulk copy of the source rows (fp32 for fp32 x and the block
@@ -79,8 +90,8 @@ int rows_layout(LayerParams& p) {
   int best_rs = 0;
   long long best_flight = -1;
   for (int r = 0; r < 4; ++r) {
-    if (rs_list[r] > (q4 ? kRsMaxQ4 : kRsMaxB16)) continue;
-    if (fast && rs_list[r] != (q4 ? kRsMaxQ4 : kRsMaxB16)) continue;  // tensor-core stages: fixed rows
+    if (rs_list[r] > rows_rsm(p.wfmt)) continue;
+    if (fast && rs_list[r] != rows_rsm(p.wfmt)) continue;  // tensor-core stages: fixed rows
     LayerParams t = p;
     if (!rows_layout_rs(t, rs_list[r], xbytes, tab, tmax)) continue;
     const long long flight = (long long)t.ns * t.stage_bytes + (long long)t.nsd * t.rs * t.rp;
@@ -133,7 +144,7 @@ cudaError_t rows_tensor_maps(LayerParams& p) {
   if (!rows_fast(p)) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const int rs = p.wfmt == 1 ? kRsMaxQ4 : kRsMaxB16;
+  const int rs = rows_rsm(p.wfmt);
   const int rb = (int)p.rb;
   if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, rb, p.I, p.E, rs, 2) ||
       !encode_rows(fn, &p.tm_d_e, p.expert_w, rb, p.I, p.E, rs, 1) ||

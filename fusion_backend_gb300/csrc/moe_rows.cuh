@@ -63,7 +63,8 @@ enum : int { kXReg = 0, kXF32 = 1 };
 constexpr int kMaxStagesRing = 8;
 constexpr int kBarStage = 1;  // named barrier of the compute warps, once per stage
 constexpr int kRsMaxB16 = 4;  // rows per stage, bf16 weights
-constexpr int kRsMaxQ4 = 8;   // rows per stage, 4-bit weights
+constexpr int kRsMaxQ4 = 8;   // rows per stage, 4-bit and int8 weights
+enum : int { kWkBf16 = 0, kWkQ4 = 1, kWkI8 = 2 };  // weight kinds (the plan's wfmt)
 
 // Routing tables of one block, carved from shared memory with sizes of the
 // plan (T tokens, K per token, E experts).
@@ -79,14 +80,15 @@ struct RowTab {
   float* wt;         // [T*K][T] weight of token t for active expert u (0 if not routed)
   int32_t* misc;     // [4] the number of active experts U
   int32_t* qtab;     // [T*K - K + 1][4] per possible U: routed stages, first active expert, first group
+  uint32_t* xmax;    // [T] int8 activation: bits of max |x| of token t
 };
 
 __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTab* v) {
   const int TK = T * K;
-  const int sz[11] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
-                      (TK - K + 1) * 16};
-  int off = 0, o[11];
-  for (int i = 0; i < 11; ++i) {
+  const int sz[12] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
+                      (TK - K + 1) * 16, T * 4};
+  int off = 0, o[12];
+  for (int i = 0; i < 12; ++i) {
     o[i] = off;
     off += (sz[i] + 15) & ~15;
   }
@@ -102,6 +104,7 @@ __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTa
     v->wt = reinterpret_cast<float*>(base + o[8]);
     v->misc = reinterpret_cast<int32_t*>(base + o[9]);
     v->qtab = reinterpret_cast<int32_t*>(base + o[10]);
+    v->xmax = reinterpret_cast<uint32_t*>(base + o[11]);
   }
   return off;
 }
@@ -116,6 +119,12 @@ MOE_DEV uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t c) {
 // nibble OR-ed into the mantissa of 2^23 reads 2^23 + n).
 MOE_DEV float nib_f32(uint32_t w, int j) {
   return __fsub_rn(__uint_as_float(0x4B000000u | ((w >> (4 * j)) & 0xFu)), 8388616.0f);
+}
+// Signed byte j of a 32-bit word as a float (exact: the byte with its sign
+// bit flipped, c + 128 in 0..255, placed in the mantissa of 2^23 reads
+// 2^23 + c + 128).
+MOE_DEV float i8_f32(uint32_t w, int j) {
+  return __fsub_rn(__uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u + j)), 8388736.0f);
 }
 
 // v[0..7] per lane -> the warp sum of v[(lane >> 2) & 7], in every lane of the
@@ -306,10 +315,14 @@ MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int n
 }
 
 // ------------------------------------------------------------------- kernel
-// TMAX: token capacity (T <= TMAX).  Q4: 4-bit weights.  FAST: H = 2048,
-// E <= 256 and a bf16-exact activation (the tensor-core loops).
-template <int TMAX, bool Q4, bool FAST, int NCH>
+// TMAX: token capacity (T <= TMAX).  WK: weight kind (kWkBf16, kWkQ4,
+// kWkI8).  FAST: H = 2048, E <= 256 and a bf16-exact activation (the
+// tensor-core loops; bf16 and 4-bit weights).
+template <int TMAX, int WK, bool FAST, int NCH>
 __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
+  constexpr bool Q4 = WK == kWkQ4;
+  constexpr bool I8 = WK == kWkI8;  // int8 weights and activation: CUDA-core loop
+  static_assert(!(I8 && FAST), "int8 weights run the general loop");
   constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;                  // 4-bit tensor-core loop
   constexpr bool Q4MC = Q4C && TMAX >= 4;           // 4-bit: tensor-core down projection
@@ -440,6 +453,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     for (int i = lane; i < (P.E + 31) / 32; i += 32) tb.bitmap[i] = 0u;
     for (int i = lane; i < TK; i += 32) tb.mask[i] = 0u;
     for (int i = lane; i < TK * T; i += 32) tb.wt[i] = 0.f;
+    for (int i = lane; i < T; i += 32) tb.xmax[i] = 0u;
   } else if (warp == 2) {
     // the routed run of this block for every possible count U of active
     // experts (K <= U <= min(E, T K)): groups [q0, q1) of the flattened
@@ -646,15 +660,52 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
                      P.block_mode ? tb.inv[2 * t + 1] : 0.f, 8 * q, v[k]);
       }
     }
-    __syncthreads();
+    if constexpr (I8) {
+      // int8 activation: max |x| of every token (non-negative floats order
+      // as their bit patterns)
 #pragma unroll
-    for (int k = 0; k < kMaxGroups; ++k) {
-      const int gi = tid + kRowThreads * k;
-      if (gi < groups) {
-        const int t = gi / (H / 8), q = gi % (H / 8);
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(xs) + (size_t)t * H + 8 * q);
-        dst[0] = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
-        dst[1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
+      for (int k = 0; k < kMaxGroups; ++k) {
+        const int gi = tid + kRowThreads * k;
+        if (gi < groups) {
+          float m = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[k][e]));
+          atomicMax(&tb.xmax[gi / (H / 8)], __float_as_uint(m));
+        }
+      }
+    }
+    __syncthreads();
+    if constexpr (I8) {
+      // token t's codes at xs + t H (bytes), its scale x_scale = max|x| / 127
+      // at float index t after the T rows: q = round-half-away(x / x_scale)
+      // clamped to +-127, all in fp32 (x_scale = 0: q = 0)
+#pragma unroll
+      for (int k = 0; k < kMaxGroups; ++k) {
+        const int gi = tid + kRowThreads * k;
+        if (gi < groups) {
+          const int t = gi / (H / 8), q = gi % (H / 8);
+          const float sc = __fdiv_rn(__uint_as_float(tb.xmax[t]), 127.0f);
+          uint32_t w[2] = {0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            int c = 0;
+            if (sc != 0.f) c = max(-127, min(127, (int)roundf(__fdiv_rn(v[k][e], sc))));
+            w[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+          }
+          *reinterpret_cast<uint2*>(xs + (size_t)t * H + 8 * q) = make_uint2(w[0], w[1]);
+        }
+      }
+      if (tid < T) reinterpret_cast<float*>(xs + (size_t)T * H)[tid] = __fdiv_rn(__uint_as_float(tb.xmax[tid]), 127.0f);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kMaxGroups; ++k) {
+        const int gi = tid + kRowThreads * k;
+        if (gi < groups) {
+          const int t = gi / (H / 8), q = gi % (H / 8);
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(xs) + (size_t)t * H + 8 * q);
+          dst[0] = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
+          dst[1] = make_float4(v[k][4], v[k][5], v[k][6], v[k][7]);
+        }
       }
     }
   }
@@ -791,7 +842,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // after the stage barrier a few threads (spread over the warps) form
   // h = w silu(g) u (A2), which C uses one stage later -- one block barrier
   // per stage, and C of stage s overlaps A2 of stage s + 1.
-  constexpr int RSM = Q4 ? kRsMaxQ4 : kRsMaxB16;
+  constexpr int RSM = Q4 || I8 ? kRsMaxQ4 : kRsMaxB16;
   constexpr int NV = 2 * RSM * TMAX;  // dot values per warp per stage: (row, gate|up, token)
   float* part = reinterpret_cast<float*>(sm + P.off_part);  // [2][kRowWarps][NV]
   float* hb = reinterpret_cast<float*>(sm + P.off_h);       // [2][RSM][TMAX]
@@ -1129,9 +1180,15 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   } else {
 
     // downT chunks of this thread, by stage parity
-    uint4 dwb[2][Q4 ? 1 : RSM][NCH];
+    constexpr bool B16 = !Q4 && !I8;
+    uint4 dwb[2][B16 ? RSM : 1][NCH];
     uint32_t dwq[2][Q4 ? RSM : 1][NCH];
     uint16_t dsc[2][Q4 ? RSM : 1][NCH];
+    uint2 dwi[2][I8 ? RSM : 1][NCH];
+    // int8: the stage's row scales (gate, up, downT) by stage parity, and
+    // the activation scales
+    float* wsc = hb + 2 * RSM * TMAX;  // [2][3][RSM]
+    const float* xsc = reinterpret_cast<const float*>(xs + (size_t)T * H);
     int n_prev = 0;
     uint32_t m_prev = 0u;
     StageCursor cs;
@@ -1149,9 +1206,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         rows_of(cs, si0, n);
         const uint8_t* sl = ring + (size_t)slot * P.stage_bytes;
         // this thread's chunks of every row of the stage, into registers
-        uint4 wgb[Q4 ? 1 : RSM][NCH], wub[Q4 ? 1 : RSM][NCH];
+        uint4 wgb[B16 ? RSM : 1][NCH], wub[B16 ? RSM : 1][NCH];
         uint32_t wgq[Q4 ? RSM : 1][NCH], wuq[Q4 ? RSM : 1][NCH];
         uint16_t sgq[Q4 ? RSM : 1][NCH], suq[Q4 ? RSM : 1][NCH];
+        uint2 wgi[I8 ? RSM : 1][NCH], wui[I8 ? RSM : 1][NCH];
+        if constexpr (I8) {
+          // the scale after each row's H codes
+          if (warp == 0 && lane < 3 * RSM) {
+            const int m = lane / RSM, r = lane % RSM;
+            if (r < n) wsc[(par * 3 + m) * RSM + r] = *reinterpret_cast<const float*>(sl + (size_t)(m * RS + r) * rp + H);
+          }
+        }
 #pragma unroll
         for (int r = 0; r < RSM; ++r) {
           if (r < n) {
@@ -1162,10 +1227,14 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
             for (int k = 0; k < NCH; ++k) {
               const int ch = tid + kRowThreads * k;
               if (FAST || ch < H / 8) {
-                if (!Q4) {
-                  wgb[Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(rg + (size_t)ch * 16);
-                  wub[Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(ru + (size_t)ch * 16);
-                  dwb[par][Q4 ? 0 : r][k] = *reinterpret_cast<const uint4*>(rd + (size_t)ch * 16);
+                if constexpr (I8) {
+                  wgi[I8 ? r : 0][k] = *reinterpret_cast<const uint2*>(rg + (size_t)ch * 8);
+                  wui[I8 ? r : 0][k] = *reinterpret_cast<const uint2*>(ru + (size_t)ch * 8);
+                  dwi[par][I8 ? r : 0][k] = *reinterpret_cast<const uint2*>(rd + (size_t)ch * 8);
+                } else if constexpr (B16) {
+                  wgb[B16 ? r : 0][k] = *reinterpret_cast<const uint4*>(rg + (size_t)ch * 16);
+                  wub[B16 ? r : 0][k] = *reinterpret_cast<const uint4*>(ru + (size_t)ch * 16);
+                  dwb[par][B16 ? r : 0][k] = *reinterpret_cast<const uint4*>(rd + (size_t)ch * 16);
                 } else {
                   const int so = H / 2 + 2 * (ch >> 2);
                   wgq[Q4 ? r : 0][k] = *reinterpret_cast<const uint32_t*>(rg + (size_t)ch * 4);
@@ -1211,8 +1280,21 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
             for (int k = 0; k < NCH; ++k) {
               const int ch = tid + kRowThreads * k;
               if (!FAST && ch >= H / 8) break;
-              if (!Q4) {
-                const uint4 vg = wgb[Q4 ? 0 : r][k], vu = wub[Q4 ? 0 : r][k];
+              if constexpr (I8) {
+                // exact int32 dot products of the codes (each thread's part
+                // stays below 2^24, so the fp32 warp sums are exact too)
+                const uint2 vg = wgi[I8 ? r : 0][k], vu = wui[I8 ? r : 0][k];
+#pragma unroll
+                for (int t = 0; t < TMAX; ++t) {
+                  if (!(mrow[r] >> t & 1u)) continue;
+                  const uint2 xq = *reinterpret_cast<const uint2*>(xs + (size_t)t * H + 8 * ch);
+                  const int gd = __dp4a((int)vg.y, (int)xq.y, __dp4a((int)vg.x, (int)xq.x, 0));
+                  const int ud = __dp4a((int)vu.y, (int)xq.y, __dp4a((int)vu.x, (int)xq.x, 0));
+                  ga[t] += (float)gd;
+                  ua[t] += (float)ud;
+                }
+              } else if constexpr (B16) {
+                const uint4 vg = wgb[B16 ? r : 0][k], vu = wub[B16 ? r : 0][k];
                 const float gf[8] = {bf16_lo(vg.x), bf16_hi(vg.x), bf16_lo(vg.y), bf16_hi(vg.y),
                                      bf16_lo(vg.z), bf16_hi(vg.z), bf16_lo(vg.w), bf16_hi(vg.w)};
                 const float uf[8] = {bf16_lo(vu.x), bf16_hi(vu.x), bf16_lo(vu.y), bf16_hi(vu.y),
@@ -1281,16 +1363,32 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           const int r = j / TMAX, t = j % TMAX;
           const float* pp = part + (size_t)par * kRowWarps * NV;
           float g = 0.f, u = 0.f;
+          if constexpr (I8) {
+            // int32 sums of the exact warp partials; then
+            // g = float(dot) * x_scale * s_gate in fp32, in that order (u alike)
+            int gi = 0, ui = 0;
 #pragma unroll
-          for (int w = 0; w < kRowWarps; ++w) {
-            g += pp[w * NV + (2 * r) * TMAX + t];
-            u += pp[w * NV + (2 * r + 1) * TMAX + t];
+            for (int w = 0; w < kRowWarps; ++w) {
+              gi += __float2int_rn(pp[w * NV + (2 * r) * TMAX + t]);
+              ui += __float2int_rn(pp[w * NV + (2 * r + 1) * TMAX + t]);
+            }
+            const float xsc_t = t < T ? xsc[t] : 0.f;
+            g = __fmul_rn(__fmul_rn(__int2float_rn(gi), xsc_t), wsc[(par * 3 + 0) * RSM + r]);
+            u = __fmul_rn(__fmul_rn(__int2float_rn(ui), xsc_t), wsc[(par * 3 + 1) * RSM + r]);
+          } else {
+#pragma unroll
+            for (int w = 0; w < kRowWarps; ++w) {
+              g += pp[w * NV + (2 * r) * TMAX + t];
+              u += pp[w * NV + (2 * r + 1) * TMAX + t];
+            }
           }
           float h = 0.f;
           if (su < 0)
             h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
           else
             h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
+          // int8: the downT row's scale goes with h (y += (h s) q)
+          if constexpr (I8) h *= wsc[(par * 3 + 2) * RSM + r];
           hb[par * RSM * TMAX + j] = h;
         }
       }
@@ -1310,8 +1408,15 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
               if (!FAST && ch >= H / 8) break;
               float w[8];
               float sc = 1.f;  // 4-bit: the block scale d, applied to h
-              if (!Q4) {
-                const uint4 v = dwb[pp][Q4 ? 0 : r][k];
+              if constexpr (I8) {
+                const uint2 v = dwi[pp][I8 ? r : 0][k];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  w[e] = i8_f32(v.x, e);
+                  w[e + 4] = i8_f32(v.y, e);
+                }
+              } else if constexpr (B16) {
+                const uint4 v = dwb[pp][B16 ? r : 0][k];
                 w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
                 w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
               } else {
@@ -1450,10 +1555,10 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 // blocks (G <= the SM count) resident at once.  A launch whose blocks could
 // not all be resident is refused (cudaErrorCooperativeLaunchTooLarge) instead
 // of ending in a timed-out barrier.
-template <int TMAX, bool Q4, bool FAST, int NCH>
+template <int TMAX, int WK, bool FAST, int NCH>
 inline cudaError_t rows_configure(int smem, int G) {
   // one record per instance (the statics of each template instantiation)
-  auto* const kern = k_rows<TMAX, Q4, FAST, NCH>;
+  auto* const kern = k_rows<TMAX, WK, FAST, NCH>;
   constexpr int kDevs = 64;
   static std::atomic<int> done_smem[kDevs];
   static std::mutex mu;
@@ -1476,9 +1581,9 @@ inline cudaError_t rows_configure(int smem, int G) {
   return cudaSuccess;
 }
 
-template <int TMAX, bool Q4, bool FAST, int NCH = 1>
+template <int TMAX, int WK, bool FAST, int NCH = 1>
 inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
-  cudaError_t err = rows_configure<TMAX, Q4, FAST, NCH>(p.smem, p.G);
+  cudaError_t err = rows_configure<TMAX, WK, FAST, NCH>(p.smem, p.G);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1490,7 +1595,7 @@ inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kRowThreads);
   cfg.dynamicSmemBytes = p.smem;
-  return cudaLaunchKernelEx(&cfg, k_rows<TMAX, Q4, FAST, NCH>, p);
+  return cudaLaunchKernelEx(&cfg, k_rows<TMAX, WK, FAST, NCH>, p);
 }
 
 }  // namespace moe

@@ -7,10 +7,10 @@ namespace moe {
 
 cudaError_t launch_rows_q4_fast(const LayerParams& p, cudaStream_t stream) {
   switch (tmax_for(p.T)) {
-    case 1: return launch_rows_t<1, true, true>(p, stream);
-    case 2: return launch_rows_t<2, true, true>(p, stream);
-    case 4: return launch_rows_t<4, true, true>(p, stream);
-    default: return launch_rows_t<8, true, true>(p, stream);
+    case 1: return launch_rows_t<1, kWkQ4, true>(p, stream);
+    case 2: return launch_rows_t<2, kWkQ4, true>(p, stream);
+    case 4: return launch_rows_t<4, kWkQ4, true>(p, stream);
+    default: return launch_rows_t<8, kWkQ4, true>(p, stream);
   }
 }
 

@@ -86,7 +86,19 @@ typedef enum {
    * Row layout: C/2 bytes of codes (element 2j in the low nibble of byte j,
    * element 2j+1 in the high nibble), then C/32 little-endian fp16 scales;
    * 9*C/16 bytes per row of C elements. */
-  MOE_FFN_W_Q4B32 = 1
+  MOE_FFN_W_Q4B32 = 1,
+  /* int8 rows with one fp32 scale per stored row (the int8 linear,
+   * sd.linear_i8.v1, of "ggml operator extensions", section "sd.cpp
+   * integration"): weight = s * q, q in -127..127.  Row layout: C int8 codes, the
+   * little-endian fp32 scale s, 12 zero bytes; C + 16 bytes per row of C
+   * elements.  The activation is quantised per token to int8 in fp32
+   * (x_scale = max|x| / 127, q = round-half-away(x / x_scale) clamped to
+   * +-127; x_scale = 0 gives q = 0), the gate and up projections are exact
+   * int32 dot products, g = float(int32_dot) * x_scale * s in fp32 in that
+   * order (likewise u), then SwiGLU; the down projection takes the
+   * dequantised rows s * q of the transposed down matrix.  Decode path only
+   * (T <= 8), H a multiple of 16. */
+  MOE_FFN_W_I8 = 2
 } moe_ffn_weight_format;
 
 typedef struct {
@@ -101,8 +113,8 @@ typedef struct moe_ffn_plan* moe_ffn_plan_t;
  * Host only: no device call, no launch, no device allocation.
  * Supported:
  *   decode path, 1 <= T <= 8: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
- *     H <= 4096 and a multiple of 8 (bf16 weights) or of 256 (4-bit
- *     weights), I, Is >= 1; x fp32 or bf16;
+ *     H <= 4096 and a multiple of 8 (bf16 weights), of 256 (4-bit
+ *     weights) or of 16 (int8 weights), I, Is >= 1; x fp32 or bf16;
  *   batched path, 9 <= T <= 1024 (routing, expert-sorted gather, grouped
  *     GEMMs on the tcgen05 tensor cores, fixed-order combine): bf16 or 4-bit
  *     weights and bf16 x, E <= 256, top_k <= 32, H a multiple of 256, I and

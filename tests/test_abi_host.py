@@ -56,6 +56,8 @@ def test_prepare_reports_workspace_without_device(lib):
         (datagen.Shapes(64, 128, 8, 2, 128, 256), fb.W_BF16),     # T > 8: H a multiple of 256
         (datagen.Shapes(64, 256, 8, 2, 192, 256), fb.W_BF16),     # T > 8: I a multiple of 128
         (datagen.Shapes(64, 256, 300, 2, 128, 256), fb.W_BF16),   # T > 8: E <= 256
+        (datagen.Shapes(1, 264, 8, 2, 128, 256), fb.W_I8),        # int8 rows need H a multiple of 16
+        (datagen.Shapes(64, 256, 8, 2, 128, 256), fb.W_I8),       # int8 weights: decode path only
     ],
 )
 def test_prepare_rejects_unsupported(lib, shapes, wfmt):
@@ -90,6 +92,15 @@ def test_prepare_batched_q4_plan_and_workspace(lib):
     # x by slot incl. the shared slots (fp16), h by slot (fp16), y by slot (fp32)
     assert ws >= (TK + s.T) * s.H * 2 + (TK + s.T) * s.I * 2 + (TK + s.T) * s.H * 4
     fb.moe_ffn_destroy(plan)
+
+
+def test_prepare_int8_decode_plan(lib):
+    for s in (datagen.Shapes(1, 2048, 128, 8, 768, 512), datagen.Shapes(8, 272, 8, 2, 130, 70)):
+        plan, ws = fb.moe_ffn_prepare(s, fb.ACT_BF16, fb.W_I8)
+        assert ws > 0 and ws % 256 == 0
+        assert fb.moe_ffn_query(plan, fb.QUERY_PATH) == 0
+        assert fb.moe_ffn_query(plan, fb.QUERY_LAUNCHES_PER_EXECUTE) == 1
+        fb.moe_ffn_destroy(plan)
 
 
 def test_prepare_rejects_bad_enums_and_nulls(lib):
