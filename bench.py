@@ -19,7 +19,7 @@ Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (the reference arm).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
-       [--config decode_bf16|decode_q4|batched_bf16|batched_q4|stack_q4] [--T T] [--no-extras] [--no-cpu-baseline]
+       [--config decode_bf16|decode_q4|decode_i8|batched_bf16|batched_q4|stack_q4] [--T T] [--no-extras] [--no-cpu-baseline]
 """
 
 from __future__ import annotations
@@ -56,7 +56,8 @@ NCU_TRAFFIC_BYTES = {("decode_bf16", 1): 83_925_760, ("decode_q4", 1): 23_644_67
 # Extra workloads measured in the default N=1 run: (config, T, steps, warm-up steps, oracle budget in s)
 EXTRAS = [("decode_bf16", 8, 400, 20, 3.0), ("two_stream_bf16", 1, 400, 20, 0.0), ("two_stream_bf16", 8, 400, 20, 0.0),
           ("decode_q4", 1, 400, 20, 3.0), ("decode_q4", 2, 400, 20, 3.0),
-          ("decode_q4", 4, 400, 20, 3.0), ("decode_q4", 8, 400, 20, 3.0), ("batched_bf16", 64, 64, 5, 3.0),
+          ("decode_q4", 4, 400, 20, 3.0), ("decode_q4", 8, 400, 20, 3.0), ("decode_i8", 1, 400, 20, 3.0),
+          ("decode_i8", 8, 400, 20, 3.0), ("batched_bf16", 64, 64, 5, 3.0),
           ("batched_bf16", 256, 64, 5, 4.0), ("batched_q4", 64, 64, 5, 3.0), ("batched_q4", 256, 64, 5, 4.0),
           ("stack_q4", 1, 32, 3, 6.0)]
 
@@ -98,7 +99,14 @@ def whole_job(ms_local: float, units_per_rank: int, world: int, dist=None, devic
 
 
 def wfmt_of(cfg: str) -> int:
+    if cfg == "decode_i8":
+        return datagen.WFMT_I8
     return datagen.WFMT_Q4B32 if cfg in ("decode_q4", "batched_q4", "stack_q4") else datagen.WFMT_BF16
+
+
+def dtype_of(wfmt: int) -> str:
+    return {datagen.WFMT_BF16: "bf16", datagen.WFMT_Q4B32: "q4b32 weights, fp32 accumulate",
+            datagen.WFMT_I8: "int8 weights and per-token int8 activation, int32 dot, fp32 epilogue"}[wfmt]
 
 
 def workload(cfg: str, T: int):
@@ -110,6 +118,8 @@ def workload(cfg: str, T: int):
                            f"gated shared expert on a forked stream, event join, join add): T={T}, H={H}, E={E}, "
                            f"top_k={K_TOP}, I={I}, Is={IS}",
         "decode_q4": f"decode 4-bit MoE FFN layer (blocks of 32, fp16 scale): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
+        "decode_i8": f"decode int8 MoE FFN layer (int8 rows + fp32 row scale, int8 activation per token): T={T}, H={H}, "
+                     f"E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_bf16": f"batched bf16 MoE FFN layer (grouped GEMMs): T={T}, H={H}, E={E}, top_k={K_TOP}, I={I}, Is={IS}",
         "batched_q4": f"batched 4-bit MoE FFN layer (grouped GEMMs, fp16 operands): T={T}, H={H}, E={E}, top_k={K_TOP}, "
                       f"I={I}, Is={IS}",
@@ -541,7 +551,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=None, help="default: 200 decode, 20 batched, 8 stack")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="decode_bf16",
-                    choices=["decode_bf16", "decode_q4", "batched_bf16", "batched_q4", "stack_q4"])
+                    choices=["decode_bf16", "decode_q4", "decode_i8", "batched_bf16", "batched_q4", "stack_q4"])
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="measure the selected workload only")
@@ -637,7 +647,7 @@ def main():
             "metric": METRIC, "value": main_r["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": main_r["warmup"], "ms_per_step": main_r["ms_per_step"], "us_per_layer": main_r["us_per_layer"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if wfmt == datagen.WFMT_BF16 else "q4b32 weights, fp32 accumulate", "data": "synthetic",
+            "dtype": dtype_of(wfmt), "data": "synthetic",
             "config": cfg_block, "roofline": main_r["roofline"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": main_r["gpu_launches"], "clocks": main_r["clocks"],
         }
