@@ -102,17 +102,24 @@ struct LayerParams {
   int ns;           // stages in the ring (tensor-core path: gate + up boxes)
   int nsd;          // tensor-core path: downT boxes in their own ring
   int rp;           // row pitch in a ring slot (rb)
-  int stage_bytes;  // 3 * rs * rb
+  int stage_bytes;  // 3 * rs * rb (tensor-core path: one gate + up slot)
+  int dstage_bytes; // tensor-core path: one downT slot
   int xmode;        // 0 x in registers (each thread its 8 columns), 1 fp32 rows in shared memory
   int off_bar, off_x, off_tab, off_h, off_part, off_ring, off_dring, smem;
 
-  // Tensor maps of the tensor-core path (bf16 weights, H = 2048): boxes of
-  // one stage's gate + up rows (gu) and downT rows (d) of the routed experts
-  // (e) and of the shared expert (s), 128-byte swizzled in shared memory.
+  // Tensor maps of the tensor-core path (H = 2048): boxes of one stage's
+  // gate + up rows (gu) and downT rows (d) of the routed experts (e) and of
+  // the shared expert (s), 128-byte swizzled in shared memory.  Int8
+  // weights: the boxes hold the codes, and the sc maps the rows' 16-byte
+  // scale records.
   CUtensorMap tm_gu_e;
   CUtensorMap tm_d_e;
   CUtensorMap tm_gu_s;
   CUtensorMap tm_d_s;
+  CUtensorMap tm_gusc_e;
+  CUtensorMap tm_dsc_e;
+  CUtensorMap tm_gusc_s;
+  CUtensorMap tm_dsc_s;
 };
 
 // ---- batched path (T > kDecodeMaxT): routing, a gather of x by expert, two

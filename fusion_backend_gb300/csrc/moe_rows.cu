@@ -13,17 +13,16 @@ static_assert(kWkBf16 == MOE_FFN_W_BF16 && kWkQ4 == MOE_FFN_W_Q4B32 && kWkI8 == 
 
 cudaError_t launch_rows_bf16_fast(const LayerParams& p, cudaStream_t stream);
 cudaError_t launch_rows_q4_fast(const LayerParams& p, cudaStream_t stream);
+cudaError_t launch_rows_i8_fast(const LayerParams& p, cudaStream_t stream);
 cudaError_t launch_rows_generic(const LayerParams& p, cudaStream_t stream);
 
 namespace {
 
-// The fast (tensor-core) instances: bf16 or 4-bit weights, H = 2048,
-// E <= 256, and an activation that bf16 holds exactly -- bf16 x, or the
-// block form whose normalised input is bf16 -- so that it enters the bf16
-// products unchanged.  Int8 weights run the general instances.
-bool rows_fast(const LayerParams& p) {
-  return p.wfmt != kWkI8 && p.H == 2048 && p.E <= 256 && (p.act == 1 || p.block_mode);
-}
+// The fast (tensor-core) instances: H = 2048, E <= 256, and an activation
+// that bf16 holds exactly -- bf16 x, or the block form whose normalised
+// input is bf16 -- so that it enters the bf16 products unchanged (int8
+// weights quantise it, which needs no more).
+bool rows_fast(const LayerParams& p) { return p.H == 2048 && p.E <= 256 && (p.act == 1 || p.block_mode); }
 
 // Rows per stage at most, by weight format.
 int rows_rsm(int wfmt) { return wfmt == kWkBf16 ? kRsMaxB16 : kRsMaxQ4; }
@@ -51,9 +50,13 @@ static bool rows_layout_rs(LayerParams& p, int rs, int xbytes, int tab, int tmax
   const int avail = kSmemBudget - 1024 - p.off_ring;  // 1024: slack to align the ring in the shared window
   if (rows_fast(p)) {
     // tensor-core path: a ring of gate + up boxes (2 rs rows) and a ring of
-    // downT boxes (rs rows) with one slot more
-    p.stage_bytes = 2 * rs * p.rp;
-    const int dbytes = rs * p.rp;
+    // downT boxes (rs rows) with one slot more.  Int8: the boxes hold the H
+    // codes of each row, then (1 KB further, keeping slots 1 KB aligned) the
+    // rows' 16-byte scale records.
+    const bool i8 = p.wfmt == kWkI8;
+    p.stage_bytes = i8 ? 2 * rs * p.H + 1024 : 2 * rs * p.rp;
+    const int dbytes = i8 ? rs * p.H + 1024 : rs * p.rp;
+    p.dstage_bytes = dbytes;
     p.ns = std::min(kMaxStagesRing - 1, (avail - dbytes) / (p.stage_bytes + dbytes));
     p.nsd = p.ns + 1;
     if (p.ns < 2 || red_bytes > p.ns * p.stage_bytes) return false;
@@ -122,19 +125,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 5-D byte view of an expert block sequence [E][3 matrices][I rows][rb bytes]
-// (a bf16 row, or a 4-bit row of nibbles + scales): (128 bytes, row, matrix,
-// 128-byte chunk, expert), and a box of `rows` rows x `mats` matrices x all
-// rb/128 chunks of one expert, stored in shared memory as
-// [chunk][matrix][row][128 bytes] with the 128-byte swizzle.
-bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int rb, int I, int E,
-                 int rows, int mats) {
-  if (rb % 128) return false;
-  const cuuint64_t dims[5] = {128, (cuuint64_t)I, 3, (cuuint64_t)(rb / 128), (cuuint64_t)E};
+// (a bf16 row, a 4-bit row of nibbles + scales, or the codes of an int8 row):
+// (128 bytes, row, matrix, 128-byte chunk, expert), and a box of `rows` rows
+// x `mats` matrices x `chunks` chunks of one expert, stored in shared memory
+// as [chunk][matrix][row][128 bytes] with the 128-byte swizzle.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int rb, int chunks, int I,
+                 int E, int rows, int mats) {
+  if (rb % 16 || chunks * 128 > rb) return false;
+  const cuuint64_t dims[5] = {128, (cuuint64_t)I, 3, (cuuint64_t)chunks, (cuuint64_t)E};
   const cuuint64_t strides[4] = {(cuuint64_t)rb, (cuuint64_t)I * rb, 128, (cuuint64_t)3 * I * rb};
-  const cuuint32_t box[5] = {128, (cuuint32_t)rows, (cuuint32_t)mats, (cuuint32_t)(rb / 128), 1};
+  const cuuint32_t box[5] = {128, (cuuint32_t)rows, (cuuint32_t)mats, (cuuint32_t)chunks, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The 16-byte scale records of int8 rows (at byte H of each row): (16 bytes,
+// row, matrix, expert, 1), a box of `rows` rows x `mats` matrices stored as
+// [matrix][row][16 bytes], unswizzled.
+bool encode_scales(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const uint8_t* base, int H, int rb, int I,
+                   int E, int rows, int mats) {
+  const cuuint64_t dims[5] = {16, (cuuint64_t)I, 3, (cuuint64_t)E, 1};
+  const cuuint64_t strides[4] = {(cuuint64_t)rb, (cuuint64_t)I * rb, (cuuint64_t)3 * I * rb,
+                                 (cuuint64_t)3 * I * rb * E};
+  const cuuint32_t box[5] = {16, (cuuint32_t)rows, (cuuint32_t)mats, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t*>(base + H), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -146,10 +164,17 @@ cudaError_t rows_tensor_maps(LayerParams& p) {
   if (!fn) return cudaErrorNotSupported;
   const int rs = rows_rsm(p.wfmt);
   const int rb = (int)p.rb;
-  if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, rb, p.I, p.E, rs, 2) ||
-      !encode_rows(fn, &p.tm_d_e, p.expert_w, rb, p.I, p.E, rs, 1) ||
-      !encode_rows(fn, &p.tm_gu_s, p.shexp_w, rb, p.Is, 1, rs, 2) ||
-      !encode_rows(fn, &p.tm_d_s, p.shexp_w, rb, p.Is, 1, rs, 1))
+  const int chunks = p.wfmt == kWkI8 ? p.H / 128 : rb / 128;
+  if (!encode_rows(fn, &p.tm_gu_e, p.expert_w, rb, chunks, p.I, p.E, rs, 2) ||
+      !encode_rows(fn, &p.tm_d_e, p.expert_w, rb, chunks, p.I, p.E, rs, 1) ||
+      !encode_rows(fn, &p.tm_gu_s, p.shexp_w, rb, chunks, p.Is, 1, rs, 2) ||
+      !encode_rows(fn, &p.tm_d_s, p.shexp_w, rb, chunks, p.Is, 1, rs, 1))
+    return cudaErrorInvalidValue;
+  if (p.wfmt == kWkI8 &&
+      (!encode_scales(fn, &p.tm_gusc_e, p.expert_w, p.H, rb, p.I, p.E, rs, 2) ||
+       !encode_scales(fn, &p.tm_dsc_e, p.expert_w, p.H, rb, p.I, p.E, rs, 1) ||
+       !encode_scales(fn, &p.tm_gusc_s, p.shexp_w, p.H, rb, p.Is, 1, rs, 2) ||
+       !encode_scales(fn, &p.tm_dsc_s, p.shexp_w, p.H, rb, p.Is, 1, rs, 1)))
     return cudaErrorInvalidValue;
   return cudaSuccess;
 }
@@ -171,7 +196,11 @@ cudaError_t launch_join_add(const float* a, const float* b, float* out, int n, c
 
 cudaError_t launch_rows(const LayerParams& p, cudaStream_t stream) {
   if (!rows_fast(p)) return launch_rows_generic(p, stream);
-  return p.wfmt == 1 ? launch_rows_q4_fast(p, stream) : launch_rows_bf16_fast(p, stream);
+  switch (p.wfmt) {
+    case kWkQ4: return launch_rows_q4_fast(p, stream);
+    case kWkI8: return launch_rows_i8_fast(p, stream);
+    default: return launch_rows_bf16_fast(p, stream);
+  }
 }
 
 }  // namespace moe

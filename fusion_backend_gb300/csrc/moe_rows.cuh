@@ -81,14 +81,15 @@ struct RowTab {
   int32_t* misc;     // [4] the number of active experts U
   int32_t* qtab;     // [T*K - K + 1][4] per possible U: routed stages, first active expert, first group
   uint32_t* xmax;    // [T] int8 activation: bits of max |x| of token t
+  float* xsc;        // [T] int8 activation: x_scale = max|x| / 127 of token t
 };
 
 __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTab* v) {
   const int TK = T * K;
-  const int sz[12] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
-                      (TK - K + 1) * 16, T * 4};
-  int off = 0, o[12];
-  for (int i = 0; i < 12; ++i) {
+  const int sz[13] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
+                      (TK - K + 1) * 16, T * 4, T * 4};
+  int off = 0, o[13];
+  for (int i = 0; i < 13; ++i) {
     o[i] = off;
     off += (sz[i] + 15) & ~15;
   }
@@ -105,6 +106,7 @@ __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTa
     v->misc = reinterpret_cast<int32_t*>(base + o[9]);
     v->qtab = reinterpret_cast<int32_t*>(base + o[10]);
     v->xmax = reinterpret_cast<uint32_t*>(base + o[11]);
+    v->xsc = reinterpret_cast<float*>(base + o[12]);
   }
   return off;
 }
@@ -259,6 +261,31 @@ MOE_DEV void ldmatrix_x4_trans(uint32_t* r, const void* row) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(row)));
 }
+// Four 8x8 b16 matrices from the shared-memory row address this lane
+// supplies (lanes 8q .. 8q+7 give the 8 rows of matrix q): lane l gets
+// 32-bit element (l / 4, l % 4) of each matrix.
+MOE_DEV void ldmatrix_x4(uint32_t* r, const void* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row)));
+}
+// D += A B, m16n8k16, fp16 operands, fp32 accumulators (fragments as for
+// mma_bf16).
+MOE_DEV void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Signed bytes 2j and 2j + 1 of a 32-bit word -> the fp16 pair of their
+// values, exactly: the byte with its sign bit flipped, u = c + 128, as the
+// low byte of fp16 0x6400 (1024) reads 1024 + u, and 1024 + u - 1152 = c.
+MOE_DEV uint32_t i8_pair_f16(uint32_t w, int j) {
+  const uint32_t v = __byte_perm(w ^ 0x80808080u, 0x64646464u, j ? 0x5342u : 0x5140u);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64806480u));
+  return r;
+}
 // Byte offset of bf16 element k (even) of a row in a box stored as
 // [H/64 chunks][rows][64 elements] with the 128-byte swizzle of the tensor
 // copies: line L = chunk * rows + row, 16-byte unit (k / 8) % 8 at unit
@@ -321,11 +348,12 @@ MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int n
 template <int TMAX, int WK, bool FAST, int NCH>
 __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
   constexpr bool Q4 = WK == kWkQ4;
-  constexpr bool I8 = WK == kWkI8;  // int8 weights and activation: CUDA-core loop
-  static_assert(!(I8 && FAST), "int8 weights run the general loop");
-  constexpr bool MMA_C = FAST && !Q4 && TMAX >= 4;  // bf16: tensor-core down projection
-  constexpr bool Q4C = FAST && Q4;                  // 4-bit tensor-core loop
-  constexpr bool Q4MC = Q4C && TMAX >= 4;           // 4-bit: tensor-core down projection
+  constexpr bool I8 = WK == kWkI8;              // int8 weights and activation
+  constexpr bool B16C = FAST && WK == kWkBf16;  // bf16 tensor-core loop
+  constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
+  constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
+  constexpr bool Q4MC = Q4C && TMAX >= 4;       // 4-bit: tensor-core down projection
+  constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
   extern __shared__ __align__(128) uint8_t sm[];
@@ -387,14 +415,23 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   };
   auto advance = [&](StageCursor& c, int ns) { cursor_next(c, n_sh, ur0, gr0, gI, ns); };
-  // Tensor-core path: the downT box of a stage into its own ring.
+  // Tensor-core path: the downT box of a stage into its own ring (int8: the
+  // codes, then the rows' scale records).
   auto issue_d = [&](const StageCursor& c) {
     int i0, n;
     rows_of(c, i0, n);
     const int e = c.u < 0 ? 0 : tb.active[c.u];
     const void* dm = c.u < 0 ? (const void*)&Pk.tm_d_s : (const void*)&Pk.tm_d_e;
-    mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(RS * rb));
-    tma_load_5d(dring + (size_t)c.slot * RS * rb, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
+    uint8_t* dst = dring + (size_t)c.slot * P.dstage_bytes;
+    if constexpr (I8) {
+      const void* dsc = c.u < 0 ? (const void*)&Pk.tm_dsc_s : (const void*)&Pk.tm_dsc_e;
+      mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(RS * H + RS * 16));
+      tma_load_5d(dst, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
+      tma_load_5d(dst + (size_t)RS * H, dsc, 0, i0, 2, e, 0, &fulld[c.slot], pol);
+    } else {
+      mbar_arrive_expect_tx(&fulld[c.slot], (uint32_t)(RS * rb));
+      tma_load_5d(dst, dm, 0, i0, 2, 0, e, &fulld[c.slot], pol);
+    }
   };
   // One thread issues a stage.  Tensor-core path: one tiled tensor copy of
   // the stage's gate + up rows (a whole box; rows past the matrix are
@@ -408,8 +445,15 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     if constexpr (FAST) {
       const int e = c.u < 0 ? 0 : tb.active[c.u];
       const void* gu = c.u < 0 ? (const void*)&Pk.tm_gu_s : (const void*)&Pk.tm_gu_e;
-      mbar_arrive_expect_tx(bar, (uint32_t)r_stage_bytes);
-      tma_load_5d(dst, gu, 0, i0, 0, 0, e, bar, pol);
+      if constexpr (I8) {
+        const void* gsc = c.u < 0 ? (const void*)&Pk.tm_gusc_s : (const void*)&Pk.tm_gusc_e;
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * RS * H + 2 * RS * 16));
+        tma_load_5d(dst, gu, 0, i0, 0, 0, e, bar, pol);
+        tma_load_5d(dst + (size_t)2 * RS * H, gsc, 0, i0, 0, e, 0, bar, pol);
+      } else {
+        mbar_arrive_expect_tx(bar, (uint32_t)r_stage_bytes);
+        tma_load_5d(dst, gu, 0, i0, 0, 0, e, bar, pol);
+      }
     } else {
       const uint8_t* src;
       long long mat;
@@ -482,6 +526,12 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       if (lane == 1) prefetch_tensormap(&Pk.tm_d_e);
       if (lane == 2) prefetch_tensormap(&Pk.tm_gu_s);
       if (lane == 3) prefetch_tensormap(&Pk.tm_d_s);
+      if constexpr (I8) {
+        if (lane == 4) prefetch_tensormap(&Pk.tm_gusc_e);
+        if (lane == 5) prefetch_tensormap(&Pk.tm_dsc_e);
+        if (lane == 6) prefetch_tensormap(&Pk.tm_gusc_s);
+        if (lane == 7) prefetch_tensormap(&Pk.tm_dsc_s);
+      }
     }
   }
   // the shared stages (every thread advances the issue cursors in step; the
@@ -617,7 +667,56 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // block kp, lane quad q) -- unit tid = (8w + kp) * 4 + q, the fragments of
   // steps 2kp and 2kp + 1.  Other shapes: fp32 rows.  All reads of the source
   // precede the barrier, all writes follow it.
-  if constexpr (FAST) {
+  if constexpr (I8C) {
+    // int8 loop: each token quantised as in the general loop (x_scale =
+    // max|x| / 127 in fp32, codes round-half-away(x / x_scale) clamped to
+    // +-127), the codes as exact fp16 A fragments.  Unit U = (4w + b) * 4 + q
+    // of token t's row (32 bytes at 32 U) holds, for the 16-column steps i of
+    // the 64-column block b of warp slice w, the pairs (x[c], x[c + 1]) and
+    // (x[c + 2], x[c + 3]), c = 256w + 64b + 16i + 4q, i = 0..3; thread tid
+    // stages half hh = tid & 1 (i = 2hh, 2hh + 1) of unit tid / 2.  Odd
+    // tokens store the two halves swapped, so a quarter warp's 16-byte reads
+    // of tokens 2k and 2k + 1 fall in different banks.
+    const int U = tid >> 1, hh = tid & 1;
+    const int c_base = 256 * (U >> 4) + 64 * ((U >> 2) & 3) + 4 * (U & 3) + 32 * hh;
+    float v[TMAX][8];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[t][e] = 0.f;
+      if (t < T) {
+        const uint8_t* row = xs + (size_t)t * H * (src4 ? 4 : 2);
+        const float hi = P.block_mode ? tb.inv[2 * t] : 0.f, lo = P.block_mode ? tb.inv[2 * t + 1] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x2_from_smem(row, src4, P.block_mode, hi, lo, c_base + 16 * (j >> 1) + 2 * (j & 1), v[t] + 2 * j);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[t][e]));
+      }
+      // max |x| of token t over the warp, then over the block (non-negative
+      // floats order as their bit patterns)
+      const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      if (lane == 0 && t < T) atomicMax(&tb.xmax[t], mw);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        const float sc = __fdiv_rn(__uint_as_float(tb.xmax[t]), 127.0f);
+        uint32_t f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          int c[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            c[e] = sc != 0.f ? max(-127, min(127, (int)roundf(__fdiv_rn(v[t][2 * j + e], sc)))) : 0;
+          f[j] = (uint32_t)__half_as_ushort(__int2half_rn(c[0])) | ((uint32_t)__half_as_ushort(__int2half_rn(c[1])) << 16);
+        }
+        *reinterpret_cast<uint4*>(xs + (size_t)t * kXPitch + 32 * U + 16 * (hh ^ (t & 1))) = make_uint4(f[0], f[1], f[2], f[3]);
+      }
+    }
+    if (tid < T) tb.xsc[tid] = __fdiv_rn(__uint_as_float(tb.xmax[tid]), 127.0f);
+  } else if constexpr (FAST) {
     uint32_t fr[TMAX][4];
     const int w = tid >> 5, kp = (tid >> 2) & 7, q = tid & 3;
 #pragma unroll
@@ -677,8 +776,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     __syncthreads();
     if constexpr (I8) {
       // token t's codes at xs + t H (bytes), its scale x_scale = max|x| / 127
-      // at float index t after the T rows: q = round-half-away(x / x_scale)
-      // clamped to +-127, all in fp32 (x_scale = 0: q = 0)
+      // in the routing tables: q = round-half-away(x / x_scale) clamped to
+      // +-127, all in fp32 (x_scale = 0: q = 0)
 #pragma unroll
       for (int k = 0; k < kMaxGroups; ++k) {
         const int gi = tid + kRowThreads * k;
@@ -695,7 +794,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           *reinterpret_cast<uint2*>(xs + (size_t)t * H + 8 * q) = make_uint2(w[0], w[1]);
         }
       }
-      if (tid < T) reinterpret_cast<float*>(xs + (size_t)T * H)[tid] = __fdiv_rn(__uint_as_float(tb.xmax[tid]), 127.0f);
+      if (tid < T) tb.xsc[tid] = __fdiv_rn(__uint_as_float(tb.xmax[tid]), 127.0f);
     } else {
 #pragma unroll
       for (int k = 0; k < kMaxGroups; ++k) {
@@ -860,7 +959,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 #pragma unroll
   for (int j = 0; j < (Q4MC ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
 
-  if constexpr (FAST && !Q4) {
+  if constexpr (B16C) {
     // ---- tensor-core stage loop (bf16 weights, H = 2048, 4 rows a stage).
     // Warp w owns the 256-column slice [256w, 256w + 256) of H.
     //   A: D[token][stage row] = x . W over the slice, m16n8k16 with the
@@ -1177,6 +1276,146 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         }
       }
     }
+  } else if constexpr (I8C) {
+    // ---- tensor-core stage loop (int8 weights and activation, H = 2048, 8
+    // rows a stage).  A stored row is H codes, then a 16-byte record whose
+    // first word is the row's fp32 scale; the boxes hold the codes (128-byte
+    // chunks, swizzled) and, after them, the stage rows' records.  Warp w
+    // owns the 256-column slice [256w, 256w + 256) of H: code chunks 2w and
+    // 2w + 1 of every row.
+    //   A: D[token][row] = qx . q over the slice, m16n8k16 on fp16 operands
+    //      (codes are exact in fp16; each product is exact in fp32, and every
+    //      partial sum is an integer below 256 * 127^2 < 2^22, so the fp32
+    //      accumulators hold the int32 dot product exactly); per 64-column
+    //      block, one ldmatrix brings 4 codes of each stage row per lane for
+    //      each of the block's four 16-column steps, and the x fragments use
+    //      the same column order.  The gate rows and the up rows are two
+    //      8-row tiles.
+    //   A2: g = float(sum of the 8 warps' integer partials) * x_scale * s in
+    //      fp32 (the up rows alike), h = w silu(g) u.
+    //   C: CUDA cores, thread j owns columns 8j .. 8j + 7 and skips the
+    //      tokens the stage's group does not serve: y += (h s_down) q.
+    const int gq = lane >> 2, qq = lane & 3;
+    const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(512 * warp + 32 * qq);
+    const int xh0 = 16 * (gq & 1), xh1 = 16 * ((gq & 1) ^ 1);  // the two halves of a unit (odd tokens swapped)
+    const bool xon = gq < T;
+    const int rr = lane & 7, mi = lane >> 3;  // ldmatrix: the row and the matrix (16-byte unit) this lane addresses
+    StageCursor cs;
+    cursor_init(cs, NS);
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    uint32_t dph = 1u;
+    for (int s = 0; s < n_stages; ++s) {
+      advance(cs, NS);
+      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+      const int su = cs.u;
+      int si0, n;
+      rows_of(cs, si0, n);
+      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
+      // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
+      float acc[2][4][4];  // [gate|up][step i of a block][D fragment]
+#pragma unroll
+      for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[gu][i][0] = acc[gu][i][1] = acc[gu][i][2] = acc[gu][i][3] = 0.f;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint4 xa = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh0) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xb = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh1) : make_uint4(0u, 0u, 0u, 0u);
+        const int chunk = 2 * warp + (b >> 1);
+#pragma unroll
+        for (int gu = 0; gu < 2; ++gu) {
+          uint32_t wr[4];
+          ldmatrix_x4(wr, sl + (size_t)((chunk * 2 + gu) * 8 + rr) * 128 + ((((b & 1) * 4 + mi) ^ rr) << 4));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4& xv = i < 2 ? xa : xb;
+            const uint32_t a0 = (i & 1) ? xv.z : xv.x, a2 = (i & 1) ? xv.w : xv.y;
+            mma_f16(acc[gu][i], a0, 0u, a2, 0u, i8_pair_f16(wr[i], 0), i8_pair_f16(wr[i], 1));
+          }
+        }
+      }
+      if (gq < TMAX) {
+        float* pw = part + (size_t)warp * NV;
+#pragma unroll
+        for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = (acc[gu][0][e] + acc[gu][1][e]) + (acc[gu][2][e] + acc[gu][3][e]);
+      }
+      // the row scales of value j = (row, token) of A2, read before the slot
+      // is released
+      const int j = tid;
+      float s_gate = 0.f, s_up = 0.f;
+      if (j < n * TMAX) {
+        const int r = j / TMAX;
+        s_gate = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)r * 16);
+        s_up = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)(RS + r) * 16);
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // every warp is done with this stage's gate + up box and with the
+      // previous stage's downT box: both slots take their next stages
+      if (s + NS < n_stages) {
+        advance(ci, NS);
+        if (tid == kRowThreads - 1) issue(ci);
+      }
+      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+        advance(cd, P.nsd);
+        if (tid == kRowThreads - 1) issue_d(cd);
+      }
+      // -- A2: value j = (row, token) = r * TMAX + t on thread j
+      if (j < n * TMAX) {
+        const int t = j % TMAX;
+        int gi = 0, ui = 0;
+#pragma unroll
+        for (int w = 0; w < kRowWarps; ++w) {
+          gi += __float2int_rn(part[w * NV + j]);
+          ui += __float2int_rn(part[w * NV + RSM * TMAX + j]);
+        }
+        const float xsc_t = t < T ? tb.xsc[t] : 0.f;
+        const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi), xsc_t), s_gate);
+        const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui), xsc_t), s_up);
+        float h = 0.f;
+        if (su < 0)
+          h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
+        else
+          h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
+        hb[j] = h;
+      }
+      named_bar_sync(kBarStage, kRowThreads);
+      // -- C.  Box lines: chunk * 8 + row; thread j's 8 codes are half j & 1
+      // of 16-byte unit (j & 15) / 2 of chunk j / 16.
+      if (++dslot == P.nsd) {
+        dslot = 0;
+        dph ^= 1u;
+      }
+      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
+      {
+        const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
+        const uint32_t m = su < 0 ? all_tokens : tb.mask[su];
+        const int dchunk = tid >> 4, dunit = (tid & 15) >> 1, dhalf = tid & 1;
+#pragma unroll
+        for (int r = 0; r < kRsMaxQ4; ++r) {
+          if (r < n) {
+            const int line = dchunk * RS + r;
+            const uint2 q = *reinterpret_cast<const uint2*>(dbox + (size_t)line * 128 + ((dunit ^ (line & 7)) << 4) + 8 * dhalf);
+            const float sd = *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)r * 16);
+            float w[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              w[e] = i8_f32(q.x, e);
+              w[e + 4] = i8_f32(q.y, e);
+            }
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (!(m >> t & 1u)) continue;
+              const float c = hb[r * TMAX + t] * sd;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(c, w[e], y[t][0][e]);
+            }
+          }
+        }
+      }
+    }
   } else {
 
     // downT chunks of this thread, by stage parity
@@ -1188,7 +1427,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     // int8: the stage's row scales (gate, up, downT) by stage parity, and
     // the activation scales
     float* wsc = hb + 2 * RSM * TMAX;  // [2][3][RSM]
-    const float* xsc = reinterpret_cast<const float*>(xs + (size_t)T * H);
+    const float* xsc = tb.xsc;
     int n_prev = 0;
     uint32_t m_prev = 0u;
     StageCursor cs;

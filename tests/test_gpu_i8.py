@@ -1,7 +1,9 @@
 """GPU parity of the int8 weight format: int8 rows with an fp32 row scale and
 an int8 activation (the int8 linear, sd.linear_i8.v1, of "ggml operator
 extensions", section "sd.cpp integration": float(int32_dot(W, X)) * X_scale
-* W_scale), with the SwiGLU epilogue, on the decode path.
+* W_scale), with the SwiGLU epilogue, on the decode path: the tensor-core
+loop (H = 2048, bf16 x or the block form) and the general loop (other
+shapes, fp32 x).
 
 The activation quantiser and the gate/up projections are the same fp32
 operations on both sides, so the GPU's g and u equal the oracle's bit for
@@ -68,6 +70,9 @@ def check_i8(layer, x, act, label, **kw):
         (Shapes(T=5, H=128, E=4, top_k=4, I=17, Is=9), ACT_F32),      # every expert selected, I < rows of a stage
         (Shapes(T=2, H=2320, E=16, top_k=4, I=64, Is=48), ACT_BF16),  # H > 2048: two column chunks per thread
         (Shapes(T=1, H=4096, E=8, top_k=2, I=40, Is=24), ACT_F32),    # H at its maximum
+        (Shapes(T=3, H=2048, E=32, top_k=4, I=96, Is=40), ACT_F32),   # H = 2048 with fp32 x: the general loop
+        (Shapes(T=1, H=2048, E=16, top_k=4, I=130, Is=70), ACT_BF16),  # tensor-core loop, ragged 8-row stages
+        (Shapes(T=5, H=2048, E=24, top_k=3, I=20, Is=12), ACT_BF16),   # tensor-core loop, T=5, I < 3 stages
     ],
 )
 def test_i8_small_and_ragged(shapes, act):
@@ -81,7 +86,7 @@ def decode_i8_layer():
     return datagen.make_layer(2026, DECODE, WFMT_I8)
 
 
-@pytest.mark.parametrize("T", [1, 2, 8])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_decode_i8_full_size(decode_i8_layer, T):
     x, _ = draw_tokens(2026, decode_i8_layer, T, ACT_BF16, first_token=10 * T)
     check_i8(decode_i8_layer, x, ACT_BF16, f"decode i8 T={T}")
