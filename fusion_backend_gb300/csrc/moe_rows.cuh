@@ -1295,81 +1295,91 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      fp32 (the up rows alike), h = w silu(g) u.
     //   C: CUDA cores, thread j owns columns 8j .. 8j + 7 and skips the
     //      tokens the stage's group does not serve: y += (h s_down) q.
+    // One block barrier per stage: after the barrier of stage s, A2 of stage
+    // s and C of stage s - 1 run together (partials and h by stage parity),
+    // so a downT slot is refilled one stage later than its gate + up slot.
     const int gq = lane >> 2, qq = lane & 3;
     const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(512 * warp + 32 * qq);
     const int xh0 = 16 * (gq & 1), xh1 = 16 * ((gq & 1) ^ 1);  // the two halves of a unit (odd tokens swapped)
     const bool xon = gq < T;
     const int rr = lane & 7, mi = lane >> 3;  // ldmatrix: the row and the matrix (16-byte unit) this lane addresses
+    const int dchunk = tid >> 4, dunit = (tid & 15) >> 1, dhalf = tid & 1;
     StageCursor cs;
     cursor_init(cs, NS);
-    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
     uint32_t dph = 1u;
-    for (int s = 0; s < n_stages; ++s) {
-      advance(cs, NS);
-      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
-      const int su = cs.u;
-      int si0, n;
-      rows_of(cs, si0, n);
-      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
-      // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
-      float acc[2][4][4];  // [gate|up][step i of a block][D fragment]
-#pragma unroll
-      for (int gu = 0; gu < 2; ++gu)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[gu][i][0] = acc[gu][i][1] = acc[gu][i][2] = acc[gu][i][3] = 0.f;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint4 xa = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh0) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 xb = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh1) : make_uint4(0u, 0u, 0u, 0u);
-        const int chunk = 2 * warp + (b >> 1);
-#pragma unroll
-        for (int gu = 0; gu < 2; ++gu) {
-          uint32_t wr[4];
-          ldmatrix_x4(wr, sl + (size_t)((chunk * 2 + gu) * 8 + rr) * 128 + ((((b & 1) * 4 + mi) ^ rr) << 4));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4& xv = i < 2 ? xa : xb;
-            const uint32_t a0 = (i & 1) ? xv.z : xv.x, a2 = (i & 1) ? xv.w : xv.y;
-            mma_f16(acc[gu][i], a0, 0u, a2, 0u, i8_pair_f16(wr[i], 0), i8_pair_f16(wr[i], 1));
-          }
-        }
-      }
-      if (gq < TMAX) {
-        float* pw = part + (size_t)warp * NV;
+    int n_prev = 0;
+    uint32_t m_prev = 0u;
+    for (int s = 0; s <= n_stages; ++s) {
+      const int par = s & 1;
+      int n = 0, su = -1;
+      const int j = tid;  // A2 value j = (row, token) = r * TMAX + t
+      float s_gate = 0.f, s_up = 0.f;
+      if (s < n_stages) {
+        advance(cs, NS);
+        if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+        su = cs.u;
+        int si0;
+        rows_of(cs, si0, n);
+        const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
+        // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
+        float acc[2][4][4];  // [gate|up][step i of a block][D fragment]
 #pragma unroll
         for (int gu = 0; gu < 2; ++gu)
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = (acc[gu][0][e] + acc[gu][1][e]) + (acc[gu][2][e] + acc[gu][3][e]);
-      }
-      // the row scales of value j = (row, token) of A2, read before the slot
-      // is released
-      const int j = tid;
-      float s_gate = 0.f, s_up = 0.f;
-      if (j < n * TMAX) {
-        const int r = j / TMAX;
-        s_gate = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)r * 16);
-        s_up = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)(RS + r) * 16);
+          for (int i = 0; i < 4; ++i) acc[gu][i][0] = acc[gu][i][1] = acc[gu][i][2] = acc[gu][i][3] = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint4 xa = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh0) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 xb = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh1) : make_uint4(0u, 0u, 0u, 0u);
+          const int chunk = 2 * warp + (b >> 1);
+#pragma unroll
+          for (int gu = 0; gu < 2; ++gu) {
+            uint32_t wr[4];
+            ldmatrix_x4(wr, sl + (size_t)((chunk * 2 + gu) * 8 + rr) * 128 + ((((b & 1) * 4 + mi) ^ rr) << 4));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4& xv = i < 2 ? xa : xb;
+              const uint32_t a0 = (i & 1) ? xv.z : xv.x, a2 = (i & 1) ? xv.w : xv.y;
+              mma_f16(acc[gu][i], a0, 0u, a2, 0u, i8_pair_f16(wr[i], 0), i8_pair_f16(wr[i], 1));
+            }
+          }
+        }
+        if (gq < TMAX) {
+          float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
+#pragma unroll
+          for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = (acc[gu][0][e] + acc[gu][1][e]) + (acc[gu][2][e] + acc[gu][3][e]);
+        }
+        // the row scales of A2's value j, read before the slot is released
+        if (j < n * TMAX) {
+          const int r = j / TMAX;
+          s_gate = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)r * 16);
+          s_up = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)(RS + r) * 16);
+        }
       }
       named_bar_sync(kBarStage, kRowThreads);
-      // every warp is done with this stage's gate + up box and with the
-      // previous stage's downT box: both slots take their next stages
+      // every warp is done with this stage's gate + up box and (C of stage
+      // s - 2 ended before this barrier) with the downT box of stage s - 2
       if (s + NS < n_stages) {
         advance(ci, NS);
         if (tid == kRowThreads - 1) issue(ci);
       }
-      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+      if (s >= 2 && s - 2 + P.nsd < n_stages) {
         advance(cd, P.nsd);
         if (tid == kRowThreads - 1) issue_d(cd);
       }
-      // -- A2: value j = (row, token) = r * TMAX + t on thread j
-      if (j < n * TMAX) {
+      // -- A2 of stage s
+      if (s < n_stages && j < n * TMAX) {
         const int t = j % TMAX;
+        const float* pp = part + (size_t)par * kRowWarps * NV;
         int gi = 0, ui = 0;
 #pragma unroll
         for (int w = 0; w < kRowWarps; ++w) {
-          gi += __float2int_rn(part[w * NV + j]);
-          ui += __float2int_rn(part[w * NV + RSM * TMAX + j]);
+          gi += __float2int_rn(pp[w * NV + j]);
+          ui += __float2int_rn(pp[w * NV + RSM * TMAX + j]);
         }
         const float xsc_t = t < T ? tb.xsc[t] : 0.f;
         const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi), xsc_t), s_gate);
@@ -1379,23 +1389,21 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
         else
           h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
-        hb[j] = h;
+        hb[par * RSM * TMAX + j] = h;
       }
-      named_bar_sync(kBarStage, kRowThreads);
-      // -- C.  Box lines: chunk * 8 + row; thread j's 8 codes are half j & 1
-      // of 16-byte unit (j & 15) / 2 of chunk j / 16.
-      if (++dslot == P.nsd) {
-        dslot = 0;
-        dph ^= 1u;
-      }
-      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-      {
+      // -- C of stage s - 1.  Box lines: chunk * 8 + row; thread j's 8 codes
+      // are half j & 1 of 16-byte unit (j & 15) / 2 of chunk j / 16.
+      if (s >= 1) {
+        if (++dslot == P.nsd) {
+          dslot = 0;
+          dph ^= 1u;
+        }
+        if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
         const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
-        const uint32_t m = su < 0 ? all_tokens : tb.mask[su];
-        const int dchunk = tid >> 4, dunit = (tid & 15) >> 1, dhalf = tid & 1;
+        const float* hp = hb + (par ^ 1) * RSM * TMAX;
 #pragma unroll
         for (int r = 0; r < kRsMaxQ4; ++r) {
-          if (r < n) {
+          if (r < n_prev) {
             const int line = dchunk * RS + r;
             const uint2 q = *reinterpret_cast<const uint2*>(dbox + (size_t)line * 128 + ((dunit ^ (line & 7)) << 4) + 8 * dhalf);
             const float sd = *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)r * 16);
@@ -1407,14 +1415,16 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
             }
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
-              if (!(m >> t & 1u)) continue;
-              const float c = hb[r * TMAX + t] * sd;
+              if (!(m_prev >> t & 1u)) continue;
+              const float c = hp[r * TMAX + t] * sd;
 #pragma unroll
               for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(c, w[e], y[t][0][e]);
             }
           }
         }
       }
+      n_prev = n;
+      m_prev = s < n_stages ? (su < 0 ? all_tokens : tb.mask[su]) : 0u;
     }
   } else {
 
