@@ -352,7 +352,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool B16C = FAST && WK == kWkBf16;  // bf16 tensor-core loop
   constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
-  constexpr bool Q4MC = Q4C && TMAX >= 4;       // 4-bit: tensor-core down projection
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
@@ -955,9 +954,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   float yc[MMA_C ? 16 : 1][4];  // tensor-core down projection: y of this warp's slice, D fragments
 #pragma unroll
   for (int j = 0; j < (MMA_C ? 16 : 1); ++j) yc[j][0] = yc[j][1] = yc[j][2] = yc[j][3] = 0.f;
-  float yc4[Q4MC ? 16 : 1][4];  // 4-bit tensor-core down projection: y of this warp's slice, D fragments
+  float yc4[Q4C ? 16 : 1][4];  // 4-bit tensor-core down projection: y of this warp's slice, D fragments
 #pragma unroll
-  for (int j = 0; j < (Q4MC ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
+  for (int j = 0; j < (Q4C ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
 
   if constexpr (B16C) {
     // ---- tensor-core stage loop (bf16 weights, H = 2048, 4 rows a stage).
@@ -1151,7 +1150,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           lw[gu] = (2 * warp + gu) * kRsMaxQ4 + gq;
         }
         // blocks in two halves of four (the scale words of a half picked once)
-#pragma unroll(Q4MC ? 1 : 2)
+#pragma unroll 1
         for (int kh = 0; kh < 2; ++kh) {
           uint4 sh[2];  // (row 2q, row 2q + 1) scale words of blocks 4kh .. 4kh+3, per tile
 #pragma unroll
@@ -1223,31 +1222,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         dph ^= 1u;
       }
       if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-      if constexpr (!Q4MC) {
-        // CUDA cores (one or two tokens): thread j owns columns 8j .. 8j+7,
-        // one 32-bit word of nibbles (chunk j/32, unit (j%32)/4) and the
-        // scale of block j/4 (scale chunk, unit j/32, value (j%32)/4)
-        const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
-#pragma unroll
-        for (int r = 0; r < kRsMaxQ4; ++r) {
-          if (r < n) {
-            const int lw = warp * kRsMaxQ4 + r, ls = 8 * kRsMaxQ4 + r;
-            const uint32_t wq =
-                *reinterpret_cast<const uint32_t*>(dbox + lw * 128 + (((lane >> 2) ^ (lw & 7)) << 4) + 4 * (lane & 3));
-            const float d = __half2float(*reinterpret_cast<const __half*>(
-                dbox + ls * 128 + ((warp ^ (ls & 7)) << 4) + 2 * (lane >> 2)));
-            float w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = nib_f32(wq, e);
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              const float hv = hb[r * TMAX + t] * d;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(hv, w[e], y[t][0][e]);
-            }
-          }
-        }
-      } else {
+      {
         const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
         // B: h d_b for rows 2q, 2q + 1 (k) and token lane/4 (n)
         const float h0 = (2 * qq < n && gq < TMAX) ? hb[(2 * qq) * TMAX + gq] : 0.f;
@@ -1717,7 +1692,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         P.partial[((size_t)cta * T + t0 + 1) * H + c + 8] = yc[j][3];
       }
     }
-  } else if constexpr (Q4MC) {
+  } else if constexpr (Q4C) {
     // tile 2b + i: columns 256w + 32b + 4g + 2i (and + 1), tokens 2q (and + 1)
     const int g = lane >> 2, t0 = 2 * (lane & 3);
 #pragma unroll

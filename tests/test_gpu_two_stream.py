@@ -18,7 +18,7 @@ import pytest
 
 import datagen
 import oracle
-from datagen import ACT_BF16, ACT_F32, WFMT_BF16, WFMT_Q4B32
+from datagen import ACT_BF16, ACT_F32, WFMT_BF16, WFMT_I8, WFMT_Q4B32
 from tests.cases import DECODE, TINY, draw_tokens, with_T
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,8 @@ torch = pytest.importorskip("torch")
 @pytest.mark.parametrize(
     "base,T,act,wfmt",
     [(TINY, 2, ACT_F32, WFMT_BF16), (DECODE, 1, ACT_BF16, WFMT_BF16), (DECODE, 8, ACT_BF16, WFMT_BF16),
-     (DECODE, 1, ACT_BF16, WFMT_Q4B32), (DECODE, 4, ACT_BF16, WFMT_Q4B32)],
+     (DECODE, 1, ACT_BF16, WFMT_Q4B32), (DECODE, 4, ACT_BF16, WFMT_Q4B32), (DECODE, 2, ACT_BF16, WFMT_I8),
+     (TINY, 3, ACT_F32, WFMT_I8)],
 )
 def test_two_streams_match_sequential_oracle_and_fused(base, T, act, wfmt):
     import fusion_backend_gb300 as fb
