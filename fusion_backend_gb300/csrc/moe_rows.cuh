@@ -1126,20 +1126,26 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     // fragment rows in shared memory (nibble order), 16 bytes per block.
     const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(32 * warp + qq) * 16;
     const bool xon = gq < T;
+    // One block barrier per stage: after the barrier of stage s, A2 of stage
+    // s and C of stage s - 1 run together (partials and h by stage parity),
+    // so a downT slot is refilled one stage later than its gate + up slot.
     StageCursor cs;
     cursor_init(cs, NS);
-    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
     uint32_t dph = 1u;
-    for (int s = 0; s < n_stages; ++s) {
-      advance(cs, NS);
-      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
-      const int su = cs.u;
-      int si0, n;
-      rows_of(cs, si0, n);
-      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
-      // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
-      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [gate|up][row 2q + e], token lane/4
-      {
+    int n_prev = 0;
+    for (int s = 0; s <= n_stages; ++s) {
+      const int par = s & 1;
+      int n = 0, su = -1;
+      if (s < n_stages) {
+        advance(cs, NS);
+        if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+        su = cs.u;
+        int si0;
+        rows_of(cs, si0, n);
+        const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
+        // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
+        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [gate|up][row 2q + e], token lane/4
         uint4 sc[2][2];  // block scales of rows 2q, 2q + 1 of the gate and up tiles
         int lw[2];       // nibble chunk w, row lane/4 (the B column) of each tile
 #pragma unroll
@@ -1177,56 +1183,57 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
             }
           }
         }
-      }
-      if (gq < TMAX) {
-        float* pw = part + (size_t)warp * NV;
+        if (gq < TMAX) {
+          float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
 #pragma unroll
-        for (int gu = 0; gu < 2; ++gu)
+          for (int gu = 0; gu < 2; ++gu)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = acc[gu][e];
+            for (int e = 0; e < 2; ++e) pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = acc[gu][e];
+        }
       }
       named_bar_sync(kBarStage, kRowThreads);
-      // every warp is done with this stage's gate + up box and with the
-      // previous stage's downT box: both slots take their next stages
+      // every warp is done with this stage's gate + up box and (C of stage
+      // s - 2 ended before this barrier) with the downT box of stage s - 2
       if (s + NS < n_stages) {
         advance(ci, NS);
         if (tid == kRowThreads - 1) issue(ci);
       }
-      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+      if (s >= 2 && s - 2 + P.nsd < n_stages) {
         advance(cd, P.nsd);
         if (tid == kRowThreads - 1) issue_d(cd);
       }
-      // -- A2: value j = (row, token) = r * TMAX + t on thread j
+      // -- A2 of stage s: value j = (row, token) = r * TMAX + t on thread j
       {
         const int j = tid;
-        if (j < n * TMAX) {
+        if (s < n_stages && j < n * TMAX) {
           const int t = j % TMAX;
+          const float* pp = part + (size_t)par * kRowWarps * NV;
           float g = 0.f, u = 0.f;
 #pragma unroll
           for (int w = 0; w < kRowWarps; ++w) {
-            g += part[w * NV + j];
-            u += part[w * NV + RSM * TMAX + j];
+            g += pp[w * NV + j];
+            u += pp[w * NV + RSM * TMAX + j];
           }
           float h = 0.f;
           if (su < 0)
             h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
           else
             h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
-          hb[j] = h;
+          hb[par * RSM * TMAX + j] = h;
         }
       }
-      named_bar_sync(kBarStage, kRowThreads);
-      // -- C.  Box lines: chunk * 8 + row.
-      if (++dslot == P.nsd) {
-        dslot = 0;
-        dph ^= 1u;
-      }
-      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-      {
+      // -- C of stage s - 1.  Box lines: chunk * 8 + row.
+      if (s >= 1) {
+        if (++dslot == P.nsd) {
+          dslot = 0;
+          dph ^= 1u;
+        }
+        if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
         const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
+        const float* hp = hb + (par ^ 1) * RSM * TMAX;
         // B: h d_b for rows 2q, 2q + 1 (k) and token lane/4 (n)
-        const float h0 = (2 * qq < n && gq < TMAX) ? hb[(2 * qq) * TMAX + gq] : 0.f;
-        const float h1 = (2 * qq + 1 < n && gq < TMAX) ? hb[(2 * qq + 1) * TMAX + gq] : 0.f;
+        const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
+        const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
         const int l0 = 8 * kRsMaxQ4 + 2 * qq;
         const uint4 s0 = *reinterpret_cast<const uint4*>(dbox + l0 * 128 + ((warp ^ (l0 & 7)) << 4));
         const uint4 s1 = *reinterpret_cast<const uint4*>(dbox + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
@@ -1250,6 +1257,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           }
         }
       }
+      n_prev = n;
     }
   } else if constexpr (I8C) {
     // ---- tensor-core stage loop (int8 weights and activation, H = 2048, 8
