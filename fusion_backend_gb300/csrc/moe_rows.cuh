@@ -973,49 +973,55 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     // fragment rows in shared memory, 16 bytes per 32-column block.
     const uint8_t* xrow = xs + (size_t)(lane >> 2) * kXPitch + (size_t)(32 * warp + (lane & 3)) * 16;
     const bool xon = (lane >> 2) < T;
+    // One block barrier per stage: after the barrier of stage s, A2 of stage
+    // s and C of stage s - 1 run together (partials and h by stage parity),
+    // so a downT slot is refilled one stage later than its gate + up slot.
     StageCursor cs;
     cursor_init(cs, NS);
-    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage
+    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
     uint32_t dph = 1u;
-    for (int s = 0; s < n_stages; ++s) {
-      advance(cs, NS);
-      if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
-      const int su = cs.u;
-      int si0, n;
-      rows_of(cs, si0, n);
-      const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
-      // -- A (four accumulators, so the tensor-core steps do not chain).  B
-      // column n = lane / 4 is row n of the gate + up box (lines chunk * 8 + n).
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int nrow = lane >> 2;
-        float dq[4][4];
+    int n_prev = 0;
+    for (int s = 0; s <= n_stages; ++s) {
+      const int par = s & 1;
+      int n = 0, su = -1;
+      if (s < n_stages) {
+        advance(cs, NS);
+        if (!mbar_wait(&full[cs.slot], cs.ph)) timed_out = true;
+        su = cs.u;
+        int si0;
+        rows_of(cs, si0, n);
+        const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
+        // -- A (four accumulators, so the tensor-core steps do not chain).  B
+        // column n = lane / 4 is row n of the gate + up box (lines chunk * 8 + n).
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int nrow = lane >> 2;
+          float dq[4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.f;
+          for (int q = 0; q < 4; ++q) dq[q][0] = dq[q][1] = dq[q][2] = dq[q][3] = 0.f;
 #pragma unroll
-        for (int kp2 = 0; kp2 < 8; kp2 += 2) {
+          for (int kp2 = 0; kp2 < 8; kp2 += 2) {
 #pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int kp = kp2 + e2;
-            const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int kp = kp2 + e2;
+              const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int k0 = 256 * warp + 32 * kp + 16 * h + 2 * (lane & 3);
-              const int line = (k0 >> 6) * (2 * kRsMaxB16) + nrow;
-              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0));
-              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0 + 8));
-              mma_bf16(dq[2 * e2 + h], h ? xv.z : xv.x, 0u, h ? xv.w : xv.y, 0u, b0, b1);
+              for (int h = 0; h < 2; ++h) {
+                const int k0 = 256 * warp + 32 * kp + 16 * h + 2 * (lane & 3);
+                const int line = (k0 >> 6) * (2 * kRsMaxB16) + nrow;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0));
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sl + swz_off(line, k0 + 8));
+                mma_bf16(dq[2 * e2 + h], h ? xv.z : xv.x, 0u, h ? xv.w : xv.y, 0u, b0, b1);
+              }
             }
           }
-        }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) d[e] = (dq[0][e] + dq[1][e]) + (dq[2][e] + dq[3][e]);
-      }
-      {
+          for (int e = 0; e < 2; ++e) d[e] = (dq[0][e] + dq[1][e]) + (dq[2][e] + dq[3][e]);
+        }
         // this lane: token lane/4, stage rows 2(lane & 3) and +1 (0..3 gate, 4..7 up)
         const int t = lane >> 2;
         if (t < TMAX) {
-          float* pw = part + (size_t)warp * NV;
+          float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int nr = 2 * (lane & 3) + q, gu = nr >> 2, r = nr & 3;
@@ -1024,84 +1030,88 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         }
       }
       named_bar_sync(kBarStage, kRowThreads);
-      // every warp is done with this stage's gate + up box and with the
-      // previous stage's downT box: both slots take their next stages
+      // every warp is done with this stage's gate + up box and (C of stage
+      // s - 2 ended before this barrier) with the downT box of stage s - 2
       if (s + NS < n_stages) {
         advance(ci, NS);
         if (tid == kRowThreads - 1) issue(ci);
       }
-      if (s >= 1 && s - 1 + P.nsd < n_stages) {
+      if (s >= 2 && s - 2 + P.nsd < n_stages) {
         advance(cd, P.nsd);
         if (tid == kRowThreads - 1) issue_d(cd);
       }
-      // -- A2: value j = (row, token) = r * TMAX + t on thread j
+      // -- A2 of stage s: value j = (row, token) = r * TMAX + t on thread j
       {
         const int j = tid;
-        if (j < n * TMAX) {
+        if (s < n_stages && j < n * TMAX) {
           const int t = j % TMAX;
+          const float* pp = part + (size_t)par * kRowWarps * NV;
           float g = 0.f, u = 0.f;
 #pragma unroll
           for (int w = 0; w < kRowWarps; ++w) {
-            g += part[w * NV + j];
-            u += part[w * NV + RSM * TMAX + j];
+            g += pp[w * NV + j];
+            u += pp[w * NV + RSM * TMAX + j];
           }
           float h = 0.f;
           if (su < 0)
             h = t < T ? tb.s[t] * silu_mul(g, u) : 0.f;
           else
             h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
-          hb[j] = h;
+          hb[par * RSM * TMAX + j] = h;
         }
       }
-      named_bar_sync(kBarStage, kRowThreads);
-      // -- C
-      if (++dslot == P.nsd) {
-        dslot = 0;
-        dph ^= 1u;
-      }
-      if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-      const uint8_t* dbox = dring + (size_t)dslot * kRsMaxB16 * rb;
-      if constexpr (!MMA_C) {
-        // CUDA cores (one or two tokens): chunk tid of every downT row
-        const int k = 8 * tid;
+      // -- C of stage s - 1
+      if (s >= 1) {
+        if (++dslot == P.nsd) {
+          dslot = 0;
+          dph ^= 1u;
+        }
+        if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
+        const uint8_t* dbox = dring + (size_t)dslot * kRsMaxB16 * rb;
+        const float* hp = hb + (par ^ 1) * RSM * TMAX;
+        if constexpr (!MMA_C) {
+          // CUDA cores (one or two tokens): chunk tid of every downT row
+          const int k = 8 * tid;
 #pragma unroll
-        for (int r = 0; r < kRsMaxB16; ++r) {
-          if (r < n) {
-            const uint4 v = *reinterpret_cast<const uint4*>(dbox + swz_off((k >> 6) * kRsMaxB16 + r, k));
-            const float w[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+          for (int r = 0; r < kRsMaxB16; ++r) {
+            if (r < n_prev) {
+              const uint4 v = *reinterpret_cast<const uint4*>(dbox + swz_off((k >> 6) * kRsMaxB16 + r, k));
+              const float w[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              const float hv = hb[r * TMAX + t];
+              for (int t = 0; t < TMAX; ++t) {
+                const float hv = hp[r * TMAX + t];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(hv, w[e], y[t][0][e]);
+                for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(hv, w[e], y[t][0][e]);
+              }
             }
           }
-        }
-      } else {
-        const int t = lane >> 2, k0 = 2 * (lane & 3);
-        const float h0 = (k0 < n && t < TMAX) ? hb[k0 * TMAX + t] : 0.f;
-        const float h1 = (k0 + 1 < n && t < TMAX) ? hb[(k0 + 1) * TMAX + t] : 0.f;
-        const uint32_t bh = pack_bf16(h0, h1);
-        const uint32_t bl = pack_bf16(h0 - bf16_lo(bh), h1 - bf16_hi(bh));
-        // matrix q = lane / 8 of the 16x16 A tile: stored rows k = (q / 2) * 8
-        // + lane % 8 at columns (q % 2) * 8 ..; row k is downT row k % 4 of
-        // the stage (k >= 4 repeat them, times h = 0)
-        const int q = lane >> 3, r = lane & 3;
+        } else {
+          const int t = lane >> 2, k0 = 2 * (lane & 3);
+          const float h0 = (k0 < n_prev && t < TMAX) ? hp[k0 * TMAX + t] : 0.f;
+          const float h1 = (k0 + 1 < n_prev && t < TMAX) ? hp[(k0 + 1) * TMAX + t] : 0.f;
+          const uint32_t bh = pack_bf16(h0, h1);
+          const uint32_t bl = pack_bf16(h0 - bf16_lo(bh), h1 - bf16_hi(bh));
+          // matrix q = lane / 8 of the 16x16 A tile: stored rows k = (q / 2) * 8
+          // + lane % 8 at columns (q % 2) * 8 ..; row k is downT row k % 4 of
+          // the stage (k >= 4 repeat them, times h = 0)
+          const int q = lane >> 3, r = lane & 3;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t at[8][4];
+          for (int half = 0; half < 2; ++half) {
+            uint32_t at[8][4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int m0 = 256 * warp + 16 * (8 * half + j) + (q & 1) * 8;
-            ldmatrix_x4_trans(at[j], dbox + swz_off((m0 >> 6) * kRsMaxB16 + r, m0));
+            for (int j = 0; j < 8; ++j) {
+              const int m0 = 256 * warp + 16 * (8 * half + j) + (q & 1) * 8;
+              ldmatrix_x4_trans(at[j], dbox + swz_off((m0 >> 6) * kRsMaxB16 + r, m0));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bh, 0u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bl, 0u);
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bh, 0u);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) mma_bf16(yc[8 * half + j], at[j][0], at[j][1], at[j][2], at[j][3], bl, 0u);
         }
       }
+      n_prev = n;
     }
   } else if constexpr (Q4C) {
     // ---- tensor-core stage loop (4-bit weights, H = 2048, 8 rows a stage).
