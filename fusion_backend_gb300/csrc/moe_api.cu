@@ -315,7 +315,8 @@ int moe_ffn_prepare(const moe_ffn_shapes* shapes, moe_ffn_dtype dtype, moe_ffn_p
   L.logits = off;
   off = align256(off + T * ((E + 1 + 3) / 4 * 4) * 4);
   L.partial = off;
-  if (path == 0) off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * 4);
+  // per-block partial outputs: fp32, or (T = 1) 8-byte tagged words
+  if (path == 0) off = align256(off + (size_t)kMaxGrid * T * (size_t)s.H * (T == 1 ? 8 : 4));
   if (path == 1) {
     const size_t TK = T * K, H = s.H, hw = s.I > s.Is ? s.I : s.Is;
     L.lbound = off;
@@ -418,7 +419,7 @@ int moe_ffn_read_routing(moe_ffn_plan_t plan, const void* workspace, moe_ffn_str
 
 int moe_ffn_probe_timeout(moe_ffn_plan_t plan, moe_ffn_stream_t stream, void* workspace, size_t workspace_bytes,
                           int32_t which) {
-  if (!valid_plan(plan) || !workspace || (which != 0 && which != 1)) return MOE_FFN_ERR_INVALID_ARG;
+  if (!valid_plan(plan) || !workspace || which < 0 || which > 2) return MOE_FFN_ERR_INVALID_ARG;
   if (workspace_bytes < plan->ws.total) return MOE_FFN_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MOE_FFN_ERR_MISALIGNED;
   DeviceInfo* dev = nullptr;

@@ -132,6 +132,24 @@ MOE_DEV unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
 MOE_DEV void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// Two consecutive 8-byte words (16-byte aligned) with an L2 policy
+// (createpolicy); each word is written whole, the pair is not one access.
+MOE_DEV void st_relaxed_gpu_v2_u64(unsigned long long* p, unsigned long long a, unsigned long long b, uint64_t pol) {
+  asm volatile("st.relaxed.gpu.global.L2::cache_hint.v2.u64 [%0], {%1, %2}, %3;" ::"l"(p), "l"(a), "l"(b), "l"(pol)
+               : "memory");
+}
+
+// ------------------------------------------------------- tagged words
+// A value published to other blocks together with the call that wrote it:
+// the upper half of a 64-bit word is the call's tag, the lower half the
+// fp32 value.  A reader polls the word until the tag is its own call's, so
+// the value arrives with its own "ready" flag (one trip through L2 instead
+// of a barrier and then the data).
+MOE_DEV unsigned long long tagged(uint32_t tag, float v) {
+  return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+MOE_DEV uint32_t tag_of_word(unsigned long long w) { return (uint32_t)(w >> 32); }
+MOE_DEV float value_of_word(unsigned long long w) { return __uint_as_float((uint32_t)w); }
 // With relaxed loads that observed other threads' release stores before it,
 // this fence makes the loads an acquire: later accesses see what those
 // threads wrote before their releases.

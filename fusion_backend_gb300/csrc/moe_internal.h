@@ -47,6 +47,12 @@ enum : int { kCtrlStatus = 0, kCtrlProbe = 2, kCtrlWords = 64 };
 // overwrote, or never initialised) takes the flag barrier, which needs no
 // prior state.  Both decisions are the same in every block: they read
 // `epoch` and `sig` before any block can change them.
+//
+// With one token the second barrier is not used: each partial output is a word
+// tagged with the call (the low half of e above the fp32 value).  Each block
+// first marks its own partial words with another tag, before the first
+// barrier, which publishes the marks; a reader then polls the words it needs
+// until each carries the call's tag -- it can see only the mark or the value.
 struct RowSync {
   unsigned long long epoch;
   unsigned long long sig;
@@ -86,7 +92,7 @@ struct LayerParams {
   RowSync* sync;
   float* logits;   // [T][ls]: columns 0..E-1 router logits, column E the shared-gate logit
   int ls;          // logits row stride in floats: E + 1 rounded up to a multiple of 4
-  float* partial;  // [G][T][H] per-block partial outputs
+  float* partial;  // [G][T][H] per-block partial outputs: fp32, or (T = 1) 8-byte tagged words
   int32_t* r_counts;
   int32_t* r_offsets;
   int32_t* r_perm;

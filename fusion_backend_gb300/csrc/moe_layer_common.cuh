@@ -112,6 +112,39 @@ MOE_DEV bool grid_barrier(RowSync* sy, int which, bool fast, int G, unsigned lon
   return !__syncthreads_or(!ok);
 }
 
+// Bounded poll of one thread on n <= N tagged words p[i * stride] (see
+// `tagged`): v[i] = the value of word i once its tag is `tag`.  The pending
+// words are loaded together (relaxed loads), again and again until every
+// tag matches.  Gives up after about a second (the global timer, and an
+// iteration cap in case it does not advance) and returns false; a word never
+// seen with the tag reads 0.
+template <int N>
+MOE_DEV bool poll_tagged(const unsigned long long* p, size_t stride, int n, uint32_t tag, float* v) {
+  uint32_t pending = 0u;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    v[i] = 0.f;
+    if (i < n) pending |= 1u << i;
+  }
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0; pending; ++it) {
+    unsigned long long w[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = (pending >> i & 1u) ? ld_relaxed_gpu_u64(p + (size_t)i * stride) : 0ull;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((pending >> i & 1u) && tag_of_word(w[i]) == tag) {
+        v[i] = value_of_word(w[i]);
+        pending &= ~(1u << i);
+      }
+    if (!pending) break;
+    if (it == 32) t0 = global_ns();
+    if (it >= kSpinLimit || (it > 32 && (it & 15) == 0 && global_ns() - t0 > kWaitLimitNs)) return false;
+    if (it > 32) __nanosleep(32);
+  }
+  return true;
+}
+
 // -------------------------------------------------------------- reductions
 MOE_DEV float warp_sum(float v) {
 #pragma unroll

@@ -1,5 +1,5 @@
 // The failure-path probe of the fused MoE FFN layer, sm_103a: one small
-// kernel that runs the layer's two kinds of bounded wait against conditions
+// kernel that runs the layer's kinds of bounded wait against conditions
 // nothing ever satisfies, so that the give-up path (status word set to the
 // timeout status, kernel returns, context usable) can be tested without a
 // fault.
@@ -14,8 +14,10 @@ namespace moe {
 // the status word must end as the timeout status, and the kernel returns.
 // which = 0: an mbarrier phase that never completes (the wait of a shared-
 // memory copy that never lands); which = 1: the row kernel's grid-barrier
-// wait on a flag slot that never receives the expected epoch (the slot is
-// the control words 4..5, and the epoch expected is one more than it holds).
+// wait on a flag slot that never receives the expected epoch; which = 2: the
+// row kernel's poll of a tagged word (a partial output) that never carries
+// the expected tag.  The slot is the control words 4..5; the value expected
+// is one more than it holds.
 __global__ void k_probe_timeout(uint32_t* ctrl, int which) {
   __shared__ uint64_t bar;
   const int lane = threadIdx.x & 31;
@@ -32,7 +34,13 @@ __global__ void k_probe_timeout(uint32_t* ctrl, int which) {
     const unsigned long long never = ld_relaxed_gpu_u64(slot) + 1ull;
     if (lane == 0) ctrl[kCtrlStatus] = 0u;
     __syncwarp();
-    ok = grid_flags_wait(slot, 1, never);
+    if (which == 1) {
+      ok = grid_flags_wait(slot, 1, never);
+    } else {
+      float v;
+      ok = poll_tagged<1>(slot, 0, 1, tag_of_word(ld_relaxed_gpu_u64(slot)) + 1u, &v);
+      ok = __all_sync(0xffffffffu, ok);
+    }
   }
   if (!ok && lane == 0) atomicExch(reinterpret_cast<int*>(&ctrl[kCtrlStatus]), kStatusTimeout);
 }

@@ -31,10 +31,11 @@
 //        A2 h_t = w_t silu(g_t) u_t of each row from the warp partials;
 //        C  y[cols][tokens] += downT_r^T h over the stage's rows;
 //   5. end: each block stores its partial y[T][H] (fp32) and announces it
-//      (second grid-wide barrier); then each block sums the G partials of
-//      its own output columns in block order and writes out (adding x_res in
-//      the block form).  All orders are fixed, so results are bitwise
-//      repeatable.
+//      (second grid-wide barrier; with one token the partials are words
+//      tagged with the call instead, polled by their readers); then each block sums
+//      the G partials of its own output columns in block order and writes
+//      out (adding x_res in the block form).  All orders are fixed, so
+//      results are bitwise repeatable.
 // The grid-wide barriers use per-block flag slots tagged with the call's
 // epoch (RowSync), so no workspace word has to be reset between calls.
 //
@@ -353,6 +354,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
+  // One token: the partial outputs are words tagged with the call, polled by
+  // the column sums (no second grid-wide barrier; see RowSync)
+  constexpr bool TAGGED = TMAX == 1;
   static_assert(NCH == 1 || (NCH == 2 && !FAST), "8-column chunks per thread: 1, or 2 for H > 2048");
   constexpr int EPL = FAST ? 8 : 32;         // top-k keys per lane
   extern __shared__ __align__(128) uint8_t sm[];
@@ -571,6 +575,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   const unsigned long long prev_epoch = __ldcg(&sync->epoch);
   const unsigned long long epoch = prev_epoch + 1ull;
   const bool fast_sync = __ldcg(&sync->sig) == ~prev_epoch;
+  const uint32_t tag = (uint32_t)epoch;
+  // tagged partials: kept in L2 (evict-last; rewritten every call, read
+  // within microseconds), and this block's words first get a tag that is not
+  // the call's -- the grid-wide barrier publishes that before any reader
+  // polls them
+  const uint64_t pol_keep = policy_evict_last();
+  if constexpr (TAGGED) {
+    const unsigned long long stale = tagged(~tag, 0.f);
+    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
+    for (int i = 2 * tid; i < T * H; i += 2 * kRowThreads) st_relaxed_gpu_v2_u64(mine + i, stale, stale, pol_keep);
+  }
   if (cta == 0) {
     if (tid == 0) P.ctrl[kCtrlStatus] = 0u;  // a status left by the failure-path probe
     for (int c = P.G + tid; c < kMaxGrid; c += kRowThreads) sync->status[c] = 0;
@@ -1713,16 +1728,23 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   } else if constexpr (Q4C) {
     // tile 2b + i: columns 256w + 32b + 4g + 2i (and + 1), tokens 2q (and + 1)
     const int g = lane >> 2, t0 = 2 * (lane & 3);
+    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int c = 256 * warp + 32 * (j >> 1) + 4 * g + 2 * (j & 1);
-      if (t0 < T)
-        *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0) * H + c) = make_float2(yc4[j][0], yc4[j][2]);
-      if (t0 + 1 < T)
-        *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0 + 1) * H + c) =
-            make_float2(yc4[j][1], yc4[j][3]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (t0 + e >= T) continue;
+        if constexpr (TAGGED)
+          st_relaxed_gpu_v2_u64(mine + (size_t)(t0 + e) * H + c, tagged(tag, yc4[j][e]), tagged(tag, yc4[j][2 + e]),
+                                pol_keep);
+        else
+          *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0 + e) * H + c) =
+              make_float2(yc4[j][e], yc4[j][2 + e]);
+      }
     }
   } else {
+    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
       if (t >= T) break;
@@ -1730,65 +1752,76 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       for (int k = 0; k < NCH; ++k) {
         const int ch = tid + kRowThreads * k;
         if (!FAST && ch >= H / 8) break;
-        float4* dst = reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t) * H + 8 * ch);
-        dst[0] = make_float4(y[t][k][0], y[t][k][1], y[t][k][2], y[t][k][3]);
-        dst[1] = make_float4(y[t][k][4], y[t][k][5], y[t][k][6], y[t][k][7]);
+        if constexpr (TAGGED) {
+          unsigned long long* dst = mine + (size_t)t * H + 8 * ch;
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            st_relaxed_gpu_v2_u64(dst + e, tagged(tag, y[t][k][e]), tagged(tag, y[t][k][e + 1]), pol_keep);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t) * H + 8 * ch);
+          dst[0] = make_float4(y[t][k][0], y[t][k][1], y[t][k][2], y[t][k][3]);
+          dst[1] = make_float4(y[t][k][4], y[t][k][5], y[t][k][6], y[t][k][7]);
+        }
       }
     }
   }
-  // every block's partial, then the sum of this block's columns: the block
-  // barrier orders all threads' stores before thread 0's release (a
-  // cumulative release at GPU scope), and warp 0's acquire orders every
-  // other block's stores before this block's reads
+  // every block's partial, then the sum of this block's columns.  fp32
+  // partials: the second grid-wide barrier orders all blocks' stores before
+  // the reads (the block barrier orders all threads' stores before thread
+  // 0's cumulative release, warp 0's acquire orders every other block's
+  // stores before this block's reads).  Tagged partials (one token): each read
+  // polls its word until it carries the call's tag; the first barrier
+  // already ordered every block's reads of x before any block writes out.
   // This block's output columns [da, db) for all tokens (O values).  In the
-  // block form the residual x_res of those columns is read now, before the
-  // barrier: no other block writes them, and every block read all of x at
-  // its start.
+  // block form the residual x_res of those columns is read now: no other
+  // block writes them, and every block read all of x at its start.
   const int da = (int)muldiv(H, cta, P.G), db = (int)muldiv(H, cta + 1, P.G);
   const int nD = db - da, O = T * nD;
   float resid = 0.f;
   if (P.block_mode && tid < O) resid = __ldcg(P.out + (size_t)(tid / nD) * H + da + tid % nD);
-  const bool tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
-  if (tail_timed_out || block_timed_out) {
-    if (tid == 0) sync->status[cta] = kStatusTimeout;
-  } else if (tid == 0) {
-    sync->status[cta] = 0;
-  }
+  bool tail_timed_out = false;
+  if constexpr (!TAGGED) tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
   // The O sums of G partials.  Thread (sp, o) adds partials sp, sp + S, ...
   // in order, up to 16 loads in flight together; the S part sums are then
   // added in order.
-  if (O > 0) {
-    const int S = O >= kRowThreads ? 1 : kRowThreads / O;
-    // The ring is idle now (every issued stage was waited on); reuse it.
-    float* red = reinterpret_cast<float*>(ring);  // [S][O]
-    for (int idx = tid; idx < S * O; idx += kRowThreads) {
-      const int o = idx % O, sp = idx / O;
-      const int t = o / nD, col = da + o % nD;
-      const float* src = P.partial + (size_t)t * H + col;
-      const size_t stride = (size_t)T * H;
-      float acc = 0.f;
-      for (int c0 = sp; c0 < P.G; c0 += 16 * S) {
-        float v[16];
+  bool sums_timed_out = false;
+  const int S = O >= kRowThreads ? 1 : kRowThreads / max(O, 1);
+  // The ring is idle now (every issued stage was waited on); reuse it.
+  float* red = reinterpret_cast<float*>(ring);  // [S][O]
+  for (int idx = tid; idx < S * O; idx += kRowThreads) {
+    const int o = idx % O, sp = idx / O;
+    const int t = o / nD, col = da + o % nD;
+    const size_t stride = (size_t)T * H;
+    float acc = 0.f;
+    for (int c0 = sp; c0 < P.G; c0 += 16 * S) {
+      float v[16];
+      if constexpr (TAGGED) {
+        const unsigned long long* src = reinterpret_cast<const unsigned long long*>(P.partial) + (size_t)t * H + col;
+        const int n = min(16, (P.G - 1 - c0) / S + 1);
+        if (!poll_tagged<16>(src + (size_t)c0 * stride, (size_t)S * stride, n, tag, v)) sums_timed_out = true;
+      } else {
+        const float* src = P.partial + (size_t)t * H + col;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const int c = c0 + q * S;
           v[q] = c < P.G ? __ldcg(src + (size_t)c * stride) : 0.f;
         }
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (c0 + q * S < P.G) acc += v[q];
       }
-      red[sp * O + o] = acc;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (c0 + q * S < P.G) acc += v[q];
     }
-    __syncthreads();
-    for (int oo = tid; oo < O; oo += kRowThreads) {
-      float acc = red[oo];
-      for (int q = 1; q < S; ++q) acc += red[q * O + oo];
-      const int t = oo / nD, col = da + oo % nD;
-      float* dst = P.out + (size_t)t * H + col;
-      *dst = P.block_mode ? __fadd_rn(oo < kRowThreads ? resid : *dst, acc) : acc;
-    }
+    red[sp * O + o] = acc;
   }
+  if (__syncthreads_or(sums_timed_out)) tail_timed_out = true;
+  for (int oo = tid; oo < O; oo += kRowThreads) {
+    float acc = red[oo];
+    for (int q = 1; q < S; ++q) acc += red[q * O + oo];
+    const int t = oo / nD, col = da + oo % nD;
+    float* dst = P.out + (size_t)t * H + col;
+    *dst = P.block_mode ? __fadd_rn(oo < kRowThreads ? resid : *dst, acc) : acc;
+  }
+  if (tid == 0) sync->status[cta] = tail_timed_out || block_timed_out ? kStatusTimeout : 0;
 }
 
 // Per device, once per instance and shared-memory size: the kernel's dynamic

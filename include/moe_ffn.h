@@ -229,7 +229,9 @@ int moe_ffn_execute_static_scratch(moe_ffn_plan_t plan, moe_ffn_stream_t stream,
  * a condition that nothing ever satisfies: which = 0 an mbarrier phase that
  * never completes (the wait of a shared-memory copy that never lands), which
  * = 1 a workspace flag that never receives the value waited for (the decode
- * kernel's grid-wide barriers).  The wait gives up after its iteration cap, records
+ * kernel's grid-wide barriers), which = 2 a tagged workspace word that never
+ * carries the tag waited for (the decode kernel's poll of the partial
+ * outputs, T = 1).  The wait gives up after its iteration cap, records
  * MOE_FFN_ERR_TIMEOUT in the workspace status word (read it with
  * moe_ffn_read_status) and the kernel returns; the CUDA context stays usable
  * and the next execute on the workspace clears the word.  Returns a host-side

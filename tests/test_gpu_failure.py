@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.mark.parametrize("which", [0, 1])  # 0: an mbarrier phase that never completes; 1: a counter never reached
+# 0: an mbarrier phase that never completes; 1: a barrier flag that never receives the epoch; 2: a tagged word
+# that never carries the call's tag
+@pytest.mark.parametrize("which", [0, 1, 2])
 def test_bounded_wait_gives_up_and_context_stays_usable(which):
     import fusion_backend_gb300 as fb
     import oracle
@@ -52,7 +54,7 @@ def test_probe_rejects_bad_arguments():
     plan, ws_bytes = fb.moe_ffn_prepare(with_T(TINY, 1), ACT_F32, WFMT_BF16)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     with pytest.raises(fb.MoeFFNError) as e:
-        fb.moe_ffn_probe_timeout(plan, ws, 2)
+        fb.moe_ffn_probe_timeout(plan, ws, 3)
     assert e.value.status == fb.ERR_INVALID_ARG
     with pytest.raises(fb.MoeFFNError) as e:
         fb.moe_ffn_probe_timeout(plan, ws, 0, workspace_bytes=ws_bytes - 1)
