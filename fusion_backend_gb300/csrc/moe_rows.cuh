@@ -571,33 +571,28 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // ---- the activation (block form: x_res) and the workspace belong to this
   // kernel from here on
   pdl_wait();
+  // The activation (or x_res) of all tokens: one bulk copy per block into
+  // shared memory -- every block needs all of it, and one read per block
+  // keeps the L2 lines of x from being hammered by every warp of the grid.
+  // Issued first: nothing before it depends on it, and its latency covers
+  // the reads of the call's epoch.
+  const int src4 = P.act == 0 || P.block_mode;  // fp32 source rows
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)(T * H * (src4 ? 4 : 2));
+    mbar_arrive_expect_tx(xbar, bytes);
+    bulk_g2s(xs, P.x, bytes, xbar, policy_evict_last());
+  }
   RowSync* const sync = P.sync;
   const unsigned long long prev_epoch = __ldcg(&sync->epoch);
   const unsigned long long epoch = prev_epoch + 1ull;
   const bool fast_sync = __ldcg(&sync->sig) == ~prev_epoch;
   const uint32_t tag = (uint32_t)epoch;
   // tagged partials: kept in L2 (evict-last; rewritten every call, read
-  // within microseconds), and this block's words first get a tag that is not
-  // the call's -- the grid-wide barrier publishes that before any reader
-  // polls them
+  // within microseconds)
   const uint64_t pol_keep = policy_evict_last();
-  if constexpr (TAGGED) {
-    const unsigned long long stale = tagged(~tag, 0.f);
-    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
-    for (int i = 2 * tid; i < T * H; i += 2 * kRowThreads) st_relaxed_gpu_v2_u64(mine + i, stale, stale, pol_keep);
-  }
   if (cta == 0) {
     if (tid == 0) P.ctrl[kCtrlStatus] = 0u;  // a status left by the failure-path probe
     for (int c = P.G + tid; c < kMaxGrid; c += kRowThreads) sync->status[c] = 0;
-  }
-  // The activation (or x_res) of all tokens: one bulk copy per block into
-  // shared memory -- every block needs all of it, and one read per block
-  // keeps the L2 lines of x from being hammered by every warp of the grid.
-  const int src4 = P.act == 0 || P.block_mode;  // fp32 source rows
-  if (tid == 0) {
-    const uint32_t bytes = (uint32_t)(T * H * (src4 ? 4 : 2));
-    mbar_arrive_expect_tx(xbar, bytes);
-    bulk_g2s(xs, P.x, bytes, xbar, policy_evict_last());
   }
   bool timed_out = false;
   if (!mbar_wait(xbar, 0)) timed_out = true;
@@ -674,6 +669,14 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
       __syncthreads();
     }
+  }
+  // tagged partials: this block's words first get a tag that is not the
+  // call's -- the grid-wide barrier below publishes that before any reader
+  // polls them
+  if constexpr (TAGGED) {
+    const unsigned long long stale = tagged(~tag, 0.f);
+    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
+    for (int i = 2 * tid; i < T * H; i += 2 * kRowThreads) st_relaxed_gpu_v2_u64(mine + i, stale, stale, pol_keep);
   }
   // activation in its compute form, in place, while the other blocks finish
   // their logits.  Fast shapes: the bf16 A fragments of the tensor-core
