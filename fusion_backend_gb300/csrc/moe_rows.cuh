@@ -40,12 +40,15 @@
 // epoch (RowSync), so no workspace word has to be reset between calls.
 //
 // Tensor-core instances (H = 2048, bf16-exact activation): the stage loops
-// run on mma.m16n8k16 / m16n8k8 over the swizzled tensor-copy boxes.  With
-// 4-bit weights each code becomes the exact bf16 (code - 8) in registers (the
-// nibble OR-ed into the mantissa of bf16 128 reads 128 + n, minus 136), the
-// products of a 32-element block are summed on the tensor cores and scaled by
-// the block's fp16 scale in fp32, so no weight is rounded.  The general
-// instance decodes every weight to fp32 and uses CUDA-core FMAs.
+// run on mma.m16n8k16 / m16n8k8 over the swizzled tensor-copy boxes, one
+// block barrier per stage.  With 4-bit weights each code becomes the exact
+// bf16 (code - 8) in registers (the nibble OR-ed into the mantissa of bf16
+// 128 reads 128 + n, minus 136), the products of a 32-element block are
+// summed on the tensor cores and scaled by the block's fp16 scale in fp32, so
+// no weight is rounded.  With int8 weights the activation is quantised per
+// token and the codes of both operands enter fp16 products exactly, so the
+// gate and up dot products are exact integers.  The general instance decodes
+// every weight to fp32 and uses CUDA-core FMAs (int8: int32 dp4a).
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
