@@ -357,6 +357,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
+  constexpr bool I8MC = I8C && TMAX >= 4;       // int8: tensor-core down projection
+  constexpr bool QMC = Q4C || I8MC;             // the m16n8k8 down projection (yc4 accumulators)
   // One token: the partial outputs are words tagged with the call, polled by
   // the column sums (no second grid-wide barrier; see RowSync)
   constexpr bool TAGGED = TMAX == 1;
@@ -975,9 +977,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   float yc[MMA_C ? 16 : 1][4];  // tensor-core down projection: y of this warp's slice, D fragments
 #pragma unroll
   for (int j = 0; j < (MMA_C ? 16 : 1); ++j) yc[j][0] = yc[j][1] = yc[j][2] = yc[j][3] = 0.f;
-  float yc4[Q4C ? 16 : 1][4];  // 4-bit tensor-core down projection: y of this warp's slice, D fragments
+  float yc4[QMC ? 16 : 1][4];  // 4-bit / int8 tensor-core down projection: y of this warp's slice, D fragments
 #pragma unroll
-  for (int j = 0; j < (Q4C ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
+  for (int j = 0; j < (QMC ? 16 : 1); ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
 
   if constexpr (B16C) {
     // ---- tensor-core stage loop (bf16 weights, H = 2048, 4 rows a stage).
@@ -1415,6 +1417,37 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
         const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
         const float* hp = hb + (par ^ 1) * RSM * TMAX;
+        if constexpr (I8MC) {
+          // Four or more tokens: tensor cores, y[col][token] += Q^T (h s_down),
+          // one m16n8k8 step per 16-column tile with the stage's 8 rows as k
+          // (codes exact in bf16; h s_down as bf16 hi + lo).  Tile i of the
+          // 32-column block b holds columns 32b + 4g + 2i (A rows g) and + 1
+          // (rows g + 8) of the slice: this lane reads the 4 codes at 32b + 4g
+          // of rows 2q and 2q + 1, two tiles' worth.
+          const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
+          const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
+          const float v0 = h0 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq) * 16);
+          const float v1 = h1 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq + 1) * 16);
+          const uint32_t bh = pack_bf16(v0, v1);
+          const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int chunk = 2 * warp + (b >> 2), unit = 2 * (b & 3) + (gq >> 2), off = 4 * (gq & 3);
+            const int l0 = chunk * RS + 2 * qq;  // line & 7 = the row
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(dbox + (size_t)l0 * 128 + ((unit ^ (l0 & 7)) << 4) + off);
+            const uint32_t w1 =
+                *reinterpret_cast<const uint32_t*>(dbox + (size_t)(l0 + 1) * 128 + ((unit ^ ((l0 + 1) & 7)) << 4) + off);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              // (row 2q, row 2q + 1) of columns 2i and 2i + 1 of the four: bf16 of the exact float
+              const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
+              const uint32_t a1 =
+                  __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
+              mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
+              mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
+            }
+          }
+        } else {
 #pragma unroll
         for (int r = 0; r < kRsMaxQ4; ++r) {
           if (r < n_prev) {
@@ -1435,6 +1468,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
               for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(c, w[e], y[t][0][e]);
             }
           }
+        }
         }
       }
       n_prev = n;
@@ -1731,7 +1765,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         P.partial[((size_t)cta * T + t0 + 1) * H + c + 8] = yc[j][3];
       }
     }
-  } else if constexpr (Q4C) {
+  } else if constexpr (QMC) {
     // tile 2b + i: columns 256w + 32b + 4g + 2i (and + 1), tokens 2q (and + 1)
     const int g = lane >> 2, t0 = 2 * (lane & 3);
     unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
