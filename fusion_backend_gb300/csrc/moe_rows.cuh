@@ -357,8 +357,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
-  constexpr bool I8MC = I8C && TMAX >= 4;       // int8: tensor-core down projection
-  constexpr bool QMC = Q4C || I8MC;             // the m16n8k8 down projection (yc4 accumulators)
+  constexpr bool QMC = Q4C || I8C;              // the m16n8k8 down projection (yc4 accumulators)
   // One token: the partial outputs are words tagged with the call, polled by
   // the column sums (no second grid-wide barrier; see RowSync)
   constexpr bool TAGGED = TMAX == 1;
@@ -1309,8 +1308,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      8-row tiles.
     //   A2: g = float(sum of the 8 warps' integer partials) * x_scale * s in
     //      fp32 (the up rows alike), h = w silu(g) u.
-    //   C: CUDA cores, thread j owns columns 8j .. 8j + 7 and skips the
-    //      tokens the stage's group does not serve: y += (h s_down) q.
+    //   C: y[col][token] += Q^T (h s_down) on the tensor cores, m16n8k8
+    //      with the stage's 8 rows as k (as the 4-bit loop).
     // One block barrier per stage: after the barrier of stage s, A2 of stage
     // s and C of stage s - 1 run together (partials and h by stage parity),
     // so a downT slot is refilled one stage later than its gate + up slot.
@@ -1319,13 +1318,11 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     const int xh0 = 16 * (gq & 1), xh1 = 16 * ((gq & 1) ^ 1);  // the two halves of a unit (odd tokens swapped)
     const bool xon = gq < T;
     const int rr = lane & 7, mi = lane >> 3;  // ldmatrix: the row and the matrix (16-byte unit) this lane addresses
-    const int dchunk = tid >> 4, dunit = (tid & 15) >> 1, dhalf = tid & 1;
     StageCursor cs;
     cursor_init(cs, NS);
     int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
     uint32_t dph = 1u;
     int n_prev = 0;
-    uint32_t m_prev = 0u;
     for (int s = 0; s <= n_stages; ++s) {
       const int par = s & 1;
       int n = 0, su = -1;
@@ -1407,8 +1404,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
         hb[par * RSM * TMAX + j] = h;
       }
-      // -- C of stage s - 1.  Box lines: chunk * 8 + row; thread j's 8 codes
-      // are half j & 1 of 16-byte unit (j & 15) / 2 of chunk j / 16.
+      // -- C of stage s - 1.  Box lines: chunk * 8 + row.
       if (s >= 1) {
         if (++dslot == P.nsd) {
           dslot = 0;
@@ -1417,62 +1413,37 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
         const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
         const float* hp = hb + (par ^ 1) * RSM * TMAX;
-        if constexpr (I8MC) {
-          // Four or more tokens: tensor cores, y[col][token] += Q^T (h s_down),
-          // one m16n8k8 step per 16-column tile with the stage's 8 rows as k
-          // (codes exact in bf16; h s_down as bf16 hi + lo).  Tile i of the
-          // 32-column block b holds columns 32b + 4g + 2i (A rows g) and + 1
-          // (rows g + 8) of the slice: this lane reads the 4 codes at 32b + 4g
-          // of rows 2q and 2q + 1, two tiles' worth.
-          const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
-          const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
-          const float v0 = h0 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq) * 16);
-          const float v1 = h1 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq + 1) * 16);
-          const uint32_t bh = pack_bf16(v0, v1);
-          const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
+        // Tensor cores: y[col][token] += Q^T (h s_down), one m16n8k8 step
+        // per 16-column tile with the stage's 8 rows as k (codes exact in
+        // bf16; h s_down as bf16 hi + lo).  Tile i of the 32-column block b
+        // holds columns 32b + 4g + 2i (A rows g) and + 1 (rows g + 8) of the
+        // slice: this lane reads the 4 codes at 32b + 4g of rows 2q and
+        // 2q + 1, two tiles' worth.
+        const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
+        const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
+        const float v0 = h0 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq) * 16);
+        const float v1 = h1 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq + 1) * 16);
+        const uint32_t bh = pack_bf16(v0, v1);
+        const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
 #pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int chunk = 2 * warp + (b >> 2), unit = 2 * (b & 3) + (gq >> 2), off = 4 * (gq & 3);
-            const int l0 = chunk * RS + 2 * qq;  // line & 7 = the row
-            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(dbox + (size_t)l0 * 128 + ((unit ^ (l0 & 7)) << 4) + off);
-            const uint32_t w1 =
-                *reinterpret_cast<const uint32_t*>(dbox + (size_t)(l0 + 1) * 128 + ((unit ^ ((l0 + 1) & 7)) << 4) + off);
+        for (int b = 0; b < 8; ++b) {
+          const int chunk = 2 * warp + (b >> 2), unit = 2 * (b & 3) + (gq >> 2), off = 4 * (gq & 3);
+          const int l0 = chunk * RS + 2 * qq;  // line & 7 = the row
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(dbox + (size_t)l0 * 128 + ((unit ^ (l0 & 7)) << 4) + off);
+          const uint32_t w1 =
+              *reinterpret_cast<const uint32_t*>(dbox + (size_t)(l0 + 1) * 128 + ((unit ^ ((l0 + 1) & 7)) << 4) + off);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              // (row 2q, row 2q + 1) of columns 2i and 2i + 1 of the four: bf16 of the exact float
-              const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
-              const uint32_t a1 =
-                  __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
-              mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
-              mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
-            }
+          for (int i = 0; i < 2; ++i) {
+            // (row 2q, row 2q + 1) of columns 2i and 2i + 1 of the four: bf16 of the exact float
+            const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
+            const uint32_t a1 =
+                __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
+            mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
+            mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
           }
-        } else {
-#pragma unroll
-        for (int r = 0; r < kRsMaxQ4; ++r) {
-          if (r < n_prev) {
-            const int line = dchunk * RS + r;
-            const uint2 q = *reinterpret_cast<const uint2*>(dbox + (size_t)line * 128 + ((dunit ^ (line & 7)) << 4) + 8 * dhalf);
-            const float sd = *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)r * 16);
-            float w[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              w[e] = i8_f32(q.x, e);
-              w[e + 4] = i8_f32(q.y, e);
-            }
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (!(m_prev >> t & 1u)) continue;
-              const float c = hp[r * TMAX + t] * sd;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) y[t][0][e] = fmaf(c, w[e], y[t][0][e]);
-            }
-          }
-        }
         }
       }
       n_prev = n;
-      m_prev = s < n_stages ? (su < 0 ? all_tokens : tb.mask[su]) : 0u;
     }
   } else {
 
