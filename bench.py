@@ -58,7 +58,8 @@ NCU_TRAFFIC_BYTES = {("decode_bf16", 1): 83_757_568, ("decode_q4", 1): 23_651_32
 EXTRAS = [("decode_bf16", 8, 400, 20, 3.0), ("two_stream_bf16", 1, 400, 20, 0.0), ("two_stream_bf16", 8, 400, 20, 0.0),
           ("decode_q4", 1, 400, 20, 3.0), ("decode_q4", 2, 400, 20, 3.0),
           ("decode_q4", 4, 400, 20, 3.0), ("decode_q4", 8, 400, 20, 3.0), ("decode_i8", 1, 400, 20, 3.0),
-          ("decode_i8", 8, 400, 20, 3.0), ("batched_bf16", 64, 64, 5, 3.0),
+          ("decode_i8", 2, 400, 20, 3.0), ("decode_i8", 4, 400, 20, 3.0), ("decode_i8", 8, 400, 20, 3.0),
+          ("batched_bf16", 64, 64, 5, 3.0),
           ("batched_bf16", 256, 64, 5, 4.0), ("batched_q4", 64, 64, 5, 3.0), ("batched_q4", 256, 64, 5, 4.0),
           ("stack_q4", 1, 32, 3, 6.0)]
 
