@@ -6,6 +6,8 @@ lives here (tests may call the oracle, the generator may not).
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import datagen
@@ -19,6 +21,15 @@ DECODE = Shapes(T=1, H=2048, E=128, top_k=8, I=768, Is=512)
 SMALL_Q4 = Shapes(T=1, H=256, E=8, top_k=2, I=256, Is=256)
 
 NEAR_TIE_GAP = 1e-3
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> list[str]:
+    """The data lines of tests/golden/<name> (comment lines, starting with '#', skipped)."""
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.lstrip().startswith("#")]
 
 
 def with_T(s: Shapes, T: int) -> Shapes:

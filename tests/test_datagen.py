@@ -10,10 +10,14 @@ MASK = (1 << 64) - 1
 
 
 def test_splitmix64_published_sequence():
-    # splitmix64 started from state 0 (Steele, Lea and Flood 2014; Vigna's reference code).
+    # splitmix64 started from state 0 (tests/golden/splitmix64_state0.txt: Steele, Lea and Flood 2014; Vigna's
+    # reference code)
+    from tests.cases import golden
+
     L = datagen.lib()
-    got = [L.dg_mix64((GAMMA * i) & MASK) for i in (1, 2, 3)]
-    assert got == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    for row in golden("splitmix64_state0.txt"):
+        i, want = row.split()
+        assert L.dg_mix64((GAMMA * int(i)) & MASK) == int(want, 16), f"output {i}"
 
 
 def test_slices_regenerate_exactly():

@@ -393,19 +393,14 @@ def test_rmsnorm_matches_numpy():
 
 def test_float_to_bf16_rounds_ties_to_even():
     """bf16 keeps 8 significant bits.  Values exactly halfway between two bf16 neighbours go to the one with an
-    even last bit: 1 + 3*2^-8 (between 0x3F81 and 0x3F82) rounds up to 0x3F82, 1 + 2^-8 (between 0x3F80 and 0x3F81)
-    rounds down to 0x3F80; truncation would give 0x3F81 for the first, rounding half up 0x3F81 for the second."""
-    assert oracle.float_to_bf16(1.0 + 3 * 2.0**-8) == 0x3F82
-    assert oracle.float_to_bf16(1.0 + 2.0**-8) == 0x3F80
-    assert oracle.float_to_bf16(-(1.0 + 3 * 2.0**-8)) == 0xBF82
-    assert oracle.float_to_bf16(-(1.0 + 2.0**-8)) == 0xBF80
-    # just above a tie rounds up, just below rounds down
-    assert oracle.float_to_bf16(1.0 + 2.0**-8 + 2.0**-20) == 0x3F81
-    assert oracle.float_to_bf16(1.0 + 3 * 2.0**-8 - 2.0**-20) == 0x3F81
-    # exact values and the largest finite bf16
-    assert oracle.float_to_bf16(1.0 + 2.0**-7) == 0x3F81
-    assert oracle.float_to_bf16(3.4375) == 0x405C
-    assert oracle.float_to_bf16(float(np.float32(3.3895313892515355e38))) == 0x7F7F
+    even last bit (tests/golden/bf16_round_to_nearest_even.txt, worked from the bit patterns): truncation or
+    rounding half up each fail one of the tie rows."""
+    from tests.cases import golden
+
+    for row in golden("bf16_round_to_nearest_even.txt"):
+        f32_bits, bf16_bits = row.split()[:2]
+        v = float(np.array([int(f32_bits, 16)], np.uint32).view(np.float32)[0])
+        assert oracle.float_to_bf16(v) == int(bf16_bits, 16), row
 
 
 def test_rmsnorm_exact_ties_with_unit_factor():
@@ -419,13 +414,14 @@ def test_rmsnorm_exact_ties_with_unit_factor():
 
 
 def test_rmsnorm_eps_inside_the_root():
-    """x = 1e-3 everywhere: y = c / sqrt(c^2 + eps).  eps = 1e-6 gives 1/sqrt(2) = 0.7071 -> bf16 0x3F35;
-    eps = 1e-5 gives 0.3015 -> 0x3E9A; eps = 0 gives 1 -> 0x3F80.  eps added outside the root (c / (c + eps))
-    would give 0.999 -> 0x3F80, and eps scaled by H would give a value near 0.022."""
-    c = np.full(64, 1e-3, np.float32)
-    assert np.all(oracle.rmsnorm_bf16(c, eps=1e-6) == 0x3F35)
-    assert np.all(oracle.rmsnorm_bf16(c, eps=1e-5) == 0x3E9A)
-    assert np.all(oracle.rmsnorm_bf16(c, eps=0.0) == 0x3F80)
+    """x = 1e-3 everywhere: y = c / sqrt(c^2 + eps) (tests/golden/rmsnorm_eps.txt, worked by hand): the eps
+    values tell eps inside the root from eps outside it or scaled by H."""
+    from tests.cases import golden
+
+    for row in golden("rmsnorm_eps.txt"):
+        H, eps, want = row.split()
+        c = np.full(int(H), 1e-3, np.float32)
+        assert np.all(oracle.rmsnorm_bf16(c, eps=float(eps)) == int(want, 16)), row
 
 
 def test_block_step_is_norm_then_layer_then_residual():
@@ -445,17 +441,20 @@ def test_block_step_is_norm_then_layer_then_residual():
 
 
 def test_i8_activation_quantizer_known_values():
-    """max|x| = 127 gives the scale 127 / 127 = 1 exactly, so q is x rounded half away from zero."""
-    x = np.array([127.0, -63.5, 0.5, -0.5, 1.49, -1.5, 2.5, 0.0] + [3.0] * 8)
-    q, s = oracle.quantize_i8(x)
-    assert s == 1.0
-    assert list(q[:8]) == [127, -64, 1, -1, 1, -2, 3, 0]
-    # a scale that is not a power of two: max 1.0 -> 1/127 in fp32; 0.5 / s = 63.5 -> 64
-    q, s = oracle.quantize_i8(np.array([1.0, 0.5, -0.25, -1.0] + [0.0] * 12))
-    assert s == float(np.float32(1.0) / np.float32(127.0))
-    assert list(q[:4]) == [127, 64, -32, -127]
-    q, s = oracle.quantize_i8(np.zeros(16))
-    assert s == 0.0 and not q.any()
+    """tests/golden/int8_activation_quantizer.txt, worked by hand: max|x| = 127 gives the scale 127 / 127 = 1
+    exactly, so q is x rounded half away from zero; max|x| = 1 gives fp32(1/127) and 0.5 / s = 63.5 -> 64; a
+    zero row gives scale 0 and zero codes."""
+    from tests.cases import golden
+
+    for row in golden("int8_activation_quantizer.txt"):
+        xs, fill, codes, scale = [f.strip() for f in row.split("|")]
+        vals = [float(v) for v in xs.split(",")]
+        x = np.array(vals + [float(fill)] * (16 - len(vals)))
+        q, s = oracle.quantize_i8(x)
+        assert s == float(np.array([int(scale, 16)], np.uint32).view(np.float32)[0]), row
+        assert list(q[: len(vals)]) == [int(c) for c in codes.split(",")], row
+        if float(fill) == 0.0:
+            assert not q[len(vals):].any()
 
 
 def test_i8_weight_rows_decode():
