@@ -683,15 +683,16 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     for (int i = 2 * tid; i < T * H; i += 2 * kRowThreads) st_relaxed_gpu_v2_u64(mine + i, stale, stale, pol_keep);
   }
   // activation in its compute form, in place, while the other blocks finish
-  // their logits.  Fast shapes: the bf16 A fragments of the tensor-core
-  // loops, token t's row at t * kXPitch, 16 bytes per (warp slice w, 32-column
+  // their logits.  Fast shapes: the bf16 fragments of the tensor-core loops
+  // (A operand of the bf16 loop, B operand of the 4-bit loop; the same
+  // registers per lane), token t's row at t * kXPitch, 16 bytes per (warp slice w, 32-column
   // block kp, lane quad q) -- unit tid = (8w + kp) * 4 + q, the fragments of
   // steps 2kp and 2kp + 1.  Other shapes: fp32 rows.  All reads of the source
   // precede the barrier, all writes follow it.
   if constexpr (I8C) {
     // int8 loop: each token quantised as in the general loop (x_scale =
     // max|x| / 127 in fp32, codes round-half-away(x / x_scale) clamped to
-    // +-127), the codes as exact fp16 A fragments.  Unit U = (4w + b) * 4 + q
+    // +-127), the codes as exact fp16 B fragments.  Unit U = (4w + b) * 4 + q
     // of token t's row (32 bytes at 32 U) holds, for the 16-column steps i of
     // the 64-column block b of warp slice w, the pairs (x[c], x[c + 1]) and
     // (x[c + 2], x[c + 3]), c = 256w + 64b + 16i + 4q, i = 0..3; thread tid
@@ -1141,12 +1142,12 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     // 8 the 64 fp16 block scales.  Warp w owns the 256-column slice
     // [256w, 256w + 256) of H: nibble chunk w of every row, and the 8 block
     // scales in 16-byte unit w of chunk 8.
-    //   A: per 32-column block kp, D[token][row] = x . Q over the block
+    //   A: per 32-column block kp, D[row][token] = Q . x over the block
     //      (two m16n8k16 steps; Q = code - 8 is exact in bf16), then times
-    //      the row's block scale into fp32 accumulators; the gate rows and
-    //      the up rows are two 8-row tiles.  The k order inside a block
-    //      follows the nibble order of a 32-bit word, and the x fragments
-    //      follow it.
+    //      the row's block scale into fp32 accumulators; the 16 A rows are
+    //      the 8 gate rows and the 8 up rows, the B columns the tokens.  The
+    //      k order inside a block follows the nibble order of a 32-bit word,
+    //      and the x fragments follow it.
     //   A2: h = w silu(g) u from the 8 warps' partials.
     //   C: per block b of the slice, y[col][token] += Q^T (h d_b), one
     //      m16n8k8 step per 16-column tile with the stage's 8 rows as k;
@@ -1154,8 +1155,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      of block b holds columns 32b + 4g + 2i (rows g) and + 1 (rows
     //      g + 8) of the slice, g = 0..7.
     const int gq = lane >> 2, qq = lane & 3;
-    // x: the A fragments of token lane/4 (rows 8..15 zero) from the
-    // fragment rows in shared memory (nibble order), 16 bytes per block.
+    // x: the B fragments of token lane/4 from the fragment rows in shared
+    // memory (nibble order), 16 bytes per block.
     const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(32 * warp + qq) * 16;
     const bool xon = gq < T;
     // One block barrier per stage: after the barrier of stage s, A2 of stage
@@ -1176,51 +1177,49 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         int si0;
         rows_of(cs, si0, n);
         const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
-        // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
-        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [gate|up][row 2q + e], token lane/4
-        uint4 sc[2][2];  // block scales of rows 2q, 2q + 1 of the gate and up tiles
-        int lw[2];       // nibble chunk w, row lane/4 (the B column) of each tile
-#pragma unroll
-        for (int gu = 0; gu < 2; ++gu) {
-          const int l0 = (16 + gu) * kRsMaxQ4 + 2 * qq;  // scale chunk
-          sc[gu][0] = *reinterpret_cast<const uint4*>(sl + l0 * 128 + ((warp ^ (l0 & 7)) << 4));
-          sc[gu][1] = *reinterpret_cast<const uint4*>(sl + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
-          lw[gu] = (2 * warp + gu) * kRsMaxQ4 + gq;
-        }
+        // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.  The 16 A rows
+        // are the stage's 8 gate rows and its 8 up rows, the 8 B columns the
+        // tokens, so one m16n8k16 step covers both tiles.
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};  // D fragment: gate row g, tokens 2q, 2q + 1; up row g, the same tokens
+        const int lg = 16 * kRsMaxQ4 + gq, lu = 17 * kRsMaxQ4 + gq;  // scale lines of row g (line & 7 == g)
+        const uint4 sg = *reinterpret_cast<const uint4*>(sl + lg * 128 + ((warp ^ gq) << 4));
+        const uint4 su4 = *reinterpret_cast<const uint4*>(sl + lu * 128 + ((warp ^ gq) << 4));
+        const uint8_t* wgp = sl + (2 * warp * kRsMaxQ4 + gq) * 128 + 4 * qq;        // nibble chunk w, gate row g
+        const uint8_t* wup = sl + ((2 * warp + 1) * kRsMaxQ4 + gq) * 128 + 4 * qq;  // nibble chunk w, up row g
         // blocks in two halves of four (the scale words of a half picked once)
 #pragma unroll 1
         for (int kh = 0; kh < 2; ++kh) {
-          uint4 sh[2];  // (row 2q, row 2q + 1) scale words of blocks 4kh .. 4kh+3, per tile
-#pragma unroll
-          for (int gu = 0; gu < 2; ++gu)
-            sh[gu] = kh ? make_uint4(sc[gu][0].z, sc[gu][0].w, sc[gu][1].z, sc[gu][1].w)
-                        : make_uint4(sc[gu][0].x, sc[gu][0].y, sc[gu][1].x, sc[gu][1].y);
+          const uint32_t g01 = kh ? sg.z : sg.x, g23 = kh ? sg.w : sg.y;
+          const uint32_t u01 = kh ? su4.z : su4.x, u23 = kh ? su4.w : su4.y;
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             const int kp = 4 * kh + e4;
             const uint4 xv = xon ? *reinterpret_cast<const uint4*>(xrow + 64 * kp) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int gu = 0; gu < 2; ++gu) {
-              const uint32_t wq = *reinterpret_cast<const uint32_t*>(sl + lw[gu] * 128 + ((kp ^ (lw[gu] & 7)) << 4) + 4 * qq);
-              const uint32_t b0 = q4_pair_bf16(wq), b1 = q4_pair_bf16(wq >> 4);
-              const uint32_t b2 = q4_pair_bf16(wq >> 8), b3 = q4_pair_bf16(wq >> 12);
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16(d, xv.x, 0u, xv.y, 0u, b0, b1);
-              mma_bf16(d, xv.z, 0u, xv.w, 0u, b2, b3);
-              const uint32_t w0 = (e4 >> 1) ? sh[gu].y : sh[gu].x, w1 = (e4 >> 1) ? sh[gu].w : sh[gu].z;
-              const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (w0 >> 16) : (w0 & 0xFFFFu))));
-              const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (w1 >> 16) : (w1 & 0xFFFFu))));
-              acc[gu][0] = fmaf(s0, d[0], acc[gu][0]);
-              acc[gu][1] = fmaf(s1, d[1], acc[gu][1]);
-            }
+            const uint32_t wg = *reinterpret_cast<const uint32_t*>(wgp + ((kp ^ gq) << 4));
+            const uint32_t wu = *reinterpret_cast<const uint32_t*>(wup + ((kp ^ gq) << 4));
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(d, q4_pair_bf16(wg), q4_pair_bf16(wu), q4_pair_bf16(wg >> 4), q4_pair_bf16(wu >> 4), xv.x, xv.y);
+            mma_bf16(d, q4_pair_bf16(wg >> 8), q4_pair_bf16(wu >> 8), q4_pair_bf16(wg >> 12), q4_pair_bf16(wu >> 12),
+                     xv.z, xv.w);
+            const uint32_t gw = (e4 >> 1) ? g23 : g01, uw = (e4 >> 1) ? u23 : u01;
+            const float s_g = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (gw >> 16) : (gw & 0xFFFFu))));
+            const float s_u = __half2float(__ushort_as_half(static_cast<unsigned short>((e4 & 1) ? (uw >> 16) : (uw & 0xFFFFu))));
+            acc[0] = fmaf(s_g, d[0], acc[0]);
+            acc[1] = fmaf(s_g, d[1], acc[1]);
+            acc[2] = fmaf(s_u, d[2], acc[2]);
+            acc[3] = fmaf(s_u, d[3], acc[3]);
           }
         }
-        if (gq < TMAX) {
+        {
           float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
 #pragma unroll
-          for (int gu = 0; gu < 2; ++gu)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = acc[gu][e];
+          for (int e = 0; e < 2; ++e) {
+            const int t = 2 * qq + e;
+            if (t < TMAX) {
+              pw[gq * TMAX + t] = acc[e];
+              pw[(RSM + gq) * TMAX + t] = acc[2 + e];
+            }
+          }
         }
       }
       named_bar_sync(kBarStage, kRowThreads);
@@ -1298,14 +1297,14 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     // chunks, swizzled) and, after them, the stage rows' records.  Warp w
     // owns the 256-column slice [256w, 256w + 256) of H: code chunks 2w and
     // 2w + 1 of every row.
-    //   A: D[token][row] = qx . q over the slice, m16n8k16 on fp16 operands
+    //   A: D[row][token] = q . qx over the slice, m16n8k16 on fp16 operands
     //      (codes are exact in fp16; each product is exact in fp32, and every
     //      partial sum is an integer below 256 * 127^2 < 2^22, so the fp32
     //      accumulators hold the int32 dot product exactly); per 64-column
     //      block, one ldmatrix brings 4 codes of each stage row per lane for
     //      each of the block's four 16-column steps, and the x fragments use
-    //      the same column order.  The gate rows and the up rows are two
-    //      8-row tiles.
+    //      the same column order.  The 16 A rows are the 8 gate rows and the
+    //      8 up rows, the B columns the tokens.
     //   A2: g = float(sum of the 8 warps' integer partials) * x_scale * s in
     //      fp32 (the up rows alike), h = w silu(g) u.
     //   C: y[col][token] += Q^T (h s_down) on the tensor cores, m16n8k8
@@ -1336,35 +1335,38 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         rows_of(cs, si0, n);
         const uint8_t* sl = ring + (size_t)cs.slot * P.stage_bytes;
         // -- A.  Box lines: (chunk * 2 + matrix) * 8 + row.
-        float acc[2][4][4];  // [gate|up][step i of a block][D fragment]
+        // The 16 A rows are the stage's 8 gate rows and its 8 up rows, the 8
+        // B columns the tokens, so one m16n8k16 step covers both tiles.
+        float acc[4][4];  // [step i of a block][D: gate row g, tokens 2q, 2q + 1; up row g, the same tokens]
 #pragma unroll
-        for (int gu = 0; gu < 2; ++gu)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[gu][i][0] = acc[gu][i][1] = acc[gu][i][2] = acc[gu][i][3] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const uint4 xa = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh0) : make_uint4(0u, 0u, 0u, 0u);
           const uint4 xb = xon ? *reinterpret_cast<const uint4*>(xrow + 128 * b + xh1) : make_uint4(0u, 0u, 0u, 0u);
           const int chunk = 2 * warp + (b >> 1);
+          const int unit = (((b & 1) * 4 + mi) ^ rr) << 4;
+          uint32_t wg[4], wu[4];
+          ldmatrix_x4(wg, sl + (size_t)((chunk * 2) * 8 + rr) * 128 + unit);
+          ldmatrix_x4(wu, sl + (size_t)((chunk * 2 + 1) * 8 + rr) * 128 + unit);
 #pragma unroll
-          for (int gu = 0; gu < 2; ++gu) {
-            uint32_t wr[4];
-            ldmatrix_x4(wr, sl + (size_t)((chunk * 2 + gu) * 8 + rr) * 128 + ((((b & 1) * 4 + mi) ^ rr) << 4));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4& xv = i < 2 ? xa : xb;
-              const uint32_t a0 = (i & 1) ? xv.z : xv.x, a2 = (i & 1) ? xv.w : xv.y;
-              mma_f16(acc[gu][i], a0, 0u, a2, 0u, i8_pair_f16(wr[i], 0), i8_pair_f16(wr[i], 1));
-            }
+          for (int i = 0; i < 4; ++i) {
+            const uint4& xv = i < 2 ? xa : xb;
+            const uint32_t b0 = (i & 1) ? xv.z : xv.x, b1 = (i & 1) ? xv.w : xv.y;
+            mma_f16(acc[i], i8_pair_f16(wg[i], 0), i8_pair_f16(wu[i], 0), i8_pair_f16(wg[i], 1), i8_pair_f16(wu[i], 1),
+                    b0, b1);
           }
         }
-        if (gq < TMAX) {
+        {
           float* pw = part + (size_t)(par * kRowWarps + warp) * NV;
 #pragma unroll
-          for (int gu = 0; gu < 2; ++gu)
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              pw[(gu * RSM + 2 * qq + e) * TMAX + gq] = (acc[gu][0][e] + acc[gu][1][e]) + (acc[gu][2][e] + acc[gu][3][e]);
+          for (int e = 0; e < 2; ++e) {
+            const int t = 2 * qq + e;
+            if (t < TMAX) {
+              pw[gq * TMAX + t] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+              pw[(RSM + gq) * TMAX + t] = (acc[0][2 + e] + acc[1][2 + e]) + (acc[2][2 + e] + acc[3][2 + e]);
+            }
+          }
         }
         // the row scales of A2's value j, read before the slot is released
         if (j < n * TMAX) {
