@@ -40,7 +40,7 @@
 // epoch (RowSync), so no workspace word has to be reset between calls.
 //
 // Tensor-core instances (H = 2048, bf16-exact activation): the stage loops
-// run on mma.m16n8k16 / m16n8k8 over the swizzled tensor-copy boxes, one
+// run on mma.m16n8k16 over the swizzled tensor-copy boxes, one
 // block barrier per stage.  With 4-bit weights each code becomes the exact
 // bf16 (code - 8) in registers (the nibble OR-ed into the mantissa of bf16
 // 128 reads 128 + n, minus 136), the products of a 32-element block are
@@ -238,14 +238,6 @@ MOE_DEV void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// D += A B, m16n8k8, bf16 operands, fp32 accumulators (A row-major 16x8:
-// a0 rows lane/4, a1 rows lane/4 + 8, k pair 2(lane & 3); B k pair
-// 2(lane & 3) of column lane/4).
-MOE_DEV void mma_bf16_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
 // Two 4-bit codes (bits 0-3 and 16-19 of v) -> the bf16 pair (code - 8):
 // 0x4300 | n is the bf16 of 128 + n, and 128 + n - 136 is exact.
 MOE_DEV uint32_t q4_pair_bf16(uint32_t v) {
@@ -357,7 +349,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool MMA_C = B16C && TMAX >= 4;     // bf16: tensor-core down projection
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
-  constexpr bool QMC = Q4C || I8C;              // the m16n8k8 down projection (yc4 accumulators)
+  constexpr bool QMC = Q4C || I8C;              // the 8-row down projection (yc4 accumulators)
   // One token: the partial outputs are words tagged with the call, polled by
   // the column sums (no second grid-wide barrier; see RowSync)
   constexpr bool TAGGED = TMAX == 1;
@@ -1150,8 +1142,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      and the x fragments follow it.
     //   A2: h = w silu(g) u from the 8 warps' partials.
     //   C: per block b of the slice, y[col][token] += Q^T (h d_b), one
-    //      m16n8k8 step per 16-column tile with the stage's 8 rows as k;
-    //      h d_b enters as bf16 hi + lo, so y keeps fp32 accuracy.  Tile i
+    //      m16n8k16 step per 16-column tile whose k is the stage's 8 rows
+    //      twice: h d_b enters as bf16 hi (k 0..7) + lo (k 8..15), so y
+    //      keeps fp32 accuracy.  Tile i
     //      of block b holds columns 32b + 4g + 2i (rows g) and + 1 (rows
     //      g + 8) of the slice, g = 0..7.
     const int gq = lane >> 2, qq = lane & 3;
@@ -1187,7 +1180,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         const uint8_t* wgp = sl + (2 * warp * kRsMaxQ4 + gq) * 128 + 4 * qq;        // nibble chunk w, gate row g
         const uint8_t* wup = sl + ((2 * warp + 1) * kRsMaxQ4 + gq) * 128 + 4 * qq;  // nibble chunk w, up row g
         // blocks in two halves of four (the scale words of a half picked once)
-#pragma unroll 1
+#pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
           const uint32_t g01 = kh ? sg.z : sg.x, g23 = kh ? sg.w : sg.y;
           const uint32_t u01 = kh ? su4.z : su4.x, u23 = kh ? su4.w : su4.y;
@@ -1283,8 +1276,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const uint32_t a0 = q4_pair_bf16(X >> (8 * i)), a1 = q4_pair_bf16(X >> (8 * i + 4));
-            mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
-            mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
+            // k 0..7 the rows times the hi parts, k 8..15 the same rows times the lo parts
+            mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
           }
         }
       }
@@ -1307,8 +1300,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      8 up rows, the B columns the tokens.
     //   A2: g = float(sum of the 8 warps' integer partials) * x_scale * s in
     //      fp32 (the up rows alike), h = w silu(g) u.
-    //   C: y[col][token] += Q^T (h s_down) on the tensor cores, m16n8k8
-    //      with the stage's 8 rows as k (as the 4-bit loop).
+    //   C: y[col][token] += Q^T (h s_down) on the tensor cores, m16n8k16
+    //      with the stage's 8 rows twice as k (as the 4-bit loop).
     // One block barrier per stage: after the barrier of stage s, A2 of stage
     // s and C of stage s - 1 run together (partials and h by stage parity),
     // so a downT slot is refilled one stage later than its gate + up slot.
@@ -1415,9 +1408,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
         const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
         const float* hp = hb + (par ^ 1) * RSM * TMAX;
-        // Tensor cores: y[col][token] += Q^T (h s_down), one m16n8k8 step
-        // per 16-column tile with the stage's 8 rows as k (codes exact in
-        // bf16; h s_down as bf16 hi + lo).  Tile i of the 32-column block b
+        // Tensor cores: y[col][token] += Q^T (h s_down), one m16n8k16 step
+        // per 16-column tile with the stage's 8 rows twice as k (codes exact
+        // in bf16; h s_down as bf16 hi + lo).  Tile i of the 32-column block b
         // holds columns 32b + 4g + 2i (A rows g) and + 1 (rows g + 8) of the
         // slice: this lane reads the 4 codes at 32b + 4g of rows 2q and
         // 2q + 1, two tiles' worth.
@@ -1440,8 +1433,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
             const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
             const uint32_t a1 =
                 __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
-            mma_bf16_k8(yc4[2 * b + i], a0, a1, bh);
-            mma_bf16_k8(yc4[2 * b + i], a0, a1, bl);
+            // k 0..7 the rows times the hi parts, k 8..15 the same rows times the lo parts
+            mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
           }
         }
       }
