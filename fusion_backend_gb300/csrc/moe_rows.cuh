@@ -1732,21 +1732,25 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     }
   } else if constexpr (QMC) {
-    // tile 2b + i: columns 256w + 32b + 4g + 2i (and + 1), tokens 2q (and + 1)
+    // tiles 2b and 2b + 1: columns 256w + 32b + 4g .. + 3 (tile 2b + i holds
+    // + 2i and + 2i + 1), tokens 2q and 2q + 1 -- four consecutive columns
+    // of a token per lane and store
     const int g = lane >> 2, t0 = 2 * (lane & 3);
     unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int c = 256 * warp + 32 * (j >> 1) + 4 * g + 2 * (j & 1);
+    for (int b = 0; b < 8; ++b) {
+      const int c = 256 * warp + 32 * b + 4 * g;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         if (t0 + e >= T) continue;
-        if constexpr (TAGGED)
-          st_relaxed_gpu_v2_u64(mine + (size_t)(t0 + e) * H + c, tagged(tag, yc4[j][e]), tagged(tag, yc4[j][2 + e]),
-                                pol_keep);
-        else
-          *reinterpret_cast<float2*>(P.partial + ((size_t)cta * T + t0 + e) * H + c) =
-              make_float2(yc4[j][e], yc4[j][2 + e]);
+        if constexpr (TAGGED) {
+          unsigned long long* dst = mine + (size_t)(t0 + e) * H + c;
+          st_relaxed_gpu_v2_u64(dst, tagged(tag, yc4[2 * b][e]), tagged(tag, yc4[2 * b][2 + e]), pol_keep);
+          st_relaxed_gpu_v2_u64(dst + 2, tagged(tag, yc4[2 * b + 1][e]), tagged(tag, yc4[2 * b + 1][2 + e]), pol_keep);
+        } else {
+          *reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t0 + e) * H + c) =
+              make_float4(yc4[2 * b][e], yc4[2 * b][2 + e], yc4[2 * b + 1][e], yc4[2 * b + 1][2 + e]);
+        }
       }
     }
   } else {
@@ -1788,8 +1792,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   bool tail_timed_out = false;
   if constexpr (!TAGGED) tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
   // The O sums of G partials.  Thread (sp, o) adds partials sp, sp + S, ...
-  // in order, up to 16 loads in flight together; the S part sums are then
-  // added in order.
+  // in order, up to kSumBatch loads in flight together (fp32 partials: 48,
+  // so that with eight tokens on 152 blocks a thread's 76 partials take two
+  // rounds of L2 latency, not five); the S part sums are then added in order.
   bool sums_timed_out = false;
   const int S = O >= kRowThreads ? 1 : kRowThreads / max(O, 1);
   // The ring is idle now (every issued stage was waited on); reuse it.
@@ -1799,8 +1804,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     const int t = o / nD, col = da + o % nD;
     const size_t stride = (size_t)T * H;
     float acc = 0.f;
-    for (int c0 = sp; c0 < P.G; c0 += 16 * S) {
-      float v[16];
+    constexpr int kSumBatch = TAGGED ? 16 : 48;
+    for (int c0 = sp; c0 < P.G; c0 += kSumBatch * S) {
+      float v[kSumBatch];
       if constexpr (TAGGED) {
         const unsigned long long* src = reinterpret_cast<const unsigned long long*>(P.partial) + (size_t)t * H + col;
         const int n = min(16, (P.G - 1 - c0) / S + 1);
@@ -1808,13 +1814,13 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       } else {
         const float* src = P.partial + (size_t)t * H + col;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kSumBatch; ++q) {
           const int c = c0 + q * S;
           v[q] = c < P.G ? __ldcg(src + (size_t)c * stride) : 0.f;
         }
       }
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
+      for (int q = 0; q < kSumBatch; ++q)
         if (c0 + q * S < P.G) acc += v[q];
     }
     red[sp * O + o] = acc;
