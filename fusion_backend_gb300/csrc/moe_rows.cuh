@@ -1792,9 +1792,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   bool tail_timed_out = false;
   if constexpr (!TAGGED) tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
   // The O sums of G partials.  Thread (sp, o) adds partials sp, sp + S, ...
-  // in order, up to kSumBatch loads in flight together (fp32 partials: 48,
-  // so that with eight tokens on 152 blocks a thread's 76 partials take two
-  // rounds of L2 latency, not five); the S part sums are then added in order.
+  // in order, up to 16 loads in flight together; the S part sums are then
+  // added in order.
   bool sums_timed_out = false;
   const int S = O >= kRowThreads ? 1 : kRowThreads / max(O, 1);
   // The ring is idle now (every issued stage was waited on); reuse it.
@@ -1804,9 +1803,8 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     const int t = o / nD, col = da + o % nD;
     const size_t stride = (size_t)T * H;
     float acc = 0.f;
-    constexpr int kSumBatch = TAGGED ? 16 : 48;
-    for (int c0 = sp; c0 < P.G; c0 += kSumBatch * S) {
-      float v[kSumBatch];
+    for (int c0 = sp; c0 < P.G; c0 += 16 * S) {
+      float v[16];
       if constexpr (TAGGED) {
         const unsigned long long* src = reinterpret_cast<const unsigned long long*>(P.partial) + (size_t)t * H + col;
         const int n = min(16, (P.G - 1 - c0) / S + 1);
@@ -1814,13 +1812,13 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       } else {
         const float* src = P.partial + (size_t)t * H + col;
 #pragma unroll
-        for (int q = 0; q < kSumBatch; ++q) {
+        for (int q = 0; q < 16; ++q) {
           const int c = c0 + q * S;
           v[q] = c < P.G ? __ldcg(src + (size_t)c * stride) : 0.f;
         }
       }
 #pragma unroll
-      for (int q = 0; q < kSumBatch; ++q)
+      for (int q = 0; q < 16; ++q)
         if (c0 + q * S < P.G) acc += v[q];
     }
     red[sp * O + o] = acc;
