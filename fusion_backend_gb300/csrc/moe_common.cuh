@@ -159,6 +159,38 @@ MOE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory
 MOE_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// OR of v over the nthreads threads that meet at barrier id (all of them
+// execute this call).
+MOE_DEV bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+// Block-level barrier of the threads that run a kernel's whole path: every
+// thread of the block (NT == 0: barrier 0), or the first NT threads on
+// barrier kBarMain when the block has more threads with a role of their own.
+constexpr uint32_t kBarMain = 2;
+template <int NT>
+MOE_DEV void blk_sync() {
+  if constexpr (NT == 0)
+    __syncthreads();
+  else
+    named_bar_sync(kBarMain, NT);
+}
+template <int NT>
+MOE_DEV bool blk_sync_or(bool v) {
+  if constexpr (NT == 0)
+    return __syncthreads_or(v) != 0;
+  else
+    return named_bar_or(kBarMain, NT, v);
+}
 
 // ------------------------------------------------------- conversions
 MOE_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

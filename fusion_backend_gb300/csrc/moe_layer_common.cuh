@@ -71,9 +71,11 @@ MOE_DEV bool grid_flags_wait(const unsigned long long* flags, int G, unsigned lo
 // block has arrived, hence has read RowSync's epoch and sig) clears the next
 // call's counters and advances epoch and sig.  Returns false in every thread
 // of the block when a wait gave up (bounded, about a second).
+// NT: the threads of the block that take part (blk_sync).
+template <int NT = 0>
 MOE_DEV bool grid_barrier(RowSync* sy, int which, bool fast, int G, unsigned long long epoch, int cta, bool first) {
   const int tid = threadIdx.x, lane = tid & 31;
-  __syncthreads();
+  blk_sync<NT>();
   bool ok = true;
   uint32_t* count = &sy->count[epoch & 1][which];
   if (tid == 0) {
@@ -109,7 +111,7 @@ MOE_DEV bool grid_barrier(RowSync* sy, int which, bool fast, int G, unsigned lon
     __threadfence();
     sy->sig = ~epoch;
   }
-  return !__syncthreads_or(!ok);
+  return !blk_sync_or<NT>(!ok);
 }
 
 // Bounded poll of one thread on n <= N tagged words p[i * stride] (see
@@ -224,7 +226,8 @@ MOE_DEV void norm_factor_ff(float s, float c, int H, float eps, float& hi, float
 // block: warp w sums squares over its H/W slice of every row, the W pairs
 // of a row meet in shared memory (red[W][T][2]), and thread t < T combines
 // them error-free in warp order and writes inv[2t], inv[2t+1].  Ends with a
-// block barrier.
+// block barrier (of the NT threads that take part, blk_sync).
+template <int NT = 0>
 MOE_DEV void block_norm_factors(const float* x, int T, int H, float eps, float* red, float* inv, int W) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slice = (H / W + 3) & ~3;
@@ -237,7 +240,7 @@ MOE_DEV void block_norm_factors(const float* x, int T, int H, float eps, float* 
       red[(warp * T + t) * 2 + 1] = c;
     }
   }
-  __syncthreads();
+  blk_sync<NT>();
   if ((int)threadIdx.x < T) {
     const int t = threadIdx.x;
     float S = red[t * 2], C = red[t * 2 + 1];
@@ -252,7 +255,7 @@ MOE_DEV void block_norm_factors(const float* x, int T, int H, float eps, float* 
     inv[2 * t] = hi;
     inv[2 * t + 1] = lo;
   }
-  __syncthreads();
+  blk_sync<NT>();
 }
 
 // RMSNorm factor of one fp32 row by one warp (see block_norm_factors).

@@ -12,7 +12,8 @@
 // shared-expert gate s).  A block owns a contiguous run of units, so it needs
 // nothing from other blocks but the routing until its partial y is complete.
 //
-// One persistent block of 8 warps per SM (G blocks).  Before the wait on the
+// One persistent block of 8 warps (16 for the 4-bit and int8 tensor-core
+// loops) per SM (G blocks).  Before the wait on the
 // previous kernel (programmatic dependent launch; nothing produced by it is
 // read), each block loads its router row and issues the shared expert's
 // first stages -- weights are never written by a kernel that lets this one
@@ -47,8 +48,11 @@
 // summed on the tensor cores and scaled by the block's fp16 scale in fp32, so
 // no weight is rounded.  With int8 weights the activation is quantised per
 // token and the codes of both operands enter fp16 products exactly, so the
-// gate and up dot products are exact integers.  The general instance decodes
-// every weight to fp32 and uses CUDA-core FMAs (int8: int32 dp4a).
+// gate and up dot products are exact integers.  The 4-bit and int8 blocks
+// have 16 warps: warps 0..7 run the whole path except the down projection
+// of the stages, which warps 8..15 run beside them (rows_threads).  The
+// general instance decodes every weight to fp32 and uses CUDA-core FMAs
+// (int8: int32 dp4a).
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -82,7 +86,7 @@ struct RowTab {
   int32_t* active;   // [T*K] selected experts, ascending
   uint32_t* mask;    // [T*K] tokens of active expert u (bit t)
   float* wt;         // [T*K][T] weight of token t for active expert u (0 if not routed)
-  int32_t* misc;     // [4] the number of active experts U
+  int32_t* misc;     // [8] the number of active experts U; (split blocks) n_stages, first routed stage, call tag
   int32_t* qtab;     // [T*K - K + 1][4] per possible U: routed stages, first active expert, first group
   uint32_t* xmax;    // [T] int8 activation: bits of max |x| of token t
   float* xsc;        // [T] int8 activation: x_scale = max|x| / 127 of token t
@@ -90,7 +94,7 @@ struct RowTab {
 
 __host__ __device__ inline int row_tab(uint8_t* base, int T, int K, int E, RowTab* v) {
   const int TK = T * K;
-  const int sz[13] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 4 * 4,
+  const int sz[13] = {TK * 4, TK * 4, T * 4, 2 * T * 4, ((E + 31) / 32) * 4, E * 2, TK * 4, TK * 4, TK * T * 4, 8 * 4,
                       (TK - K + 1) * 16, T * 4, T * 4};
   int off = 0, o[13];
   for (int i = 0; i < 13; ++i) {
@@ -337,12 +341,18 @@ MOE_DEV void cursor_next(StageCursor& c, int n_sh, int u0, int g0, int gI, int n
   }
 }
 
+// Threads of a row-kernel block.  The 4-bit and int8 tensor-core instances
+// run 8 more warps that do only the stage loop's down projection (warps
+// 8..15), so that it runs beside the gate/up products of the first 8 warps.
+__host__ __device__ constexpr int rows_threads(int wk, bool fast) { return fast && wk != kWkBf16 ? 2 * kRowThreads : kRowThreads; }
+constexpr int kBarSplit = 3;  // named barrier: main and down-projection warps meet (start and end of the stages)
+
 // ------------------------------------------------------------------- kernel
 // TMAX: token capacity (T <= TMAX).  WK: weight kind (kWkBf16, kWkQ4,
 // kWkI8).  FAST: H = 2048, E <= 256 and a bf16-exact activation (the
 // tensor-core loops; bf16 and 4-bit weights).
 template <int TMAX, int WK, bool FAST, int NCH>
-__global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) {
+__global__ void __maxnreg__(rows_threads(WK, FAST) > kRowThreads ? 128 : 224) k_rows(const __grid_constant__ LayerParams Pk) {
   constexpr bool Q4 = WK == kWkQ4;
   constexpr bool I8 = WK == kWkI8;              // int8 weights and activation
   constexpr bool B16C = FAST && WK == kWkBf16;  // bf16 tensor-core loop
@@ -350,6 +360,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   constexpr bool Q4C = FAST && Q4;              // 4-bit tensor-core loop
   constexpr bool I8C = FAST && I8;              // int8 tensor-core loop
   constexpr bool QMC = Q4C || I8C;              // the 8-row down projection (yc4 accumulators)
+  // QMC: warps 8..15 do the down projection of every stage (see rows_threads)
+  constexpr int NTB = rows_threads(WK, FAST);             // threads of the block
+  constexpr int SYNC_NT = NTB > kRowThreads ? kRowThreads : 0;  // block barriers of warps 0..7 (blk_sync)
   // One token: the partial outputs are words tagged with the call, polled by
   // the column sums (no second grid-wide barrier; see RowSync)
   constexpr bool TAGGED = TMAX == 1;
@@ -476,6 +489,136 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   cursor_init(ci, NS);
   cursor_init(cd, P.nsd > 0 ? P.nsd : 1);
 
+  if constexpr (NTB > kRowThreads) {
+    if (warp >= kRowWarps) {
+      // ---- warps 8..15: the down projection of every stage.  Warp 8 + w
+      // owns the 256-column slice [256w, 256w + 256) of H.  They wait at
+      // kBarSplit until warps 0..7 have routed the call and issued the first
+      // copies, then meet them at the stage barrier n_stages + 1 times: after
+      // barrier s they refill the downT slot of stage s - 2 and project stage
+      // s - 1 with the h that A2 formed for it (h by stage parity).  At the
+      // end they store their partial y and meet warps 0..7 at kBarSplit once
+      // more (the OR of every wait's time-out).
+      const int w = warp - kRowWarps, gq = lane >> 2, qq = lane & 3;
+      const float* hb = reinterpret_cast<const float*>(sm + P.off_h);  // [2][kRsMaxQ4][TMAX]
+      bool h_timed_out = false;
+      named_bar_sync(kBarSplit, NTB);
+      n_stages = tb.misc[1];
+      ur0 = tb.misc[2];
+      gr0 = tb.misc[3];
+      const uint32_t tag = static_cast<uint32_t>(tb.misc[4]);
+      const uint64_t pol_keep = policy_evict_last();
+      for (int k = 0; k < min(n_stages, P.nsd); ++k) advance(cd, P.nsd);  // the copies warps 0..7 issued
+      StageCursor cc;  // the stage being projected
+      cursor_init(cc, 1);
+      int dslot = P.nsd - 1;  // its downT ring slot and phase parity
+      uint32_t dph = 1u;
+      float yc4[16][4];  // y of this warp's slice, D fragments (tiles 2b + i)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) yc4[j][0] = yc4[j][1] = yc4[j][2] = yc4[j][3] = 0.f;
+      for (int s = 0; s <= n_stages; ++s) {
+        named_bar_sync(kBarStage, NTB);
+        // C of stage s - 2 ended before this barrier: its downT slot is free
+        if (s >= 2 && s - 2 + P.nsd < n_stages) {
+          advance(cd, P.nsd);
+          if (tid == NTB - 1) issue_d(cd);
+        }
+        if (s == 0) continue;
+        advance(cc, 1);
+        int i0c, n_prev;
+        rows_of(cc, i0c, n_prev);
+        if (++dslot == P.nsd) {
+          dslot = 0;
+          dph ^= 1u;
+        }
+        if (!mbar_wait(&fulld[dslot], dph)) h_timed_out = true;
+        const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
+        const float* hp = hb + ((s - 1) & 1) * kRsMaxQ4 * TMAX;
+        // B: h times the row's scale for rows 2q, 2q + 1 (k) and token lane/4
+        // (n), as bf16 hi (k 0..7) + lo (k 8..15), so y keeps fp32 accuracy;
+        // A: the codes of the same rows, exact in bf16.  Tile i of the
+        // 32-column block b holds columns 32b + 4g + 2i (A rows g) and + 1
+        // (rows g + 8) of the slice: this lane reads the 4 codes at 32b + 4g
+        // of rows 2q and 2q + 1, two tiles' worth.
+        const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
+        const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
+        if constexpr (Q4) {
+          // box lines: chunk * 8 + row; chunk 8 holds the rows' block scales
+          const int l0 = 8 * kRsMaxQ4 + 2 * qq;
+          const uint4 s0 = *reinterpret_cast<const uint4*>(dbox + l0 * 128 + ((w ^ (l0 & 7)) << 4));
+          const uint4 s1 = *reinterpret_cast<const uint4*>(dbox + (l0 + 1) * 128 + ((w ^ ((l0 + 1) & 7)) << 4));
+          const int lr = w * kRsMaxQ4 + 2 * qq;  // nibble chunk w, row 2q
+          const uint8_t* r0p = dbox + lr * 128 + 2 * gq;
+          const uint8_t* r1p = dbox + (lr + 1) * 128 + 2 * gq;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const float v0 = h0 * half_at(s0, b), v1 = h1 * half_at(s1, b);
+            const uint32_t bh = pack_bf16(v0, v1);
+            const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
+            // codes of rows 2q, 2q + 1 at columns 32b + 4g .. + 3 of the slice
+            const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0p + ((b ^ (lr & 7)) << 4));
+            const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1p + ((b ^ ((lr + 1) & 7)) << 4));
+            const uint32_t X = u0 | (u1 << 16);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const uint32_t a0 = q4_pair_bf16(X >> (8 * i)), a1 = q4_pair_bf16(X >> (8 * i + 4));
+              mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
+            }
+          }
+        } else {
+          // box lines: chunk * 8 + row (16 chunks of codes), then the rows'
+          // 16-byte scale records
+          const float v0 = h0 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq) * 16);
+          const float v1 = h1 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq + 1) * 16);
+          const uint32_t bh = pack_bf16(v0, v1);
+          const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int chunk = 2 * w + (b >> 2), unit = 2 * (b & 3) + (gq >> 2), off = 4 * (gq & 3);
+            const int l0 = chunk * RS + 2 * qq;  // line & 7 = the row
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(dbox + (size_t)l0 * 128 + ((unit ^ (l0 & 7)) << 4) + off);
+            const uint32_t w1 =
+                *reinterpret_cast<const uint32_t*>(dbox + (size_t)(l0 + 1) * 128 + ((unit ^ ((l0 + 1) & 7)) << 4) + off);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              // (row 2q, row 2q + 1) of columns 2i and 2i + 1 of the four: bf16 of the exact float
+              const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
+              const uint32_t a1 =
+                  __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
+              mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
+            }
+          }
+        }
+      }
+      // ---- partial y of this block, this warp's slice
+      {
+        // tiles 2b and 2b + 1: columns 256w + 32b + 4g .. + 3 (tile 2b + i holds
+        // + 2i and + 2i + 1), tokens 2q and 2q + 1 -- four consecutive columns
+        // of a token per lane and store
+        const int g = lane >> 2, t0 = 2 * (lane & 3);
+        unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
+    #pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int c = 256 * w + 32 * b + 4 * g;
+    #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (t0 + e >= T) continue;
+            if constexpr (TAGGED) {
+              unsigned long long* dst = mine + (size_t)(t0 + e) * H + c;
+              st_relaxed_gpu_v2_u64(dst, tagged(tag, yc4[2 * b][e]), tagged(tag, yc4[2 * b][2 + e]), pol_keep);
+              st_relaxed_gpu_v2_u64(dst + 2, tagged(tag, yc4[2 * b + 1][e]), tagged(tag, yc4[2 * b + 1][2 + e]), pol_keep);
+            } else {
+              *reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t0 + e) * H + c) =
+                  make_float4(yc4[2 * b][e], yc4[2 * b][2 + e], yc4[2 * b + 1][e], yc4[2 * b + 1][2 + e]);
+            }
+          }
+        }
+      }
+      named_bar_or(kBarSplit, NTB, h_timed_out);
+      return;
+    }
+  }
+
   // ---- before the wait (nothing the previous kernel writes is read), side
   // by side: warp 0 initialises the barriers and issues the shared expert's
   // first stages (their weights do not depend on the previous kernel), warp 1
@@ -562,7 +705,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       wr[q] = (r_first <= P.E && c0 < H) ? *reinterpret_cast<const uint4*>(w + c0) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  __syncthreads();  // barriers initialised, tables cleared
+  blk_sync<SYNC_NT>();  // barriers initialised, tables cleared
 
   // ---- the activation (block form: x_res) and the workspace belong to this
   // kernel from here on
@@ -595,7 +738,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   // block form: RMSNorm factors of the fp32 rows, all warps (scratch: the
   // partials region, unused before the stage loop; ends with a barrier)
   if (P.block_mode)
-    block_norm_factors(reinterpret_cast<const float*>(xs), T, H, P.eps, reinterpret_cast<float*>(sm + P.off_part),
+    block_norm_factors<SYNC_NT>(reinterpret_cast<const float*>(xs), T, H, P.eps, reinterpret_cast<float*>(sm + P.off_part),
                        tb.inv, kRowWarps);
   // ---- router logits of this block's rows r = cta, cta + G, ... (<= E):
   // logit[t][r] = sum_h W[r,h] x_t[h], accumulated error-free (TwoSum of the
@@ -652,7 +795,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           red[(warp * TMAX + t) * 2 + 1] = ca[t];
         }
       }
-      __syncthreads();
+      blk_sync<SYNC_NT>();
       if (tid < T) {
         float S = red[tid * 2], C = red[tid * 2 + 1];
         for (int w = 1; w < kRowWarps; ++w) {
@@ -663,7 +806,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         }
         __stcg(P.logits + (size_t)tid * P.ls + r, __fadd_rn(S, C));
       }
-      __syncthreads();
+      blk_sync<SYNC_NT>();
     }
   }
   // tagged partials: this block's words first get a tag that is not the
@@ -712,7 +855,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
       if (lane == 0 && t < T) atomicMax(&tb.xmax[t], mw);
     }
-    __syncthreads();
+    blk_sync<SYNC_NT>();
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
       if (t < T) {
@@ -756,7 +899,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         }
       }
     }
-    __syncthreads();
+    blk_sync<SYNC_NT>();
 #pragma unroll
     for (int t = 0; t < TMAX; ++t)
       if (t < T) *reinterpret_cast<uint4*>(xs + (size_t)t * kXPitch + 16 * tid) = make_uint4(fr[t][0], fr[t][1], fr[t][2], fr[t][3]);
@@ -787,7 +930,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         }
       }
     }
-    __syncthreads();
+    blk_sync<SYNC_NT>();
     if constexpr (I8) {
       // token t's codes at xs + t H (bytes), its scale x_scale = max|x| / 127
       // in the routing tables: q = round-half-away(x / x_scale) clamped to
@@ -823,7 +966,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
   }
   // ---- every block's logits (first barrier; see RowSync)
-  if (!grid_barrier(sync, 0, fast_sync, P.G, epoch, cta, true)) timed_out = true;
+  if (!grid_barrier<SYNC_NT>(sync, 0, fast_sync, P.G, epoch, cta, true)) timed_out = true;
   // routing, every block from all logits: top-k of token t on warp 7 - t
   // (the chosen experts, their softmax weights and their bits in the
   // selection bitmap) and the shared gate sigmoid(logit_E)
@@ -858,7 +1001,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     }
   }
-  __syncthreads();
+  blk_sync<SYNC_NT>();
   if (TMAX > 1 && warp == 0 && P.part != 2) {
     // active experts in ascending order (active index u): bitmap word l on
     // lane l, an exclusive scan of the word counts
@@ -889,7 +1032,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     if (lane == 0) tb.misc[0] = U;
   }
-  if (TMAX > 1 && P.part != 2) __syncthreads();
+  if (TMAX > 1 && P.part != 2) blk_sync<SYNC_NT>();
   const int U = P.part == 2 ? 0 : tb.misc[0];
   if (P.part != 2) {
     const int32_t* q = tb.qtab + 4 * (U - K);
@@ -909,6 +1052,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
         advance(cd, P.nsd);
         if (tid == 32 * (j++ & (kRowWarps - 1))) issue_d(cd);
       }
+  }
+  if constexpr (NTB > kRowThreads) {
+    // warps 8..15 take the stage count, the first routed stage and the
+    // call's tag from here (they wait at kBarSplit since their start)
+    if (tid == 0) {
+      tb.misc[1] = n_stages;
+      tb.misc[2] = ur0;
+      tb.misc[3] = gr0;
+      tb.misc[4] = static_cast<int32_t>(tag);
+    }
+    named_bar_sync(kBarSplit, NTB);
   }
   if (cta == 0 && warp == kRowWarps - 1 && P.part != 2) {
     // routing outputs for the caller and the test readers: counts, offsets
@@ -1141,25 +1295,17 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      k order inside a block follows the nibble order of a 32-bit word,
     //      and the x fragments follow it.
     //   A2: h = w silu(g) u from the 8 warps' partials.
-    //   C: per block b of the slice, y[col][token] += Q^T (h d_b), one
-    //      m16n8k16 step per 16-column tile whose k is the stage's 8 rows
-    //      twice: h d_b enters as bf16 hi (k 0..7) + lo (k 8..15), so y
-    //      keeps fp32 accuracy.  Tile i
-    //      of block b holds columns 32b + 4g + 2i (rows g) and + 1 (rows
-    //      g + 8) of the slice, g = 0..7.
+    //   C (warps 8..15, q4_down_stage): the down projection.
     const int gq = lane >> 2, qq = lane & 3;
     // x: the B fragments of token lane/4 from the fragment rows in shared
     // memory (nibble order), 16 bytes per block.
     const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(32 * warp + qq) * 16;
     const bool xon = gq < T;
-    // One block barrier per stage: after the barrier of stage s, A2 of stage
-    // s and C of stage s - 1 run together (partials and h by stage parity),
-    // so a downT slot is refilled one stage later than its gate + up slot.
+    // One barrier of all 16 warps per stage: after the barrier of stage s,
+    // A2 of stage s runs here and C of stage s - 1 on warps 8..15 (partials
+    // and h by stage parity).  n_stages + 1 barriers, as warps 8..15 make.
     StageCursor cs;
     cursor_init(cs, NS);
-    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
-    uint32_t dph = 1u;
-    int n_prev = 0;
     for (int s = 0; s <= n_stages; ++s) {
       const int par = s & 1;
       int n = 0, su = -1;
@@ -1215,16 +1361,11 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           }
         }
       }
-      named_bar_sync(kBarStage, kRowThreads);
-      // every warp is done with this stage's gate + up box and (C of stage
-      // s - 2 ended before this barrier) with the downT box of stage s - 2
+      named_bar_sync(kBarStage, NTB);
+      // warps 0..7 are done with this stage's gate + up box
       if (s + NS < n_stages) {
         advance(ci, NS);
         if (tid == kRowThreads - 1) issue(ci);
-      }
-      if (s >= 2 && s - 2 + P.nsd < n_stages) {
-        advance(cd, P.nsd);
-        if (tid == kRowThreads - 1) issue_d(cd);
       }
       // -- A2 of stage s: value j = (row, token) = r * TMAX + t on thread j
       {
@@ -1246,42 +1387,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           hb[par * RSM * TMAX + j] = h;
         }
       }
-      // -- C of stage s - 1.  Box lines: chunk * 8 + row.
-      if (s >= 1) {
-        if (++dslot == P.nsd) {
-          dslot = 0;
-          dph ^= 1u;
-        }
-        if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-        const uint8_t* dbox = dring + (size_t)dslot * kRsMaxQ4 * rb;
-        const float* hp = hb + (par ^ 1) * RSM * TMAX;
-        // B: h d_b for rows 2q, 2q + 1 (k) and token lane/4 (n)
-        const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
-        const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
-        const int l0 = 8 * kRsMaxQ4 + 2 * qq;
-        const uint4 s0 = *reinterpret_cast<const uint4*>(dbox + l0 * 128 + ((warp ^ (l0 & 7)) << 4));
-        const uint4 s1 = *reinterpret_cast<const uint4*>(dbox + (l0 + 1) * 128 + ((warp ^ ((l0 + 1) & 7)) << 4));
-        const int lr = warp * kRsMaxQ4 + 2 * qq;  // nibble chunk w, row 2q
-        const uint8_t* r0p = dbox + lr * 128 + 2 * gq;
-        const uint8_t* r1p = dbox + (lr + 1) * 128 + 2 * gq;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const float v0 = h0 * half_at(s0, b), v1 = h1 * half_at(s1, b);
-          const uint32_t bh = pack_bf16(v0, v1);
-          const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
-          // codes of rows 2q, 2q + 1 at columns 32b + 4g .. + 3 of the slice
-          const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0p + ((b ^ (lr & 7)) << 4));
-          const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1p + ((b ^ ((lr + 1) & 7)) << 4));
-          const uint32_t X = u0 | (u1 << 16);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const uint32_t a0 = q4_pair_bf16(X >> (8 * i)), a1 = q4_pair_bf16(X >> (8 * i + 4));
-            // k 0..7 the rows times the hi parts, k 8..15 the same rows times the lo parts
-            mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
-          }
-        }
-      }
-      n_prev = n;
     }
   } else if constexpr (I8C) {
     // ---- tensor-core stage loop (int8 weights and activation, H = 2048, 8
@@ -1300,11 +1405,9 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     //      8 up rows, the B columns the tokens.
     //   A2: g = float(sum of the 8 warps' integer partials) * x_scale * s in
     //      fp32 (the up rows alike), h = w silu(g) u.
-    //   C: y[col][token] += Q^T (h s_down) on the tensor cores, m16n8k16
-    //      with the stage's 8 rows twice as k (as the 4-bit loop).
-    // One block barrier per stage: after the barrier of stage s, A2 of stage
-    // s and C of stage s - 1 run together (partials and h by stage parity),
-    // so a downT slot is refilled one stage later than its gate + up slot.
+    //   C (warps 8..15, i8_down_stage): y[col][token] += Q^T (h s_down) on
+    //      the tensor cores (as the 4-bit loop).
+    // One barrier of all 16 warps per stage (as the 4-bit loop).
     const int gq = lane >> 2, qq = lane & 3;
     const uint8_t* xrow = xs + (size_t)gq * kXPitch + (size_t)(512 * warp + 32 * qq);
     const int xh0 = 16 * (gq & 1), xh1 = 16 * ((gq & 1) ^ 1);  // the two halves of a unit (odd tokens swapped)
@@ -1312,9 +1415,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     const int rr = lane & 7, mi = lane >> 3;  // ldmatrix: the row and the matrix (16-byte unit) this lane addresses
     StageCursor cs;
     cursor_init(cs, NS);
-    int dslot = P.nsd - 1;  // downT ring slot and phase parity of the stage C works on
-    uint32_t dph = 1u;
-    int n_prev = 0;
     for (int s = 0; s <= n_stages; ++s) {
       const int par = s & 1;
       int n = 0, su = -1;
@@ -1368,16 +1468,11 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           s_up = *reinterpret_cast<const float*>(sl + (size_t)2 * RS * H + (size_t)(RS + r) * 16);
         }
       }
-      named_bar_sync(kBarStage, kRowThreads);
-      // every warp is done with this stage's gate + up box and (C of stage
-      // s - 2 ended before this barrier) with the downT box of stage s - 2
+      named_bar_sync(kBarStage, NTB);
+      // warps 0..7 are done with this stage's gate + up box
       if (s + NS < n_stages) {
         advance(ci, NS);
         if (tid == kRowThreads - 1) issue(ci);
-      }
-      if (s >= 2 && s - 2 + P.nsd < n_stages) {
-        advance(cd, P.nsd);
-        if (tid == kRowThreads - 1) issue_d(cd);
       }
       // -- A2 of stage s
       if (s < n_stages && j < n * TMAX) {
@@ -1399,46 +1494,6 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
           h = (tb.mask[su] >> t & 1u) ? tb.wt[su * T + t] * silu_mul(g, u) : 0.f;
         hb[par * RSM * TMAX + j] = h;
       }
-      // -- C of stage s - 1.  Box lines: chunk * 8 + row.
-      if (s >= 1) {
-        if (++dslot == P.nsd) {
-          dslot = 0;
-          dph ^= 1u;
-        }
-        if (!mbar_wait(&fulld[dslot], dph)) timed_out = true;
-        const uint8_t* dbox = dring + (size_t)dslot * P.dstage_bytes;
-        const float* hp = hb + (par ^ 1) * RSM * TMAX;
-        // Tensor cores: y[col][token] += Q^T (h s_down), one m16n8k16 step
-        // per 16-column tile with the stage's 8 rows twice as k (codes exact
-        // in bf16; h s_down as bf16 hi + lo).  Tile i of the 32-column block b
-        // holds columns 32b + 4g + 2i (A rows g) and + 1 (rows g + 8) of the
-        // slice: this lane reads the 4 codes at 32b + 4g of rows 2q and
-        // 2q + 1, two tiles' worth.
-        const float h0 = (2 * qq < n_prev && gq < TMAX) ? hp[(2 * qq) * TMAX + gq] : 0.f;
-        const float h1 = (2 * qq + 1 < n_prev && gq < TMAX) ? hp[(2 * qq + 1) * TMAX + gq] : 0.f;
-        const float v0 = h0 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq) * 16);
-        const float v1 = h1 * *reinterpret_cast<const float*>(dbox + (size_t)RS * H + (size_t)(2 * qq + 1) * 16);
-        const uint32_t bh = pack_bf16(v0, v1);
-        const uint32_t bl = pack_bf16(v0 - bf16_lo(bh), v1 - bf16_hi(bh));
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int chunk = 2 * warp + (b >> 2), unit = 2 * (b & 3) + (gq >> 2), off = 4 * (gq & 3);
-          const int l0 = chunk * RS + 2 * qq;  // line & 7 = the row
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(dbox + (size_t)l0 * 128 + ((unit ^ (l0 & 7)) << 4) + off);
-          const uint32_t w1 =
-              *reinterpret_cast<const uint32_t*>(dbox + (size_t)(l0 + 1) * 128 + ((unit ^ ((l0 + 1) & 7)) << 4) + off);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            // (row 2q, row 2q + 1) of columns 2i and 2i + 1 of the four: bf16 of the exact float
-            const uint32_t a0 = __byte_perm(__float_as_uint(i8_f32(w0, 2 * i)), __float_as_uint(i8_f32(w1, 2 * i)), 0x7632);
-            const uint32_t a1 =
-                __byte_perm(__float_as_uint(i8_f32(w0, 2 * i + 1)), __float_as_uint(i8_f32(w1, 2 * i + 1)), 0x7632);
-            // k 0..7 the rows times the hi parts, k 8..15 the same rows times the lo parts
-            mma_bf16(yc4[2 * b + i], a0, a1, a0, a1, bh, bl);
-          }
-        }
-      }
-      n_prev = n;
     }
   } else {
 
@@ -1707,7 +1762,13 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       if (s + 1 <= n_stages) step(std::integral_constant<int, 1>(), s + 1);
     }
   }
-  const bool block_timed_out = __syncthreads_or(timed_out);
+  // every issued copy has been waited on (or timed out); QMC: the down-projection
+  // warps meet the others here once more, after storing their partial y
+  bool block_timed_out;
+  if constexpr (NTB > kRowThreads)
+    block_timed_out = named_bar_or(kBarSplit, NTB, timed_out);
+  else
+    block_timed_out = __syncthreads_or(timed_out) != 0;
   if (block_timed_out && tid == 0) {
     // leave no copy in flight into this block's shared memory: wait (bounded)
     // once more for the last stages issued
@@ -1732,27 +1793,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
       }
     }
   } else if constexpr (QMC) {
-    // tiles 2b and 2b + 1: columns 256w + 32b + 4g .. + 3 (tile 2b + i holds
-    // + 2i and + 2i + 1), tokens 2q and 2q + 1 -- four consecutive columns
-    // of a token per lane and store
-    const int g = lane >> 2, t0 = 2 * (lane & 3);
-    unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int c = 256 * warp + 32 * b + 4 * g;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (t0 + e >= T) continue;
-        if constexpr (TAGGED) {
-          unsigned long long* dst = mine + (size_t)(t0 + e) * H + c;
-          st_relaxed_gpu_v2_u64(dst, tagged(tag, yc4[2 * b][e]), tagged(tag, yc4[2 * b][2 + e]), pol_keep);
-          st_relaxed_gpu_v2_u64(dst + 2, tagged(tag, yc4[2 * b + 1][e]), tagged(tag, yc4[2 * b + 1][2 + e]), pol_keep);
-        } else {
-          *reinterpret_cast<float4*>(P.partial + ((size_t)cta * T + t0 + e) * H + c) =
-              make_float4(yc4[2 * b][e], yc4[2 * b][2 + e], yc4[2 * b + 1][e], yc4[2 * b + 1][2 + e]);
-        }
-      }
-    }
+    // stored by warps 8..15 (qmc_store_partial)
   } else {
     unsigned long long* mine = reinterpret_cast<unsigned long long*>(P.partial) + (size_t)cta * T * H;
 #pragma unroll
@@ -1790,7 +1831,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
   float resid = 0.f;
   if (P.block_mode && tid < O) resid = __ldcg(P.out + (size_t)(tid / nD) * H + da + tid % nD);
   bool tail_timed_out = false;
-  if constexpr (!TAGGED) tail_timed_out = !grid_barrier(sync, 1, fast_sync, P.G, epoch, cta, false);
+  if constexpr (!TAGGED) tail_timed_out = !grid_barrier<SYNC_NT>(sync, 1, fast_sync, P.G, epoch, cta, false);
   // The O sums of G partials.  Thread (sp, o) adds partials sp, sp + S, ...
   // in order, up to 16 loads in flight together; the S part sums are then
   // added in order.
@@ -1823,7 +1864,7 @@ __global__ void __maxnreg__(224) k_rows(const __grid_constant__ LayerParams Pk) 
     }
     red[sp * O + o] = acc;
   }
-  if (__syncthreads_or(sums_timed_out)) tail_timed_out = true;
+  if (blk_sync_or<SYNC_NT>(sums_timed_out)) tail_timed_out = true;
   for (int oo = tid; oo < O; oo += kRowThreads) {
     float acc = red[oo];
     for (int q = 1; q < S; ++q) acc += red[q * O + oo];
@@ -1857,7 +1898,7 @@ inline cudaError_t rows_configure(int smem, int G) {
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0, sms = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, smem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, rows_threads(WK, FAST), smem);
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
@@ -1878,7 +1919,7 @@ inline cudaError_t launch_rows_t(const LayerParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(kRowThreads);
+  cfg.blockDim = dim3(rows_threads(WK, FAST));
   cfg.dynamicSmemBytes = p.smem;
   return cudaLaunchKernelEx(&cfg, k_rows<TMAX, WK, FAST, NCH>, p);
 }
