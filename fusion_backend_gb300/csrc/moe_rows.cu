@@ -8,7 +8,7 @@
 
 namespace moe {
 
-static_assert(kWkBf16 == MOE_FFN_W_BF16 && kWkQ4 == MOE_FFN_W_Q4B32 && kWkI8 == MOE_FFN_W_I8,
+static_assert(int(kWkBf16) == int(MOE_FFN_W_BF16) && int(kWkQ4) == int(MOE_FFN_W_Q4B32) && int(kWkI8) == int(MOE_FFN_W_I8),
               "weight kinds follow the public weight formats");
 
 cudaError_t launch_rows_bf16_fast(const LayerParams& p, cudaStream_t stream);

@@ -1528,6 +1528,7 @@ __global__ void __maxnreg__(rows_threads(WK, FAST) > kRowThreads ? 128 : 224) k_
         uint32_t wgq[Q4 ? RSM : 1][NCH], wuq[Q4 ? RSM : 1][NCH];
         uint16_t sgq[Q4 ? RSM : 1][NCH], suq[Q4 ? RSM : 1][NCH];
         uint2 wgi[I8 ? RSM : 1][NCH], wui[I8 ? RSM : 1][NCH];
+        (void)wgb, (void)wub, (void)wgq, (void)wuq, (void)sgq, (void)suq, (void)wgi, (void)wui;  // one kind is used
         if constexpr (I8) {
           // the scale after each row's H codes
           if (warp == 0 && lane < 3 * RSM) {
