@@ -146,3 +146,23 @@ def test_two_stream_workspace_query(lib):
         fb.moe_ffn_query(plan, fb.QUERY_TWO_STREAM_WORKSPACE)
     assert e.value.status == fb.ERR_UNSUPPORTED
     fb.moe_ffn_destroy(plan)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: without the built library every entry of the binding raises, naming the file."""
+    import subprocess
+    import sys
+
+    code = (
+        "import fusion_backend_gb300 as fb\n"
+        f"fb.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "try:\n"
+        "    fb.moe_ffn_prepare(fb.Shapes(1, 256, 8, 2, 128, 256), fb.ACT_F32, fb.W_BF16)\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', e)\n"
+        "else:\n"
+        "    print('no error')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "raised:" in r.stdout and "absent.so" in r.stdout, r.stdout
