@@ -52,7 +52,7 @@ STACK_LAYERS = 48
 PREROLL_S = 0.15  # GPU work enqueued right before each timed region (clock samples under load, full launch queue)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel from the committed ncu
 # captures (profiles/), per (config, T); None until captured for the current kernel.
-NCU_TRAFFIC_BYTES = {("decode_bf16", 1): 83_746_304, ("batched_q4", 256): 238_398_464}
+NCU_TRAFFIC_BYTES = {("batched_q4", 256): 238_398_464}
 # Extra workloads measured in the default N=1 run: (config, T, steps, warm-up steps, oracle budget in s)
 EXTRAS = [("decode_bf16", 8, 400, 20, 3.0), ("two_stream_bf16", 1, 400, 20, 0.0), ("two_stream_bf16", 8, 400, 20, 0.0),
           ("decode_q4", 1, 400, 20, 3.0), ("decode_q4", 2, 400, 20, 3.0),
